@@ -1,0 +1,175 @@
+"""Depthwise-convolution oracle: plain, slow, obviously correct CPU code.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package.  The library
+(``depthwise_convolution_gb300``) never imports it and shares no code with it.
+
+Contents
+--------
+``fwd`` / ``dgrad`` / ``wgrad``
+    The definition of the operator and of its two training passes written out
+    as direct loops in C (``dwconv_oracle.c``), float64 for floating-point data
+    and int64 for integer data, threaded over channel ranges.  Each returns the
+    result and the per-element magnitude ``mag`` (sum of |products| plus |bias|)
+    that the parity tolerance scales with.
+``forms``
+    Independent second forms used only to pin the direct loops: the
+    per-channel im2col GEMV (Flash-DWC §2.1, Fig. 1), the tiled form with
+    partial sums carried across tiles ("Tiles, halos and partial sums"), the
+    gather form of dgrad, and the literal 180-degree-rotation form of the
+    stride-1 dgrad (Flash-DWC §5.1).
+``pages``
+    The arithmetic the pages print: halo extents, storage budgets, the GEMM
+    traffic model, and the Flash-DWC tile-model closed forms.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against values
+the pages print, closed forms, special cases and brute force; none is left
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dwconv_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (no -march flags, no FP contraction)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            lib = ctypes.CDLL(path)
+            L, I, P = ctypes.c_long, ctypes.c_int, ctypes.c_void_p
+            for name in ("dwo_fwd_f64", "dwo_fwd_i64"):
+                fn = getattr(lib, name)
+                fn.argtypes = [L] * 9 + [P, P, P, P, P, I]
+                fn.restype = I
+            for name in ("dwo_dgrad_f64", "dwo_dgrad_i64", "dwo_wgrad_f64", "dwo_wgrad_i64"):
+                fn = getattr(lib, name)
+                fn.argtypes = [L] * 9 + [P, P, P, P, I]
+                fn.restype = I
+            lib.dwo_out_extent.argtypes = [L] * 5
+            lib.dwo_out_extent.restype = L
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    """Host threads the oracle uses: the cores this process may run on."""
+    return len(os.sched_getaffinity(0))
+
+
+def out_extent(X: int, F: int, S: int, D: int, P: int) -> int:
+    """floor((X + 2P - D(F-1) - 1)/S) + 1, the floor convention of the oracle."""
+    return int(_load().dwo_out_extent(X, F, S, D, P))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _prep(a, integer):
+    dt = np.int64 if integer else np.float64
+    return np.ascontiguousarray(a, dtype=dt)
+
+
+def _is_integer(*arrays) -> bool:
+    kinds = {np.asarray(a).dtype.kind for a in arrays if a is not None}
+    if kinds <= {"i", "u"}:
+        return True
+    if kinds & {"i", "u"}:
+        raise TypeError("mixing integer and floating-point operands")
+    return False
+
+
+def fwd(x, w, bias=None, stride=1, dilation=1, pad=0, nthreads=None):
+    """Forward DWC.  x [N,H,W,C], w [FH,FW,C], bias [C] or None.
+
+    Returns (y [N,OH,OW,C], mag [N,OH,OW,C]) in float64 or int64.
+    """
+    integer = _is_integer(x, w, bias)
+    x, w = _prep(x, integer), _prep(w, integer)
+    b = None if bias is None else _prep(bias, integer)
+    N, H, W, C = x.shape
+    FH, FW, Cw = w.shape
+    if Cw != C or (b is not None and b.shape != (C,)):
+        raise ValueError("channel mismatch")
+    OH, OW = out_extent(H, FH, stride, dilation, pad), out_extent(W, FW, stride, dilation, pad)
+    if OH <= 0 or OW <= 0:
+        raise ValueError("empty output")
+    y = np.empty((N, OH, OW, C), dtype=x.dtype)
+    mag = np.empty_like(y)
+    fn = _load().dwo_fwd_i64 if integer else _load().dwo_fwd_f64
+    rc = fn(N, H, W, C, FH, FW, stride, dilation, pad, _ptr(x), _ptr(w), _ptr(b), _ptr(y),
+            _ptr(mag), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle fwd rejected the arguments (code {rc})")
+    return y, mag
+
+
+def dgrad(dy, w, H, W, stride=1, dilation=1, pad=0, nthreads=None):
+    """Input gradient (adjoint scatter).  dy [N,OH,OW,C] -> (dx [N,H,W,C], mag)."""
+    integer = _is_integer(dy, w)
+    dy, w = _prep(dy, integer), _prep(w, integer)
+    N, OH, OW, C = dy.shape
+    FH, FW, Cw = w.shape
+    if Cw != C:
+        raise ValueError("channel mismatch")
+    if (out_extent(H, FH, stride, dilation, pad), out_extent(W, FW, stride, dilation, pad)) != (OH, OW):
+        raise ValueError("dy shape does not match the forward output of an H x W input")
+    dx = np.empty((N, H, W, C), dtype=dy.dtype)
+    mag = np.empty_like(dx)
+    fn = _load().dwo_dgrad_i64 if integer else _load().dwo_dgrad_f64
+    rc = fn(N, H, W, C, FH, FW, stride, dilation, pad, _ptr(dy), _ptr(w), _ptr(dx), _ptr(mag),
+            nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle dgrad rejected the arguments (code {rc})")
+    return dx, mag
+
+
+def wgrad(x, dy, FH, FW, stride=1, dilation=1, pad=0, nthreads=None):
+    """Weight gradient.  x [N,H,W,C], dy [N,OH,OW,C] -> (dw [FH,FW,C], mag)."""
+    integer = _is_integer(x, dy)
+    x, dy = _prep(x, integer), _prep(dy, integer)
+    N, H, W, C = x.shape
+    if (out_extent(H, FH, stride, dilation, pad), out_extent(W, FW, stride, dilation, pad)) != dy.shape[1:3]:
+        raise ValueError("dy shape does not match the forward output")
+    if dy.shape[0] != N or dy.shape[3] != C:
+        raise ValueError("batch/channel mismatch")
+    dw = np.empty((FH, FW, C), dtype=x.dtype)
+    mag = np.empty_like(dw)
+    fn = _load().dwo_wgrad_i64 if integer else _load().dwo_wgrad_f64
+    rc = fn(N, H, W, C, FH, FW, stride, dilation, pad, _ptr(x), _ptr(dy), _ptr(dw), _ptr(mag),
+            nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle wgrad rejected the arguments (code {rc})")
+    return dw, mag
+
+
+from . import forms, pages  # noqa: E402  (pure-Python helpers, no C needed)
+
+__all__ = ["build", "fwd", "dgrad", "wgrad", "out_extent", "default_threads", "forms", "pages"]
