@@ -1,0 +1,419 @@
+"""Benchmark: one training step of a depthwise convolution layer on GB300.
+
+A step is the whole hot path -- forward, input gradient (dgrad) and weight
+gradient (wgrad) -- over one batch of the fp16 7x7 workload
+(x[128,56,56,96], w[7,7,96], dy[128,56,56,96], pad 3).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+value     nominal GFLOP/s (2*N*OH*OW*C*FH*FW per pass, three passes) over the
+          timed steps, inputs resident in HBM, L2 flushed between steps; summed
+          over ranks (each rank runs its own batch: weak scaling, no exchange).
+e2e       the same metric with host (pinned) buffers: each step copies x, w, dy
+          to the device and y, dx, dw back, inside the timed region.
+roofline  for the pass that takes the most time: valid-tap flops per launch over
+          its CUDA-event duration, against the fp32 FMA peak derived from the
+          SM count and maximum SM clock (the passes run on the FMA pipe).
+cpu_baseline  the oracle (float64 direct loops) timed on this host's cores on a
+          bounded sample of the same workload (rank 0, N=1 only).
+--impl reference  times that oracle alone, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from depthwise_convolution_gb300 import accounting, ops, synthetic  # noqa: E402
+
+DEFAULT_WORKLOAD = "fp16-train-7x7-128x56x56x96"
+METRIC = "DWC fwd/dgrad/wgrad GFLOP/s and HBM GB/s as % of roofline on 1xGB300"
+L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2, written between timed steps
+FMA_LANES_PER_SM = 128              # fp32 FMA units per SM on Blackwell
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    out = {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        out.update({"hbm_gbs": float(m["hbm_gbs"]), "sm_max_mhz": float(m.get("sm_max_mhz", 2070.0)),
+                    "source": "measured"})
+    return out
+
+
+def csrc_sha():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "depthwise_convolution_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, pass_name):
+    """DRAM bytes per launch from a committed ncu summary, if its kernels are current."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if "=" in line:
+                k, v = (t.strip() for t in line.split("=", 1))
+                kv[k] = v
+    if kv.get("csrc_sha") != csrc_sha():
+        return None
+    v = kv.get(f"{pass_name}_dram_bytes")
+    return float(v) if v else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [p for (t, p) in self.samples if t0 <= t <= t1] or [p for (_, p) in self.samples]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][1]) if rows[0][1].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- workload
+
+class Layer:
+    """Device buffers and the three calls of one workload."""
+
+    def __init__(self, wl, rank=0, device="cuda"):
+        self.wl = wl
+        a = wl.shape_args()
+        self.OH, self.OW = ops.dwconv_output_size(wl.H, wl.W, wl.FH, wl.FW, wl.stride, wl.dilation, wl.pad)
+        seeded = dataclasses.replace(wl, seed=wl.seed + 1000 * rank)
+        d = synthetic.make_inputs(seeded, dy_hw=(self.OH, self.OW) if "dgrad" in wl.passes or
+                                  "wgrad" in wl.passes else None)
+        self.host = d
+        self.x = d["x"].to(device)
+        self.w = d["w"].to(device)
+        self.bias = None if d["bias"] is None else d["bias"].to(device)
+        self.dy = None if d["dy"] is None else d["dy"].to(device)
+        N, H, W, C = wl.N, wl.H, wl.W, wl.C
+        ydt = torch.int32 if wl.dtype == "int8" else self.x.dtype
+        self.y = torch.empty((N, self.OH, self.OW, C), dtype=ydt, device=device)
+        self.dx = torch.empty((N, H, W, C), dtype=self.x.dtype, device=device) if "dgrad" in wl.passes else None
+        self.dw = torch.empty((wl.FH, wl.FW, C), dtype=torch.float32, device=device) if "wgrad" in wl.passes else None
+        ws = ops.dwconv_bwd_filter_workspace_size(*a, self.x.dtype) if "wgrad" in wl.passes else 0
+        self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=device)
+        self.nominal = accounting.nominal_flops(*a)
+        self.valid = accounting.valid_flops(*a)
+
+    def run_pass(self, name, stream=None):
+        wl = self.wl
+        if name == "fwd":
+            ops.dwconv_fwd(self.x, self.w, self.bias, wl.stride, wl.dilation, wl.pad, out=self.y, stream=stream)
+        elif name == "dgrad":
+            ops.dwconv_bwd_data(self.dy, self.w, wl.H, wl.W, wl.stride, wl.dilation, wl.pad, out=self.dx,
+                                stream=stream)
+        else:
+            ops.dwconv_bwd_filter(self.x, self.dy, wl.FH, wl.FW, wl.stride, wl.dilation, wl.pad, out=self.dw,
+                                  workspace=self.ws, stream=stream)
+
+    def unique(self, name):
+        return accounting.unique_bytes(name, self.wl.dtype, *self.wl.shape_args(), bias=self.bias is not None)
+
+
+def time_layer(layer, steps, warmup, flush):
+    """Per-pass CUDA-event times (ms) over `steps` steps, L2 flushed before each."""
+    passes = layer.wl.passes
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for p in passes:
+            layer.run_pass(p)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)] for _ in range(steps)]
+    launches0 = ops.dwconv_launch_count()
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        for j, p in enumerate(passes):
+            layer.run_pass(p)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    launches = ops.dwconv_launch_count() - launches0
+    per_pass = {p: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)] for j, p in enumerate(passes)}
+    step_ms = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)]
+    return step_ms, per_pass, launches
+
+
+def time_e2e(layer, steps):
+    """Steps through host buffers: H2D of the inputs, the passes, D2H of the results."""
+    h = {}
+    for k in ("x", "w", "dy"):
+        t = getattr(layer, k)
+        if t is not None:
+            h[k] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(layer.host[k])
+    outs = {k: getattr(layer, k) for k in ("y", "dx", "dw") if getattr(layer, k) is not None}
+    ho = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in ho.values())
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        for k, t in h.items():
+            getattr(layer, k).copy_(t, non_blocking=True)
+        for p in layer.wl.passes:
+            layer.run_pass(p)
+        for k, t in ho.items():
+            t.copy_(outs[k], non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+# ------------------------------------------------------------ cpu baseline
+
+def oracle_sample(wl, target_s=12.0, max_images=None):
+    """Time the oracle's passes on the first n images of the workload; n grows
+    until one measurement takes about target_s.  Returns (GFLOP/s, cores, sample)."""
+    import oracle
+    from depthwise_convolution_gb300 import synthetic as syn
+    cores = oracle.default_threads()
+    OH = accounting.out_extent(wl.H, wl.FH, wl.stride, wl.dilation, wl.pad)
+    OW = accounting.out_extent(wl.W, wl.FW, wl.stride, wl.dilation, wl.pad)
+    limit = wl.N if max_images is None else min(wl.N, max_images)
+    n = 1
+    while True:
+        sub = wl.with_batch(n)
+        d = syn.make_inputs(sub, dy_hw=(OH, OW) if wl.passes != ("fwd",) else None)
+        f = {k: (None if v is None else v.to(torch.float64 if wl.dtype != "int8" else torch.int64).numpy())
+             for k, v in d.items()}
+        t0 = time.perf_counter()
+        for p in wl.passes:
+            if p == "fwd":
+                oracle.fwd(f["x"], f["w"], f["bias"], wl.stride, wl.dilation, wl.pad)
+            elif p == "dgrad":
+                oracle.dgrad(f["dy"], f["w"], wl.H, wl.W, wl.stride, wl.dilation, wl.pad)
+            else:
+                oracle.wgrad(f["x"], f["dy"], wl.FH, wl.FW, wl.stride, wl.dilation, wl.pad)
+        dt = time.perf_counter() - t0
+        flops = len(wl.passes) * accounting.nominal_flops(*sub.shape_args())
+        if dt >= target_s * 0.5 or n >= limit:
+            return flops / dt / 1e9, cores, f"{'+'.join(wl.passes)} on {n} of {wl.N} images ({dt:.1f} s)"
+        n = min(limit, max(n + 1, int(n * target_s / max(dt, 1e-3))))
+
+
+def run_reference(args, ws, rank):
+    wl = synthetic.WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    vals = []
+    sample = ""
+    cores = 0
+    for _ in range(max(args.warmup, 0)):
+        oracle_sample(wl, target_s=0.5, max_images=2)
+    for _ in range(args.steps):
+        v, cores, sample = oracle_sample(wl, target_s=3.0, max_images=8)
+        vals.append(v)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "passes": list(wl.passes), "oracle": "float64 direct loops"},
+            "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "own" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    pk = peaks()
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    fma_peak_tflops = sms * FMA_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+
+    wl = synthetic.WORKLOADS[args.workload]
+    layer = Layer(wl, rank=rank)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    step_ms, per_pass, launches = time_layer(layer, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if ws > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+
+    ms = statistics.mean(step_ms)
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    step_flops = layer.nominal * len(wl.passes)
+    value = ws * step_flops / (ms * 1e-3) / 1e9
+
+    passes = {}
+    for p in wl.passes:
+        t_ms = statistics.mean(per_pass[p])
+        ub = layer.unique(p)
+        t_roof = max(layer.valid / (fma_peak_tflops * 1e12), ub / (pk["hbm_gbs"] * 1e9))
+        passes[p] = {"ms": round(t_ms, 4), "ms_median": round(statistics.median(per_pass[p]), 4),
+                     "gflops_nominal": round(layer.nominal / t_ms / 1e6, 1),
+                     "gflops_valid": round(layer.valid / t_ms / 1e6, 1),
+                     "gbs_unique": round(ub / t_ms / 1e6, 1),
+                     "roofline_frac": round(t_roof / (t_ms * 1e-3), 4)}
+    dom = max(passes, key=lambda p: passes[p]["ms"])
+    achieved = layer.valid / (passes[dom]["ms"] * 1e-3) / 1e12
+    roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(fma_peak_tflops, 2),
+                "unit": "TFLOP/s", "frac": round(achieved / fma_peak_tflops, 4),
+                "traffic": recorded_traffic(wl.name, dom), "kernel": f"{dom} ({wl.name})",
+                "peak_source": f"derived: {sms} SMs x {FMA_LANES_PER_SM} fp32 FMA lanes x 2 flop x "
+                               f"{pk['sm_max_mhz']:.0f} MHz (max SM clock)",
+                "flops_per_launch": layer.valid,
+                "hbm_peak_gbs": pk["hbm_gbs"], "hbm_peak_source": pk["source"]}
+
+    e2e_ms, h2d, d2h = time_e2e(layer, max(10, args.steps // 10))
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": round(ws * step_flops / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    sweep = {}
+    if rank == 0 and ws == 1 and not args.no_sweep:
+        for name, other in synthetic.WORKLOADS.items():
+            if name == wl.name:
+                continue
+            try:
+                lay = Layer(other)
+                s_ms, pp, _ = time_layer(lay, max(20, args.steps // 10), 3, flush)
+                entry = {"ms_per_step": round(statistics.mean(s_ms), 4)}
+                for p in other.passes:
+                    t_ms = statistics.mean(pp[p])
+                    ub = lay.unique(p)
+                    t_roof = max(lay.valid / (fma_peak_tflops * 1e12), ub / (pk["hbm_gbs"] * 1e9))
+                    entry[p] = {"ms": round(t_ms, 4), "gflops_nominal": round(lay.nominal / t_ms / 1e6, 1),
+                                "gbs_unique": round(ub / t_ms / 1e6, 1),
+                                "roofline_frac": round(t_roof / (t_ms * 1e-3), 4)}
+                sweep[name] = entry
+                del lay
+            except Exception as e:  # report, do not hide
+                sweep[name] = {"error": str(e)[:200]}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        v, cores, sample = oracle_sample(wl)
+        cpu = {"value": round(v, 3), "unit": "GFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "storage": wl.dtype, "passes": list(wl.passes),
+                       "N": wl.N, "H": wl.H, "W": wl.W, "C": wl.C, "FH": wl.FH, "FW": wl.FW,
+                       "stride": wl.stride, "dilation": wl.dilation, "pad": wl.pad,
+                       "l2": "flushed before each timed step (256 MiB write)",
+                       "parallelism": f"{ws} independent replica(s)"},
+            "passes": passes, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+            "clocks": sampler.summary(t0, t1), "cpu_baseline": cpu, "sweep": sweep}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,109 @@
+// Internal declarations shared by the libdwconv translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dwconv.h"
+
+namespace dwc {
+
+// Problem geometry after validation.  H, W, C are input sizes; OH, OW the
+// forward output sizes (floor convention).
+struct Shape {
+    int N, H, W, C, FH, FW, S, D, P, OH, OW;
+};
+
+// Counts kernel launches for dwconv_launch_count().
+void note_launches(int n);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// ---- element access --------------------------------------------------------
+
+// Two adjacent channels of one storage type, widened to / narrowed from float2.
+template <typename T> struct Pair;
+
+template <> struct Pair<float> {
+    static __device__ __forceinline__ float2 load(const float *p) {
+        return *reinterpret_cast<const float2 *>(p);
+    }
+    static __device__ __forceinline__ void store(float *p, float2 v) {
+        *reinterpret_cast<float2 *>(p) = v;
+    }
+};
+
+template <> struct Pair<__half> {
+    static __device__ __forceinline__ float2 load(const __half *p) {
+        return __half22float2(*reinterpret_cast<const __half2 *>(p));
+    }
+    static __device__ __forceinline__ void store(__half *p, float2 v) {
+        *reinterpret_cast<__half2 *>(p) = __float22half2_rn(v);
+    }
+};
+
+template <> struct Pair<__nv_bfloat16> {
+    static __device__ __forceinline__ float2 load(const __nv_bfloat16 *p) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float2 v) {
+        *reinterpret_cast<__nv_bfloat162 *>(p) = __float22bfloat162_rn(v);
+    }
+};
+
+// Scalar widening / rounding (round to nearest even for 16-bit outputs).
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// ---- launchers (each returns the launch's cudaError_t) -----------------------
+
+// Direct kernels: any shape, any dtype the pass supports; one thread per output.
+cudaError_t launch_fwd_direct(const Shape &s, dwconv_dtype dt, const void *x, const void *w,
+                              const void *bias, void *y, cudaStream_t st);
+cudaError_t launch_dgrad_direct(const Shape &s, dwconv_dtype dt, const void *dy, const void *w,
+                                void *dx, cudaStream_t st);
+// wgrad, first pass: partial sums over Z slices of the N*OH*OW axis into
+// part[Z][FH*FW][C]; second pass: fixed-order sum over the Z slices into dw.
+cudaError_t launch_wgrad_direct(const Shape &s, dwconv_dtype dt, const void *x, const void *dy,
+                                float *part, int Z, cudaStream_t st);
+cudaError_t launch_wgrad_reduce(const float *part, int Z, long long count, float *dw,
+                                cudaStream_t st);
+
+// Register-tiled kernels for small filters (the whole filter of a channel pair
+// held in registers).  The sub-grid description lets one kernel serve the
+// forward pass (including stride = dilation cases that read one phase of the
+// input) and the phase-decomposed input gradient.
+struct TiledConv {
+    const void *in;        // x (forward) or dy (input gradient)
+    const void *w;
+    const float *bias;     // nullable; forward only
+    void *out;             // y or dx
+    int N, C;
+    int FH, FW;
+    int flip;              // 1: filter rotated by 180 degrees
+    // Input tensor [N][Hf][Wf][C]; taps read its sub-grid
+    //   (in_off + in_step*i, in_off + in_step*j), 0 <= i < Hs, 0 <= j < Ws.
+    int Hf, Wf, Hs, Ws, in_step, in_off;
+    int pad_h, pad_w;      // sub-grid input row of output row i, tap fh: i - pad_h + fh (cols alike)
+    // Output tensor [N][OHf][OWf][C]; computed element (i, j) of the OHs x OWs
+    // grid goes to (out_off + out_step*i, out_off + out_step*j).  With
+    // zero_phases, the other positions of each out_step x out_step block are
+    // written with zeros.
+    int OHf, OWf, OHs, OWs, out_step, out_off, zero_phases;
+};
+
+// Returns cudaErrorNotSupported when no tiled instance covers the request.
+cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
+
+}  // namespace dwc

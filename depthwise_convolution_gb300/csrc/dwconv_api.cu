@@ -1,0 +1,241 @@
+// C ABI of libdwconv: argument validation, shape math, kernel selection.
+//
+// Every entry point validates all arguments on the host before it touches
+// the CUDA runtime, so a rejected call enqueues nothing (and needs no GPU).
+#include <atomic>
+#include <climits>
+
+#include "common.cuh"
+
+namespace dwc {
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+}  // namespace
+
+void note_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    int v = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        g_sm_count[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+namespace {
+
+long long floor_div(long long a, long long b) {  // b > 0
+    long long q = a / b;
+    if ((a % b != 0) && (a < 0)) --q;
+    return q;
+}
+
+long long out_extent(long long X, long long F, long long S, long long D, long long P) {
+    return floor_div(X + 2 * P - D * (F - 1) - 1, S) + 1;
+}
+
+int gcd(int a, int b) {
+    while (b) {
+        int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+// Validates sizes and fills the shape (OH, OW >= 1).  Elements per tensor are
+// bounded so that every offset fits comfortably in 64-bit arithmetic.
+dwconv_status make_shape(int N, int H, int W, int C, int FH, int FW, int S, int D, int P, Shape &s) {
+    if (N <= 0 || H <= 0 || W <= 0 || C <= 0 || FH <= 0 || FW <= 0 || S <= 0 || D <= 0 || P < 0)
+        return DWCONV_ERR_INVALID_ARG;
+    const long long OH = out_extent(H, FH, S, D, P), OW = out_extent(W, FW, S, D, P);
+    if (OH < 1 || OW < 1 || OH > INT_MAX || OW > INT_MAX) return DWCONV_ERR_INVALID_ARG;
+    const long long limit = 1LL << 40;
+    if ((long long)N * H * W > limit / C || (long long)N * OH * OW > limit / C ||
+        (long long)FH * FW > limit / C)
+        return DWCONV_ERR_INVALID_ARG;
+    s = Shape{N, H, W, C, FH, FW, S, D, P, (int)OH, (int)OW};
+    return DWCONV_OK;
+}
+
+bool valid_dtype(dwconv_dtype dt) { return dt >= DWCONV_INT8 && dt <= DWCONV_BF16; }
+
+size_t elem_size(dwconv_dtype dt) {
+    switch (dt) {
+        case DWCONV_INT8: return 1;
+        case DWCONV_FP32: return 4;
+        default: return 2;
+    }
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+dwconv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DWCONV_OK : DWCONV_ERR_CUDA; }
+
+// Tiled kernels stage 16-byte copies of 32-channel slabs and store channel
+// pairs: they need every pixel row to be a whole number of 16-byte copies.
+bool tiled_layout_ok(const Shape &s, dwconv_dtype dt, const void *in, const void *out, const void *w) {
+    if (dt == DWCONV_INT8) return false;
+    const size_t es = elem_size(dt);
+    if ((s.C * es) % 16 != 0) return false;
+    return aligned(in, 16) && aligned(out, 2 * es) && aligned(w, 2 * es);
+}
+
+// wgrad split: slices of the N*OH*OW axis.  A pure function of the shape so
+// that the workspace size can be computed without a device.
+int wgrad_slices(const Shape &s) {
+    const long long positions = (long long)s.N * s.OH * s.OW;
+    const long long per_slice_blocks = (long long)((s.C + 31) / 32) * s.FH * s.FW;
+    long long z = (1216 + per_slice_blocks - 1) / per_slice_blocks;  // ~8 blocks per SM
+    long long zmax = positions / 256;                                 // >= 256 positions a slice
+    if (zmax < 1) zmax = 1;
+    if (z > zmax) z = zmax;
+    if (z > 4096) z = 4096;
+    if (z < 1) z = 1;
+    return (int)z;
+}
+
+}  // namespace
+}  // namespace dwc
+
+using namespace dwc;
+
+extern "C" {
+
+dwconv_status dwconv_output_size(int H, int W, int FH, int FW, int stride, int dilation, int pad,
+                                 int *OH, int *OW) {
+    Shape s;
+    dwconv_status st = make_shape(1, H, W, 1, FH, FW, stride, dilation, pad, s);
+    if (st != DWCONV_OK) return st;
+    if (OH) *OH = s.OH;
+    if (OW) *OW = s.OW;
+    return DWCONV_OK;
+}
+
+const char *dwconv_status_string(dwconv_status status) {
+    switch (status) {
+        case DWCONV_OK: return "DWCONV_OK";
+        case DWCONV_ERR_INVALID_ARG: return "DWCONV_ERR_INVALID_ARG: invalid size, pointer or workspace";
+        case DWCONV_ERR_UNSUPPORTED: return "DWCONV_ERR_UNSUPPORTED: dtype not provided for this pass";
+        case DWCONV_ERR_MISALIGNED: return "DWCONV_ERR_MISALIGNED: pointer not aligned to its element size";
+        case DWCONV_ERR_CUDA: return "DWCONV_ERR_CUDA: a CUDA call or kernel launch failed";
+        case DWCONV_ERR_TIMEOUT: return "DWCONV_ERR_TIMEOUT: a bounded device wait gave up";
+        default: return "unknown dwconv_status";
+    }
+}
+
+unsigned long long dwconv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride, int dilation,
+                         int pad, dwconv_dtype dtype, const void *x, const void *w,
+                         const void *bias, void *y, dwconv_stream stream) {
+    if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
+    Shape s;
+    dwconv_status st = make_shape(N, H, W, C, FH, FW, stride, dilation, pad, s);
+    if (st != DWCONV_OK) return st;
+    if (!x || !w || !y) return DWCONV_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    const size_t bs = 4;  // int32 (int8 data) or float bias
+    const size_t ys = dtype == DWCONV_INT8 ? 4 : es;
+    if (!aligned(x, es) || !aligned(w, es) || !aligned(y, ys) || (bias && !aligned(bias, bs)))
+        return DWCONV_ERR_MISALIGNED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+
+    // Taps read the input rows oh*S - P + fh*D.  With g = gcd(S, D) they all lie
+    // in one residue class r0 = (-P) mod g, so the pass is a stride S/g,
+    // dilation D/g convolution over that sub-grid.  Unit stride and dilation
+    // on the sub-grid go to the tiled kernel (this covers the stride-2,
+    // dilation-2 layer, which reads only even rows and columns).
+    const int g = gcd(stride, dilation);
+    const int r0 = (int)((g - pad % g) % g);
+    if (stride / g == 1 && dilation / g == 1 && tiled_layout_ok(s, dtype, x, y, w) && H > r0 && W > r0) {
+        TiledConv p{};
+        p.in = x; p.w = w; p.bias = static_cast<const float *>(bias); p.out = y;
+        p.N = N; p.C = C; p.FH = FH; p.FW = FW; p.flip = 0;
+        p.Hf = H; p.Wf = W; p.in_step = g; p.in_off = r0;
+        p.Hs = (H - r0 + g - 1) / g; p.Ws = (W - r0 + g - 1) / g;
+        p.pad_h = p.pad_w = (pad + r0) / g;
+        p.OHf = s.OH; p.OWf = s.OW; p.OHs = s.OH; p.OWs = s.OW;
+        p.out_step = 1; p.out_off = 0; p.zero_phases = 0;
+        cudaError_t e = launch_tiled_small(p, dtype, cs);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
+    return cuda_status(launch_fwd_direct(s, dtype, x, w, bias, y, cs));
+}
+
+dwconv_status dwconv_bwd_data(int N, int H, int W, int C, int FH, int FW, int stride,
+                              int dilation, int pad, dwconv_dtype dtype, const void *dy,
+                              const void *w, void *dx, dwconv_stream stream) {
+    if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
+    Shape s;
+    dwconv_status st = make_shape(N, H, W, C, FH, FW, stride, dilation, pad, s);
+    if (st != DWCONV_OK) return st;
+    if (dtype == DWCONV_INT8) return DWCONV_ERR_UNSUPPORTED;
+    if (!dy || !w || !dx) return DWCONV_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (!aligned(dy, es) || !aligned(w, es) || !aligned(dx, es)) return DWCONV_ERR_MISALIGNED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+
+    // When S divides D, every tap of input row ih satisfies ih = S*i + ph with
+    // ph = (-P) mod S, and dx on that phase is a unit-stride convolution of dy
+    // with the filter rotated by 180 degrees (Flash-DWC §5.1, generalised from
+    // S = 1), dilation D/S and padding (FH-1)*D/S - (ph+P)/S; every other
+    // phase receives no tap and is written as zero.
+    if (dilation % stride == 0 && dilation / stride == 1 && tiled_layout_ok(s, dtype, dy, dx, w)) {
+        const int S = stride;
+        const int ph = (S - pad % S) % S;
+        const int q = (ph + pad) / S;
+        TiledConv p{};
+        p.in = dy; p.w = w; p.bias = nullptr; p.out = dx;
+        p.N = N; p.C = C; p.FH = FH; p.FW = FW; p.flip = 1;
+        p.Hf = s.OH; p.Wf = s.OW; p.Hs = s.OH; p.Ws = s.OW; p.in_step = 1; p.in_off = 0;
+        p.pad_h = (FH - 1) * (dilation / S) - q;
+        p.pad_w = (FW - 1) * (dilation / S) - q;
+        p.OHf = H; p.OWf = W;
+        p.OHs = (H + S - 1) / S; p.OWs = (W + S - 1) / S;
+        p.out_step = S; p.out_off = ph; p.zero_phases = S > 1 ? 1 : 0;
+        cudaError_t e = launch_tiled_small(p, dtype, cs);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
+    return cuda_status(launch_dgrad_direct(s, dtype, dy, w, dx, cs));
+}
+
+size_t dwconv_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW, int stride,
+                                        int dilation, int pad, dwconv_dtype dtype) {
+    Shape s;
+    if (!valid_dtype(dtype) || dtype == DWCONV_INT8) return 0;
+    if (make_shape(N, H, W, C, FH, FW, stride, dilation, pad, s) != DWCONV_OK) return 0;
+    return (size_t)wgrad_slices(s) * FH * FW * C * sizeof(float);
+}
+
+dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int stride,
+                                int dilation, int pad, dwconv_dtype dtype, const void *x,
+                                const void *dy, float *dw, void *workspace,
+                                size_t workspace_bytes, dwconv_stream stream) {
+    if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
+    Shape s;
+    dwconv_status st = make_shape(N, H, W, C, FH, FW, stride, dilation, pad, s);
+    if (st != DWCONV_OK) return st;
+    if (dtype == DWCONV_INT8) return DWCONV_ERR_UNSUPPORTED;
+    if (!x || !dy || !dw) return DWCONV_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (!aligned(x, es) || !aligned(dy, es) || !aligned(dw, 4)) return DWCONV_ERR_MISALIGNED;
+    const int Z = wgrad_slices(s);
+    const size_t need = (size_t)Z * FH * FW * C * sizeof(float);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return DWCONV_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return DWCONV_ERR_MISALIGNED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    float *part = static_cast<float *>(workspace);
+    cudaError_t e = launch_wgrad_direct(s, dtype, x, dy, part, Z, cs);
+    if (e != cudaSuccess) return DWCONV_ERR_CUDA;
+    return cuda_status(launch_wgrad_reduce(part, Z, (long long)FH * FW * C, dw, cs));
+}
+
+}  // extern "C"

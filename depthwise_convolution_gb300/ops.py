@@ -1,0 +1,131 @@
+"""Python binding of the C ABI, one function per entry point, same names.
+
+Argument marshalling only: shapes, dtypes and device pointers of PyTorch CUDA
+tensors are passed to libdwconv, which does all of the work on the GPU.
+PyTorch provides device memory (outputs and workspace are allocated with
+torch.empty when the caller passes none) and the current CUDA stream.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+_DTYPE = {torch.int8: _lib.INT8, torch.float32: _lib.FP32, torch.float16: _lib.FP16,
+          torch.bfloat16: _lib.BF16}
+
+
+def _code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPE[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _dev(t: torch.Tensor, name: str, ndim: int) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (channels-last dense layout)")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def dwconv_output_size(H, W, FH, FW, stride=1, dilation=1, pad=0):
+    """(OH, OW) of the forward pass; raises DwconvError on invalid sizes."""
+    oh, ow = ctypes.c_int(0), ctypes.c_int(0)
+    _lib.check(_lib.load().dwconv_output_size(H, W, FH, FW, stride, dilation, pad,
+                                               ctypes.byref(oh), ctypes.byref(ow)),
+               "dwconv_output_size")
+    return oh.value, ow.value
+
+
+def dwconv_fwd(x, w, bias=None, stride=1, dilation=1, pad=0, out=None, stream=None):
+    """y = DWC(x, w) + bias.  x [N,H,W,C], w [FH,FW,C], bias [C] (fp32, or int32
+    for int8 data) or None.  Returns y [N,OH,OW,C] (int32 for int8 data)."""
+    N, H, W, C = x.shape
+    FH, FW = w.shape[0], w.shape[1]
+    dt = _code(x)
+    if w.dtype != x.dtype or tuple(w.shape) != (FH, FW, C):
+        raise ValueError("w must be [FH, FW, C] with x's dtype")
+    bias_dtype = torch.int32 if dt == _lib.INT8 else torch.float32
+    if bias is not None and (bias.dtype != bias_dtype or tuple(bias.shape) != (C,)):
+        raise ValueError(f"bias must be [C] {bias_dtype}")
+    OH, OW = dwconv_output_size(H, W, FH, FW, stride, dilation, pad)
+    y_dtype = torch.int32 if dt == _lib.INT8 else x.dtype
+    if out is None:
+        out = torch.empty((N, OH, OW, C), dtype=y_dtype, device=x.device)
+    elif out.dtype != y_dtype or tuple(out.shape) != (N, OH, OW, C):
+        raise ValueError("out has the wrong shape or dtype")
+    _lib.check(_lib.load().dwconv_fwd(
+        N, H, W, C, FH, FW, stride, dilation, pad, dt,
+        _dev(x, "x", 4), _dev(w, "w", 3), None if bias is None else _dev(bias, "bias", 1),
+        _dev(out, "out", 4), _stream(stream)), "dwconv_fwd")
+    return out
+
+
+def dwconv_bwd_data(dy, w, H, W, stride=1, dilation=1, pad=0, out=None, stream=None):
+    """dx [N,H,W,C] from dy [N,OH,OW,C] and w [FH,FW,C]."""
+    N, OH, OW, C = dy.shape
+    FH, FW = w.shape[0], w.shape[1]
+    dt = _code(dy)
+    if w.dtype != dy.dtype or tuple(w.shape) != (FH, FW, C):
+        raise ValueError("w must be [FH, FW, C] with dy's dtype")
+    if dwconv_output_size(H, W, FH, FW, stride, dilation, pad) != (OH, OW):
+        raise ValueError("dy's spatial size is not the forward output of an H x W input")
+    if out is None:
+        out = torch.empty((N, H, W, C), dtype=dy.dtype, device=dy.device)
+    elif out.dtype != dy.dtype or tuple(out.shape) != (N, H, W, C):
+        raise ValueError("out has the wrong shape or dtype")
+    _lib.check(_lib.load().dwconv_bwd_data(
+        N, H, W, C, FH, FW, stride, dilation, pad, dt,
+        _dev(dy, "dy", 4), _dev(w, "w", 3), _dev(out, "out", 4), _stream(stream)), "dwconv_bwd_data")
+    return out
+
+
+def dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation, pad, dtype) -> int:
+    """Workspace bytes dwconv_bwd_filter needs (dtype: a torch dtype or ABI code)."""
+    code = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(_lib.load().dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation,
+                                                            pad, code))
+
+
+def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, workspace=None,
+                      stream=None):
+    """dw [FH,FW,C] fp32 from x [N,H,W,C] and dy [N,OH,OW,C]."""
+    N, H, W, C = x.shape
+    dt = _code(x)
+    if dy.dtype != x.dtype:
+        raise ValueError("dy must have x's dtype")
+    if (dy.shape[0], dy.shape[3]) != (N, C) or \
+            dwconv_output_size(H, W, FH, FW, stride, dilation, pad) != tuple(dy.shape[1:3]):
+        raise ValueError("dy's shape is not the forward output's")
+    if out is None:
+        out = torch.empty((FH, FW, C), dtype=torch.float32, device=x.device)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (FH, FW, C):
+        raise ValueError("out must be [FH, FW, C] float32")
+    need = dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation, pad, dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(_lib.load().dwconv_bwd_filter(
+        N, H, W, C, FH, FW, stride, dilation, pad, dt,
+        _dev(x, "x", 4), _dev(dy, "dy", 4), _dev(out, "out", 3),
+        workspace.data_ptr(), ws_bytes, _stream(stream)), "dwconv_bwd_filter")
+    return out
+
+
+def dwconv_launch_count() -> int:
+    """Kernels libdwconv has launched in this process."""
+    return int(_lib.load().dwconv_launch_count())

@@ -1,0 +1,140 @@
+/*
+ * dwconv.h - C ABI of libdwconv, depthwise 2-D convolution on one GB300 (sm_103a).
+ *
+ * The operation ("Flash-DWC: Making Depthwise Convolution Compute-Efficient on
+ * GPUs", §2.1 "Standard and depthwise convolution", Fig. 1; layouts from §2.3
+ * "Unified channels-last layout"): every channel c has its own FH x FW filter,
+ *
+ *   y[n,oh,ow,c] = bias[c] + sum_{fh<FH, fw<FW} w[fh,fw,c] * x[n, oh*S-P+fh*D, ow*S-P+fw*D, c]
+ *
+ * where x positions outside [0,H) x [0,W) read as zero (padding is generated,
+ * never fetched: "Tiles, halos and partial sums", "Partition tensors to fit
+ * storage").  S = stride, D = dilation, P = pad, the same along both axes.
+ * Output size (floor convention):
+ *
+ *   OH = floor((H + 2P - D(FH-1) - 1) / S) + 1,   OW likewise.
+ *
+ * Layouts (all dense, row-major, channels innermost):
+ *   x, dx   [N][H][W][C]      y, dy  [N][OH][OW][C]
+ *   w       [FH][FW][C]       dw     [FH][FW][C] (fp32)     bias [C]
+ *
+ * Element types per dtype:
+ *   DWCONV_INT8  x, w int8;  bias int32 (nullable); y int32.  Forward only.
+ *                Accumulation in int32; overflow wraps (two's complement).
+ *   DWCONV_FP32  x, w, bias, y, dy, dx, dw: float.
+ *   DWCONV_FP16  x, w, y, dy, dx: IEEE half; bias, dw: float.
+ *   DWCONV_BF16  x, w, y, dy, dx: bfloat16;  bias, dw: float.
+ *   Floating-point accumulation is fp32 in every case (Flash-DWC §4.1 shows
+ *   16-bit accumulation loses too much accuracy); 16-bit outputs are rounded
+ *   to nearest even once, at the end.
+ *
+ * Ownership and ordering: the caller owns every buffer (device memory, e.g.
+ * from PyTorch); the library allocates no device memory, keeps no per-call
+ * state and caches only device properties.  Every call validates its
+ * arguments on the host, then enqueues kernels on `stream` and returns before
+ * they finish (stream-ordered, like cudaMemcpyAsync).  Input buffers must not
+ * overlap output buffers.
+ *
+ * Errors: status codes only.  Validation happens before any launch; on a
+ * non-OK status nothing was enqueued.  A launch failure returns
+ * DWCONV_ERR_CUDA; faults that happen later surface on the stream as usual.
+ */
+#ifndef DWCONV_H
+#define DWCONV_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DWCONV_OK = 0,
+    DWCONV_ERR_INVALID_ARG = 1,  /* bad size, null pointer, empty output, small workspace */
+    DWCONV_ERR_UNSUPPORTED = 2,  /* dtype/pass pair not provided (int8 backward) */
+    DWCONV_ERR_MISALIGNED = 3,   /* a pointer not aligned to its element size */
+    DWCONV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    DWCONV_ERR_TIMEOUT = 5       /* reserved: a bounded device-side wait gave up */
+} dwconv_status;
+
+typedef enum {
+    DWCONV_INT8 = 0,
+    DWCONV_FP32 = 1,
+    DWCONV_FP16 = 2,
+    DWCONV_BF16 = 3
+} dwconv_dtype;
+
+/* A CUDA stream (the same handle as cudaStream_t).  NULL = the legacy default stream. */
+typedef struct CUstream_st *dwconv_stream;
+
+/*
+ * Output extent of the forward pass for an H x W input (floor convention above).
+ * Writes *OH and *OW (either may be NULL).  Returns DWCONV_INVALID_ARG if a size
+ * or S, D is non-positive, P is negative, or the output would be empty.
+ */
+dwconv_status dwconv_output_size(int H, int W, int FH, int FW, int stride, int dilation, int pad,
+                                 int *OH, int *OW);
+
+/*
+ * Forward pass (Flash-DWC §5.1 "FC"): y = DWC(x, w) + bias.
+ * x [N][H][W][C], w [FH][FW][C], bias [C] or NULL (no bias), y [N][OH][OW][C].
+ * The bias enters each output exactly once ("Tiles, halos and partial sums":
+ * partial sums keep full precision across tiles and the bias is added once).
+ */
+dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride, int dilation,
+                         int pad, dwconv_dtype dtype, const void *x, const void *w,
+                         const void *bias, void *y, dwconv_stream stream);
+
+/*
+ * Input gradient (Flash-DWC §5.1 "BDC"): dx = the adjoint of the bias-free
+ * forward map applied to dy, i.e.
+ *   dx[n,ih,iw,c] = sum over (oh,ow,fh,fw) with oh*S-P+fh*D = ih and
+ *                   ow*S-P+fw*D = iw of w[fh,fw,c] * dy[n,oh,ow,c].
+ * For S = 1 this is the forward pass over dy with the filter rotated by 180
+ * degrees and padding D(FH-1)-P, as §5.1 states; for S > 1 positions that no
+ * tap reaches receive 0.  dy [N][OH][OW][C] (OH, OW of an H x W input),
+ * w [FH][FW][C], dx [N][H][W][C] (every element written).  Floating dtypes only;
+ * DWCONV_INT8 returns DWCONV_ERR_UNSUPPORTED.
+ */
+dwconv_status dwconv_bwd_data(int N, int H, int W, int C, int FH, int FW, int stride,
+                              int dilation, int pad, dwconv_dtype dtype, const void *dy,
+                              const void *w, void *dx, dwconv_stream stream);
+
+/*
+ * Bytes of device scratch that dwconv_bwd_filter needs for this shape (the
+ * per-slice partial sums of the split reduction).  A pure function of the
+ * arguments; 0 if they are invalid.
+ */
+size_t dwconv_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW, int stride,
+                                        int dilation, int pad, dwconv_dtype dtype);
+
+/*
+ * Weight gradient (Flash-DWC §5.1 "BFC"):
+ *   dw[fh,fw,c] = sum over (n,oh,ow) with the tap inside the input of
+ *                 dy[n,oh,ow,c] * x[n, oh*S-P+fh*D, ow*S-P+fw*D, c].
+ * The N*OH*OW accumulation axis is split into slices reduced in parallel and
+ * then summed in a fixed order (§5.1 "accumulation-axis parallelisation"), so
+ * repeated calls give bit-identical dw.  x [N][H][W][C], dy [N][OH][OW][C],
+ * dw [FH][FW][C] float (fully overwritten).  `workspace` is caller-owned
+ * device memory of at least dwconv_bwd_filter_workspace_size() bytes, 256-byte
+ * aligned; it may be NULL only if that size is 0.  Floating dtypes only.
+ */
+dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int stride,
+                                int dilation, int pad, dwconv_dtype dtype, const void *x,
+                                const void *dy, float *dw, void *workspace,
+                                size_t workspace_bytes, dwconv_stream stream);
+
+/* A static, human-readable name for a status code. */
+const char *dwconv_status_string(dwconv_status status);
+
+/*
+ * Number of kernels this library has launched in this process (all threads,
+ * all devices).  Lets a caller count launches over a region of interest.
+ */
+unsigned long long dwconv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DWCONV_H */

@@ -1,0 +1,133 @@
+"""Shared helpers for the GPU parity tests: run a pass through the library,
+run the oracle on the same quantised inputs, compare element by element.
+
+Tolerances (per output element, mag = sum |products| (+ |bias|) from the oracle):
+  int8 -> int32          bit-exact (int64 oracle reduced mod 2^32)
+  fp32                   |gpu - ref| <= 1e-5 * mag
+  fp16 / bf16 inputs     |gpu - ref| <= 2e-3 * mag, plus, for 16-bit outputs,
+                         half a unit in the last place of the output format at
+                         max(|ref|, |gpu|): the rounding the output type itself
+                         forces, which an fp32-accumulation bound cannot cover
+                         (bf16 keeps 8 significant bits, so rounding alone can
+                         reach 2^-8 |y|).  wgrad writes fp32 and gets no such term.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from depthwise_convolution_gb300 import ops
+
+TOL = {"fp32": 1e-5, "fp16": 2e-3, "bf16": 2e-3}
+SIG_BITS = {"fp16": 11, "bf16": 8}      # significand bits including the hidden one
+MIN_EXP = {"fp16": -14, "bf16": -126}   # exponent of the smallest normal number
+TORCH = {"int8": torch.int8, "fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16}
+GUARD = 256                              # guard elements on each side of an output
+
+
+def half_ulp(v: np.ndarray, dtype: str) -> np.ndarray:
+    p = SIG_BITS[dtype]
+    _, e = np.frexp(np.abs(v))           # |v| = m * 2^e, m in [0.5, 1)
+    e = np.maximum(e - 1, MIN_EXP[dtype])  # unbiased exponent, subnormals share the minimum
+    return np.ldexp(1.0, e - p)          # half of 2^(e - p + 1)
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu()
+    if t.dtype in (torch.int8, torch.int32):
+        return t.to(torch.int64).numpy()
+    return t.to(torch.float64).numpy()
+
+
+def compare(got: np.ndarray, ref: np.ndarray, mag: np.ndarray, dtype: str, out16: bool, what: str):
+    """Assert the tolerance; return the largest err / mag seen."""
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    if dtype == "int8":
+        expect = ((ref + 2**31) % 2**32) - 2**31
+        bad = np.nonzero(got != expect)
+        assert bad[0].size == 0, f"{what}: {bad[0].size} int32 mismatches, first at {tuple(b[0] for b in bad)}"
+        return 0.0
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bound = TOL[dtype] * mag
+    if out16:
+        bound = bound + half_ulp(np.maximum(np.abs(ref), np.abs(got)), dtype)
+    over = err > bound
+    if over.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(over.sum())} elements over tolerance; worst at {i}: "
+                             f"gpu={got[i]!r} ref={ref[i]!r} mag={mag[i]!r} bound={bound[i]!r}")
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(mag > 0, err / mag, 0.0)
+    return float(ratio.max()) if ratio.size else 0.0
+
+
+class Guarded:
+    """An output tensor inside a larger buffer whose ends hold a bit pattern
+    that must survive the call (an out-of-bounds write shows up there)."""
+
+    def __init__(self, shape, dtype, device="cuda"):
+        n = int(np.prod(shape))
+        self.buf = torch.empty(n + 2 * GUARD, dtype=dtype, device=device)
+        raw = self.buf.view(torch.uint8)
+        raw.fill_(0xA5)
+        self.guard_bytes = GUARD * self.buf.element_size()
+        self.t = self.buf[GUARD:GUARD + n].view(shape)
+        self.t.fill_(float("nan") if dtype.is_floating_point else -12345)
+
+    def check(self, what):
+        raw = self.buf.view(torch.uint8)
+        head = raw[:self.guard_bytes].cpu()
+        tail = raw[-self.guard_bytes:].cpu()
+        assert bool((head == 0xA5).all()) and bool((tail == 0xA5).all()), f"{what}: guard band overwritten"
+
+
+def random_inputs(dtype, N, H, W, C, FH, FW, S, D, P, seed, bias=True):
+    from depthwise_convolution_gb300 import synthetic as syn
+    wl = syn.Workload("case", dtype, N, H, W, C, FH, FW, S, D, P, bias, ("fwd", "dgrad", "wgrad"), seed)
+    OH, OW = oracle.out_extent(H, FH, S, D, P), oracle.out_extent(W, FW, S, D, P)
+    if dtype == "int8":
+        d = syn.make_inputs(wl)
+        d["dy"] = None
+    else:
+        d = syn.make_inputs(wl, dy_hw=(OH, OW))
+    return d
+
+
+def check_fwd(d, dtype, S, D, P, images=None, what="fwd"):
+    x, w, b = d["x"], d["w"], d["bias"]
+    N, H, W, C = x.shape
+    FH, FW = w.shape[:2]
+    OH, OW = oracle.out_extent(H, FH, S, D, P), oracle.out_extent(W, FW, S, D, P)
+    out_dtype = torch.int32 if dtype == "int8" else TORCH[dtype]
+    g = Guarded((N, OH, OW, C), out_dtype)
+    y = ops.dwconv_fwd(x.cuda(), w.cuda(), None if b is None else b.cuda(), S, D, P, out=g.t)
+    torch.cuda.synchronize()
+    g.check(what)
+    imgs = list(range(N)) if images is None else sorted(set(i % N for i in images))
+    ref, mag = oracle.fwd(to64(x[imgs]), to64(w), None if b is None else to64(b), S, D, P)
+    return compare(to64(y[imgs]), ref, mag, dtype, dtype in ("fp16", "bf16"), what)
+
+
+def check_dgrad(d, dtype, S, D, P, images=None, what="dgrad"):
+    dy, w = d["dy"], d["w"]
+    N, H, W, C = d["x"].shape
+    g = Guarded((N, H, W, C), TORCH[dtype])
+    dx = ops.dwconv_bwd_data(dy.cuda(), w.cuda(), H, W, S, D, P, out=g.t)
+    torch.cuda.synchronize()
+    g.check(what)
+    imgs = list(range(N)) if images is None else sorted(set(i % N for i in images))
+    ref, mag = oracle.dgrad(to64(dy[imgs]), to64(w), H, W, S, D, P)
+    return compare(to64(dx[imgs]), ref, mag, dtype, dtype in ("fp16", "bf16"), what)
+
+
+def check_wgrad(d, dtype, S, D, P, what="wgrad"):
+    x, dy = d["x"], d["dy"]
+    FH, FW, C = d["w"].shape
+    g = Guarded((FH, FW, C), torch.float32)
+    dw = ops.dwconv_bwd_filter(x.cuda(), dy.cuda(), FH, FW, S, D, P, out=g.t)
+    torch.cuda.synchronize()
+    g.check(what)
+    ref, mag = oracle.wgrad(to64(x), to64(dy), FH, FW, S, D, P)
+    return compare(to64(dw), ref, mag, dtype, False, what)

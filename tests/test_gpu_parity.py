@@ -1,0 +1,120 @@
+"""GPU parity: the CUDA path against the oracle, element by element, on the
+same seeded, quantised inputs.  Small shapes that span several tiles with
+ragged tails, edge cases, and the five workloads at full size (forward and
+input gradient checked on sampled images, weight gradient in full)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from depthwise_convolution_gb300 import ops, synthetic
+from parity import (TORCH, check_dgrad, check_fwd, check_wgrad, compare, random_inputs, to64)
+
+pytestmark = pytest.mark.gpu
+
+# (N, H, W, C, FH, FW, S, D, P)
+SMALL = [
+    (2, 13, 11, 40, 3, 3, 1, 1, 1),      # 3x3, channel tail 40 = 32 + 8, ragged rows/columns
+    (3, 23, 19, 64, 5, 5, 1, 1, 2),      # 5x5 over several tiles
+    (2, 30, 29, 96, 7, 7, 1, 1, 3),      # 7x7 over several tiles and channel slabs
+    (1, 9, 9, 32, 7, 7, 1, 1, 0),        # no padding
+    (2, 20, 22, 32, 5, 5, 2, 2, 4),      # stride 2, dilation 2: even sub-grid
+    (2, 21, 17, 48, 5, 5, 2, 2, 3),      # stride 2, dilation 2, odd pad: odd sub-grid
+    (2, 16, 15, 24, 3, 3, 2, 1, 1),      # stride 2
+    (2, 12, 12, 8, 3, 3, 1, 2, 2),       # dilation 2
+    (1, 7, 7, 6, 4, 2, 1, 1, 1),         # non-square, even filter extent, C = 6
+    (2, 10, 10, 5, 3, 3, 1, 1, 1),       # odd channel count
+    (1, 40, 40, 32, 31, 31, 1, 1, 15),   # large filter
+    (1, 5, 5, 16, 7, 7, 1, 1, 3),        # map smaller than the filter
+    (4, 7, 7, 64, 7, 7, 1, 1, 3),        # 7x7 map: several images per CTA
+    (3, 14, 14, 32, 7, 7, 1, 1, 3),      # 14x14 map
+    (2, 1, 1, 16, 3, 3, 1, 1, 1),        # 1x1 map
+    (1, 6, 6, 16, 3, 3, 3, 1, 1),        # stride 3
+    (2, 9, 8, 16, 3, 5, 1, 1, 2),        # FH != FW on the tiled path (pads differ by axis)
+    (1, 11, 11, 2, 3, 3, 1, 1, 1),       # C = 2
+]
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "x".join(map(str, c)))
+def test_small_shapes_all_passes(dtype, case):
+    N, H, W, C, FH, FW, S, D, P = case
+    d = random_inputs(dtype, N, H, W, C, FH, FW, S, D, P, seed=hash(case) % 1000 + 7)
+    check_fwd(d, dtype, S, D, P)
+    d_nobias = dict(d, bias=None)
+    check_fwd(d_nobias, dtype, S, D, P, what="fwd-nobias")
+    check_dgrad(d, dtype, S, D, P)
+    check_wgrad(d, dtype, S, D, P)
+
+
+def test_int8_tail_channels_bit_exact():
+    wl = synthetic.WORKLOADS["int8-fwd-3x3-1x8x8x5"]
+    d = synthetic.make_inputs(wl)
+    check_fwd(d, "int8", wl.stride, wl.dilation, wl.pad, what=wl.name)
+
+
+@pytest.mark.parametrize("case", [(3, 9, 7, 13, 3, 3, 1, 1, 1), (1, 6, 6, 64, 5, 5, 2, 1, 2),
+                                  (2, 8, 8, 7, 3, 3, 2, 2, 2)])
+def test_int8_other_shapes_bit_exact(case):
+    N, H, W, C, FH, FW, S, D, P = case
+    d = random_inputs("int8", N, H, W, C, FH, FW, S, D, P, seed=99)
+    check_fwd(d, "int8", S, D, P)
+
+
+def test_int8_wraps_like_two_complement():
+    """Sums beyond int32 wrap modulo 2^32 (documented behaviour)."""
+    x = torch.full((1, 3, 3, 2), -128, dtype=torch.int8)
+    w = torch.full((3, 3, 2), -128, dtype=torch.int8)
+    b = torch.tensor([2**31 - 1, -2**31], dtype=torch.int32)
+    y = ops.dwconv_fwd(x.cuda(), w.cuda(), b.cuda(), 1, 1, 1).cpu()
+    ref, _ = oracle.fwd(to64(x), to64(w), to64(b), 1, 1, 1)
+    compare(to64(y), ref, None, "int8", False, "wrap")
+
+
+FULL = [wl for wl in synthetic.WORKLOADS.values() if wl.dtype != "int8"]
+
+
+def full_inputs(wl):
+    OH, OW = oracle.out_extent(wl.H, wl.FH, wl.stride, wl.dilation, wl.pad), \
+        oracle.out_extent(wl.W, wl.FW, wl.stride, wl.dilation, wl.pad)
+    return synthetic.make_inputs(wl, dy_hw=(OH, OW) if "dgrad" in wl.passes else None)
+
+
+@pytest.mark.parametrize("wl", FULL, ids=lambda w: w.name)
+def test_full_size_workloads(wl):
+    d = full_inputs(wl)
+    images = [0, wl.N // 2, wl.N - 1]
+    check_fwd(d, wl.dtype, wl.stride, wl.dilation, wl.pad, images=images, what=f"{wl.name} fwd")
+    if "dgrad" in wl.passes:
+        check_dgrad(d, wl.dtype, wl.stride, wl.dilation, wl.pad, images=images, what=f"{wl.name} dgrad")
+    if "wgrad" in wl.passes:
+        check_wgrad(d, wl.dtype, wl.stride, wl.dilation, wl.pad, what=f"{wl.name} wgrad")
+
+
+def test_wgrad_is_deterministic():
+    d = random_inputs("bf16", 4, 28, 28, 96, 7, 7, 1, 1, 3, seed=5)
+    x, dy = d["x"].cuda(), d["dy"].cuda()
+    a = ops.dwconv_bwd_filter(x, dy, 7, 7, 1, 1, 3)
+    b = ops.dwconv_bwd_filter(x, dy, 7, 7, 1, 1, 3)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_side_stream_and_launch_count():
+    d = random_inputs("fp16", 2, 16, 16, 32, 7, 7, 1, 1, 3, seed=3)
+    s = torch.cuda.Stream()
+    before = ops.dwconv_launch_count()
+    with torch.cuda.stream(s):
+        x, w = d["x"].cuda(), d["w"].cuda()
+        y = ops.dwconv_fwd(x, w, None, 1, 1, 3, stream=s)
+    s.synchronize()
+    assert ops.dwconv_launch_count() > before
+    ref, mag = oracle.fwd(to64(d["x"]), to64(d["w"]), None, 1, 1, 3)
+    compare(to64(y), ref, mag, "fp16", True, "side stream")
+
+
+def test_zero_input_gives_bias_only():
+    x = torch.zeros(2, 9, 9, 32, dtype=torch.bfloat16, device="cuda")
+    w = torch.randn(7, 7, 32, device="cuda").to(torch.bfloat16)
+    b = torch.randn(32, device="cuda")
+    y = ops.dwconv_fwd(x, w, b, 1, 1, 3)
+    assert torch.equal(y.float(), b.to(torch.bfloat16).float().expand_as(y))
