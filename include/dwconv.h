@@ -69,7 +69,7 @@ typedef struct CUstream_st *dwconv_stream;
 
 /*
  * Output extent of the forward pass for an H x W input (floor convention above).
- * Writes *OH and *OW (either may be NULL).  Returns DWCONV_INVALID_ARG if a size
+ * Writes *OH and *OW (either may be NULL).  Returns DWCONV_ERR_INVALID_ARG if a size
  * or S, D is non-positive, P is negative, or the output would be empty.
  */
 dwconv_status dwconv_output_size(int H, int W, int FH, int FW, int stride, int dilation, int pad,
