@@ -4,10 +4,12 @@ The work is done by libdwconv.so (C ABI in include/dwconv.h, CUDA kernels in
 csrc/); this package is its Python binding.  Importing the package does not
 load the library; the first call does, and fails loudly if it is missing.
 """
-from .ops import (dwconv_bwd_data, dwconv_bwd_filter, dwconv_bwd_filter_workspace_size,
-                  dwconv_fwd, dwconv_launch_count, dwconv_output_size)
+from .ops import (dwconv_bwd_data, dwconv_bwd_filter, dwconv_bwd_filter_static,
+                  dwconv_bwd_filter_workspace_size, dwconv_fwd, dwconv_launch_count,
+                  dwconv_output_size)
 from ._lib import DwconvError
 
 __all__ = ["dwconv_fwd", "dwconv_bwd_data", "dwconv_bwd_filter",
-           "dwconv_bwd_filter_workspace_size", "dwconv_output_size", "dwconv_launch_count",
+           "dwconv_bwd_filter_workspace_size", "dwconv_bwd_filter_static", "dwconv_output_size",
+           "dwconv_launch_count",
            "DwconvError"]

@@ -126,6 +126,28 @@ def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, work
     return out
 
 
+def dwconv_bwd_filter_static(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, stream=None):
+    """dw [FH,FW,C] fp32 like dwconv_bwd_filter, for callers that cannot allocate
+    scratch: the library's built-in scratch array is used instead of a workspace.
+    Only ``out`` is allocated here when the caller passes none."""
+    N, H, W, C = x.shape
+    dt = _code(x)
+    if dy.dtype != x.dtype:
+        raise ValueError("dy must have x's dtype")
+    if (dy.shape[0], dy.shape[3]) != (N, C) or \
+            dwconv_output_size(H, W, FH, FW, stride, dilation, pad) != tuple(dy.shape[1:3]):
+        raise ValueError("dy's shape is not the forward output's")
+    if out is None:
+        out = torch.empty((FH, FW, C), dtype=torch.float32, device=x.device)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (FH, FW, C):
+        raise ValueError("out must be [FH, FW, C] float32")
+    _lib.check(_lib.load().dwconv_bwd_filter_static(
+        N, H, W, C, FH, FW, stride, dilation, pad, dt,
+        _dev(x, "x", 4), _dev(dy, "dy", 4), _dev(out, "out", 3), _stream(stream)),
+        "dwconv_bwd_filter_static")
+    return out
+
+
 def dwconv_launch_count() -> int:
     """Kernels libdwconv has launched in this process."""
     return int(_lib.load().dwconv_launch_count())

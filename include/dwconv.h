@@ -124,6 +124,38 @@ dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int 
                                 const void *dy, float *dw, void *workspace,
                                 size_t workspace_bytes, dwconv_stream stream);
 
+/* Bytes of device scratch built into the library for dwconv_bwd_filter_static. */
+#define DWCONV_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/*
+ * Weight gradient for callers that cannot allocate device memory.  The paper
+ * has no counterpart: this is a deployment convenience of this library.
+ *
+ * Same operation, arguments and result as dwconv_bwd_filter, minus the
+ * workspace.  It is for code that has no way to obtain scratch memory: for
+ * example an operator running inside a framework whose caching allocator
+ * already owns the device memory (so calling cudaMalloc would go around it),
+ * or a deployment that fixes its memory plan at start-up and forbids
+ * allocation afterwards.  The call allocates nothing; it uses a
+ * DWCONV_STATIC_SCRATCH_BYTES array compiled into the library, which every
+ * GPU that loads the library holds until the process exits.
+ *
+ * - Shapes whose dwconv_bwd_filter_workspace_size() exceeds
+ *   DWCONV_STATIC_SCRATCH_BYTES are rejected with DWCONV_ERR_INVALID_ARG
+ *   before anything is enqueued; use dwconv_bwd_filter for those.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture on the device.
+ * - All calls on a device share the one array, and it keeps whatever the last
+ *   call left in it.  Calls whose work overlaps on the GPU (different streams,
+ *   no ordering between them) race on it and give wrong results: order them.
+ *   Nothing in the array needs to start at zero; each call writes every
+ *   partial sum before reading it.
+ */
+dwconv_status dwconv_bwd_filter_static(int N, int H, int W, int C, int FH, int FW, int stride,
+                                       int dilation, int pad, dwconv_dtype dtype, const void *x,
+                                       const void *dy, float *dw, dwconv_stream stream);
+
 /* A static, human-readable name for a status code. */
 const char *dwconv_status_string(dwconv_status status);
 
