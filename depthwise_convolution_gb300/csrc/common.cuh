@@ -88,7 +88,8 @@ struct TiledConv {
     const void *in;        // x (forward) or dy (input gradient)
     const void *w;
     const float *bias;     // nullable; forward only
-    void *out;             // y or dx
+    void *out;             // y or dx (dw, float, for the weight gradient)
+    const void *dy;        // weight gradient only: dy [N][OHs][OWs][C]
     int N, C;
     int FH, FW;
     int flip;              // 1: filter rotated by 180 degrees
@@ -105,5 +106,12 @@ struct TiledConv {
 
 // Returns cudaErrorNotSupported when no tiled instance covers the request.
 cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
+
+// Weight gradient on the tiled path: slices of the accumulation axis for this
+// shape (0 if no tiled instance covers it; depends on the shape only), and the
+// launch (partials into part[Zc][FH*FW][C], then the fixed-order reduction
+// into p.out).
+int tiled_wgrad_slices(const TiledConv &p, dwconv_dtype dt);
+cudaError_t launch_tiled_wgrad(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st);
 
 }  // namespace dwc

@@ -102,6 +102,27 @@ int wgrad_slices(const Shape &s) {
     return (int)z;
 }
 
+// The weight gradient reads x on the same sub-grid as the forward pass; when
+// that sub-grid has unit stride and dilation (and the channel rows are whole
+// 16-byte copies) the tiled kernel can take it.  Shape-only: pointers may be
+// null when only the plan is wanted.
+bool wgrad_tiled_params(const Shape &s, dwconv_dtype dt, const void *x, const void *dy, float *dw,
+                        TiledConv &p) {
+    if (dt == DWCONV_INT8 || (s.C * elem_size(dt)) % 16 != 0) return false;
+    const int g = gcd(s.S, s.D);
+    const int r0 = (g - s.P % g) % g;
+    if (s.S / g != 1 || s.D / g != 1 || s.H <= r0 || s.W <= r0) return false;
+    p = TiledConv{};
+    p.in = x; p.w = nullptr; p.bias = nullptr; p.out = dw; p.dy = dy;
+    p.N = s.N; p.C = s.C; p.FH = s.FH; p.FW = s.FW; p.flip = 0;
+    p.Hf = s.H; p.Wf = s.W; p.in_step = g; p.in_off = r0;
+    p.Hs = (s.H - r0 + g - 1) / g; p.Ws = (s.W - r0 + g - 1) / g;
+    p.pad_h = p.pad_w = (s.P + r0) / g;
+    p.OHf = s.OH; p.OWf = s.OW; p.OHs = s.OH; p.OWs = s.OW;
+    p.out_step = 1; p.out_off = 0; p.zero_phases = 0;
+    return tiled_wgrad_slices(p, dt) > 0;
+}
+
 }  // namespace
 }  // namespace dwc
 
@@ -212,7 +233,14 @@ size_t dwconv_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int 
     Shape s;
     if (!valid_dtype(dtype) || dtype == DWCONV_INT8) return 0;
     if (make_shape(N, H, W, C, FH, FW, stride, dilation, pad, s) != DWCONV_OK) return 0;
-    return (size_t)wgrad_slices(s) * FH * FW * C * sizeof(float);
+    const size_t per_slice = (size_t)FH * FW * C * sizeof(float);
+    size_t need = (size_t)wgrad_slices(s) * per_slice;
+    TiledConv p;
+    if (wgrad_tiled_params(s, dtype, nullptr, nullptr, nullptr, p)) {
+        const size_t tiled = (size_t)tiled_wgrad_slices(p, dtype) * per_slice;
+        if (tiled > need) need = tiled;
+    }
+    return need;
 }
 
 dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int stride,
@@ -227,12 +255,19 @@ dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int 
     if (!x || !dy || !dw) return DWCONV_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     if (!aligned(x, es) || !aligned(dy, es) || !aligned(dw, 4)) return DWCONV_ERR_MISALIGNED;
-    const int Z = wgrad_slices(s);
-    const size_t need = (size_t)Z * FH * FW * C * sizeof(float);
+    const size_t need = dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation, pad,
+                                                         dtype);
     if (workspace_bytes < need || (need > 0 && !workspace)) return DWCONV_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return DWCONV_ERR_MISALIGNED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     float *part = static_cast<float *>(workspace);
+
+    TiledConv p;
+    if (wgrad_tiled_params(s, dtype, x, dy, dw, p) && aligned(x, 16) && aligned(dy, 16)) {
+        cudaError_t e = launch_tiled_wgrad(p, dtype, part, cs);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
+    const int Z = wgrad_slices(s);
     cudaError_t e = launch_wgrad_direct(s, dtype, x, dy, part, Z, cs);
     if (e != cudaSuccess) return DWCONV_ERR_CUDA;
     return cuda_status(launch_wgrad_reduce(part, Z, (long long)FH * FW * C, dw, cs));
