@@ -5,11 +5,11 @@ csrc/); this package is its Python binding.  Importing the package does not
 load the library; the first call does, and fails loudly if it is missing.
 """
 from .ops import (dwconv_bwd_data, dwconv_bwd_filter, dwconv_bwd_filter_static,
-                  dwconv_bwd_filter_workspace_size, dwconv_fwd, dwconv_launch_count,
-                  dwconv_output_size)
+                  dwconv_bwd_filter_workspace_size, dwconv_check_device_errors, dwconv_fwd,
+                  dwconv_launch_count, dwconv_output_size)
 from ._lib import DwconvError
 
 __all__ = ["dwconv_fwd", "dwconv_bwd_data", "dwconv_bwd_filter",
            "dwconv_bwd_filter_workspace_size", "dwconv_bwd_filter_static", "dwconv_output_size",
-           "dwconv_launch_count",
+           "dwconv_launch_count", "dwconv_check_device_errors",
            "DwconvError"]

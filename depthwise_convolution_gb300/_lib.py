@@ -26,6 +26,7 @@ SIGNATURES = {
     "dwconv_bwd_filter_workspace_size": (_SZ, [_I] * 9 + [_I]),
     "dwconv_bwd_filter": (_I, [_I] * 9 + [_I, _P, _P, _P, _P, _SZ, _P]),
     "dwconv_bwd_filter_static": (_I, [_I] * 9 + [_I, _P, _P, _P, _P]),
+    "dwconv_check_device_errors": (_I, [_P]),
     "dwconv_status_string": (ctypes.c_char_p, [_I]),
     "dwconv_launch_count": (ctypes.c_ulonglong, []),
 }

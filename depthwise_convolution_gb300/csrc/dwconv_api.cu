@@ -6,6 +6,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace dwc {
 
@@ -153,6 +154,12 @@ const char *dwconv_status_string(dwconv_status status) {
 }
 
 unsigned long long dwconv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+dwconv_status dwconv_check_device_errors(dwconv_stream stream) {
+    unsigned v = 0;
+    if (take_device_error(reinterpret_cast<cudaStream_t>(stream), &v) != cudaSuccess) return DWCONV_ERR_CUDA;
+    return v ? DWCONV_ERR_TIMEOUT : DWCONV_OK;
+}
 
 dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride, int dilation,
                          int pad, dwconv_dtype dtype, const void *x, const void *w,

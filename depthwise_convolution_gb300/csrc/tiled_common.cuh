@@ -7,13 +7,15 @@
 // TH x TW block of outputs.  The unit's input halo -- (RT*TH-1)+FH rows by
 // (CT*TW-1)+FW columns of the sub-grid, the "(T-1)S + (R-1)D + 1" extent of
 // "Tiles, halos and partial sums" with S = D = 1 on the sub-grid -- is staged
-// in shared memory with 16-byte cp.async copies; copies that fall outside the
-// input use a zero source size, so padding is generated, never fetched.
+// in shared memory by one TMA tensor copy issued by one thread; the copy
+// engine fills everything outside the tensor with zeros, so padding is
+// generated, never fetched.
 #pragma once
 
 #include <algorithm>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace dwc {
 namespace tiled {
@@ -27,91 +29,51 @@ struct Geo {
     int HH, HW;            // halo rows / columns per image
     int tiles_h, tiles_w;  // work units along output rows / columns
     int groups, ctiles;    // image groups (NI images each), channel tiles
-    long long units;       // ctiles * groups * tiles_w * tiles_h
-    long long per_ctile;   // groups * tiles_w * tiles_h
+    int units;             // ctiles * groups * tiles_w * tiles_h
+    int per_ctile;         // groups * tiles_w * tiles_h
 };
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
-    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_1() {
-    asm volatile("cp.async.wait_group 1;\n" ::: "memory");
-}
 
 // Unit index -> (channel tile, image group, column tile, row band); the row
 // band varies fastest.
 struct Unit {
     int ctile, group, twi, band;
 };
-__device__ __forceinline__ Unit decode(const Geo &g, long long u) {
+__device__ __forceinline__ Unit decode(const Geo &g, int u) {
     Unit r;
-    r.ctile = (int)(u / g.per_ctile);
-    long long v = u % g.per_ctile;
-    r.band = (int)(v % g.tiles_h);
+    r.ctile = u / g.per_ctile;
+    int v = u - r.ctile * g.per_ctile;
+    r.band = v % g.tiles_h;
     v /= g.tiles_h;
-    r.twi = (int)(v % g.tiles_w);
-    r.group = (int)(v / g.tiles_w);
+    r.twi = v % g.tiles_w;
+    r.group = v / g.tiles_w;
     return r;
 }
 
-// Stage the input halo of unit `un` into dst[NI][HH][HW][32] (zero outside).
-template <typename T, int TH, int TW>
-__device__ __forceinline__ void stage_halo(const TiledConv &p, const Geo &g, T *dst, const Unit &un) {
-    constexpr int EPC = 16 / sizeof(T);  // elements per 16-byte copy
-    constexpr int CPP = 32 / EPC;        // copies per pixel (32 channels)
-    const T *in = static_cast<const T *>(p.in);
-    const int ih0 = un.band * (g.RT * TH) - p.pad_h;
-    const int iw0 = un.twi * (g.CT * TW) - p.pad_w;
-    const int c0 = un.ctile * 32;
-    const int total = g.NI * g.HH * g.HW * CPP;
-    for (int k = threadIdx.x; k < total; k += kThreads) {
-        const int q = k % CPP;
-        const int pix = k / CPP;
-        const int b = pix % g.HW;
-        const int a = (pix / g.HW) % g.HH;
-        const int il = pix / (g.HW * g.HH);
-        const int nn = un.group * g.NI + il;
-        const int ihs = ih0 + a, iws = iw0 + b, cc = c0 + q * EPC;
-        const bool ok = nn < p.N && ihs >= 0 && ihs < p.Hs && iws >= 0 && iws < p.Ws && cc < p.C;
-        const T *src = in;
-        if (ok)
-            src += (((long long)nn * p.Hf + (p.in_off + p.in_step * ihs)) * p.Wf +
-                    (p.in_off + p.in_step * iws)) * (long long)p.C + cc;
-        cp_async16(dst + (long long)pix * 32 + q * EPC, src, ok ? 16 : 0);
-    }
+// Tensor map of the taps' sub-grid of p.in, [N][Hs][Ws][C] with the sub-grid
+// steps folded into the strides; one box = one unit's halo [NI][HH][HW][32].
+// Elements outside the sub-grid (padding, channel tail, missing images) are
+// filled with zeros by the copy engine.
+inline bool make_halo_map(CUtensorMap *m, const TiledConv &p, const Geo &g, dwconv_dtype dt, size_t es) {
+    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off * p.Wf + p.in_off) * p.C * es;
+    const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
+    const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
+                             (uint64_t)p.Hf * p.Wf * p.C * es};
+    const uint32_t box[4] = {32, (uint32_t)g.HW, (uint32_t)g.HH, (uint32_t)g.NI};
+    return encode_tmap_4d(m, dt, base, dims, str, box);
 }
 
-// Stage the output-side tile of unit `un` (dy for the weight gradient) from
-// `src` [N][OHs][OWs][C] into dst[NI][RT*TH][CT*TW][32] (zero outside).
-template <typename T, int TH, int TW>
-__device__ __forceinline__ void stage_out_tile(const TiledConv &p, const Geo &g, const T *src_base,
-                                               T *dst, const Unit &un) {
-    constexpr int EPC = 16 / sizeof(T);
-    constexpr int CPP = 32 / EPC;
-    const int rows = g.RT * TH, cols = g.CT * TW;
-    const int i0 = un.band * rows, j0 = un.twi * cols;
-    const int c0 = un.ctile * 32;
-    const int total = g.NI * rows * cols * CPP;
-    for (int k = threadIdx.x; k < total; k += kThreads) {
-        const int q = k % CPP;
-        const int pix = k / CPP;
-        const int b = pix % cols;
-        const int a = (pix / cols) % rows;
-        const int il = pix / (cols * rows);
-        const int nn = un.group * g.NI + il;
-        const int i = i0 + a, j = j0 + b, cc = c0 + q * EPC;
-        const bool ok = nn < p.N && i < p.OHs && j < p.OWs && cc < p.C;
-        const T *src = src_base;
-        if (ok) src += (((long long)nn * p.OHs + i) * p.OWs + j) * (long long)p.C + cc;
-        cp_async16(dst + (long long)pix * 32 + q * EPC, src, ok ? 16 : 0);
-    }
+// Tensor map of an output-side tensor [N][OHs][OWs][C] (dy for the weight
+// gradient); one box = one unit's output tile [NI][RT*TH][CT*TW][32].
+inline bool make_tile_map(CUtensorMap *m, const void *base, const TiledConv &p, const Geo &g, int TH, int TW,
+                          dwconv_dtype dt, size_t es) {
+    const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.OWs, (uint64_t)p.OHs, (uint64_t)p.N};
+    const uint64_t str[3] = {(uint64_t)p.C * es, (uint64_t)p.OWs * p.C * es, (uint64_t)p.OHs * p.OWs * p.C * es};
+    const uint32_t box[4] = {32, (uint32_t)(g.CT * TW), (uint32_t)(g.RT * TH), (uint32_t)g.NI};
+    return encode_tmap_4d(m, dt, base, dims, str, box);
 }
+
+// Bytes of one stage region, rounded up so the next region stays 128-byte aligned.
+inline __host__ __device__ unsigned align128(unsigned b) { return (b + 127u) & ~127u; }
 
 inline int next_pow2(int v) {
     int p = 1;
@@ -142,14 +104,23 @@ inline Geo make_geo(const TiledConv &p, int TH, int TW, size_t elem, bool out_ti
     g.tiles_w = (p.OWs + g.CT * TW - 1) / (g.CT * TW);
     g.groups = (p.N + g.NI - 1) / g.NI;
     g.ctiles = (p.C + 31) / 32;
-    g.per_ctile = (long long)g.groups * g.tiles_w * g.tiles_h;
-    g.units = (long long)g.ctiles * g.per_ctile;
+    const long long per = (long long)g.groups * g.tiles_w * g.tiles_h;
+    const long long units = per * g.ctiles;
+    g.per_ctile = (int)std::min<long long>(per, 1LL << 30);
+    g.units = units < (1LL << 30) ? (int)units : 0;  // 0: too large for the tiled kernels
     return g;
 }
 
+// Bytes of one pipeline stage: the halo box, then (weight gradient) the tile box.
+inline __host__ __device__ unsigned halo_box_bytes(const Geo &g, size_t elem) {
+    return (unsigned)((size_t)g.NI * g.HH * g.HW * 32 * elem);
+}
+inline __host__ __device__ unsigned tile_box_bytes(const Geo &g, int TH, int TW, size_t elem) {
+    return (unsigned)((size_t)g.NI * g.RT * TH * g.CT * TW * 32 * elem);
+}
 inline size_t stage_bytes(const Geo &g, int TH, int TW, size_t elem, bool out_tile) {
-    size_t px = (size_t)g.HH * g.HW + (out_tile ? (size_t)g.RT * TH * g.CT * TW : 0);
-    return 2 * (size_t)g.NI * px * 32 * elem;
+    return 2 * (size_t)(align128(halo_box_bytes(g, elem)) +
+                        (out_tile ? align128(tile_box_bytes(g, TH, TW, elem)) : 0u));
 }
 
 }  // namespace tiled

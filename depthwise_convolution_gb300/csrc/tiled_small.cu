@@ -2,7 +2,8 @@
 //
 // Design (the Flash-DWC §3.1-§3.4 dataflow restated for sm_103a):
 //   * Work units, CTA shape and halo staging: see tiled_common.cuh.  Two
-//     stage buffers: the next unit's halo streams in while this one computes.
+//     stage buffers: thread 0 issues the next unit's halo as one TMA tensor
+//     copy while the CTA computes this one; mbarrier waits are bounded.
 //   * The channel pair's FH x FW filter lives in registers as fp32 pairs and
 //     is reloaded only when the channel tile changes (filter reuse across all
 //     spatial positions a thread computes, §3.2).
@@ -23,9 +24,11 @@ namespace {
 
 using namespace tiled;
 
-template <typename T, int FH, int FW, int TH, int TW, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB) tiled_small_kernel(TiledConv p, Geo g) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS>
+__global__ void __launch_bounds__(kThreads, MINB)
+    tiled_small_kernel(const __grid_constant__ CUtensorMap halo_map, TiledConv p, Geo g, unsigned *err) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bars[2];
     constexpr int WW = TW + FW - 1;  // input columns one thread reads per row
 
     const int tid = threadIdx.x;
@@ -35,27 +38,43 @@ __global__ void __launch_bounds__(kThreads, MINB) tiled_small_kernel(TiledConv p
     const int rt = (t / g.CT) % g.RT;
     const int ct = t % g.CT;
 
+    const unsigned box_bytes = halo_box_bytes(g, sizeof(T));
     const int halo_elems = g.HH * g.HW * 32;
-    T *sbuf0 = reinterpret_cast<T *>(smem_raw);
-    T *sbuf1 = sbuf0 + g.NI * halo_elems;
+    const unsigned buf_stride = align128(box_bytes);  // byte offset of stage buffer 1
     const T *wgt = static_cast<const T *>(p.w);
     T *out = static_cast<T *>(p.out);
     const int tile_rows = g.RT * TH, tile_cols = g.CT * TW;
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    // One thread issues the whole halo of a unit as a single tensor copy.
+    auto issue = [&](int u, int b) {
+        const Unit un = decode(g, u);
+        mbar_arrive_expect_tx(&bars[b], box_bytes);
+        tma_load_4d(smem_raw + b * buf_stride, &halo_map, un.ctile * 32, un.twi * tile_cols - p.pad_w,
+                    un.band * tile_rows - p.pad_h, un.group * g.NI, &bars[b]);
+    };
 
     float2 wr[FH][FW];
     float2 bias2 = make_float2(0.f, 0.f);
     int loaded_ctile = -1;
 
-    long long u = blockIdx.x;
-    if (u >= g.units) return;
-    stage_halo<T, TH, TW>(p, g, sbuf0, decode(g, u));
-    cp_async_commit();
+    int u = blockIdx.x;
+    if (tid == 0 && u < g.units) issue(u, 0);
     for (int k = 0; u < g.units; ++k, u += gridDim.x) {
-        const long long un = u + gridDim.x;
-        if (un < g.units) stage_halo<T, TH, TW>(p, g, (k & 1) ? sbuf0 : sbuf1, decode(g, un));
-        cp_async_commit();
-        cp_async_wait_1();
-        __syncthreads();
+        const int un = u + gridDim.x;
+        if (tid == 0 && un < g.units) issue(un, (k + 1) & 1);
+        if (!mbar_wait(&bars[k & 1], (k >> 1) & 1)) {
+            // Give up: record it, let the copy still in flight land, and leave.
+            report_timeout(err);
+            if (tid == 0 && un < g.units) mbar_wait(&bars[(k + 1) & 1], ((k + 1) >> 1) & 1);
+            return;
+        }
 
         const Unit cur = decode(g, u);
         const int c = cur.ctile * 32 + 2 * cp;
@@ -68,13 +87,13 @@ __global__ void __launch_bounds__(kThreads, MINB) tiled_small_kernel(TiledConv p
                 for (int fw = 0; fw < FW; ++fw) {
                     const int sfh = p.flip ? FH - 1 - fh : fh;
                     const int sfw = p.flip ? FW - 1 - fw : fw;
-                    wr[fh][fw] = cvalid ? Pair<T>::load(wgt + ((long long)sfh * FW + sfw) * p.C + c)
+                    wr[fh][fw] = cvalid ? Pair<T>::load(wgt + (sfh * FW + sfw) * p.C + c)
                                         : make_float2(0.f, 0.f);
                 }
             bias2 = (p.bias && cvalid) ? make_float2(p.bias[c], p.bias[c + 1]) : make_float2(0.f, 0.f);
         }
 
-        const T *s = ((k & 1) ? sbuf1 : sbuf0) + (long long)img_l * halo_elems;
+        const T *s = reinterpret_cast<const T *>(smem_raw + (k & 1) * buf_stride) + img_l * halo_elems;
         const int r0 = rt * TH, j0 = ct * TW;
         float2 acc[TH][TW];
 #pragma unroll
@@ -85,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, MINB) tiled_small_kernel(TiledConv p
 #pragma unroll
         for (int r = 0; r < TH + FH - 1; ++r) {
             float2 xv[WW];
-            const T *srow = s + ((long long)(r0 + r) * g.HW + j0) * 32 + 2 * cp;
+            const T *srow = s + ((r0 + r) * g.HW + j0) * 32 + 2 * cp;
 #pragma unroll
             for (int j = 0; j < WW; ++j) xv[j] = Pair<T>::load(srow + j * 32);
 #pragma unroll
@@ -104,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, MINB) tiled_small_kernel(TiledConv p
         if (cvalid && n < p.N) {
             const int i0 = cur.band * tile_rows + r0;
             const int jj0 = cur.twi * tile_cols + j0;
+            T *img = out + (long long)n * p.OHf * p.OWf * p.C + c;
 #pragma unroll
             for (int th = 0; th < TH; ++th) {
                 const int i = i0 + th;
@@ -112,34 +132,39 @@ __global__ void __launch_bounds__(kThreads, MINB) tiled_small_kernel(TiledConv p
                 for (int tw = 0; tw < TW; ++tw) {
                     const int j = jj0 + tw;
                     if (j >= p.OWs) break;
-                    const int orow = p.out_off + p.out_step * i;
-                    const int ocol = p.out_off + p.out_step * j;
-                    if (orow < p.OHf && ocol < p.OWf)
-                        Pair<T>::store(out + (((long long)n * p.OHf + orow) * p.OWf + ocol) * p.C + c,
-                                       acc[th][tw]);
-                    if (p.zero_phases) {
-                        for (int a = 0; a < p.out_step; ++a)
-                            for (int b = 0; b < p.out_step; ++b) {
-                                if (a == p.out_off && b == p.out_off) continue;
-                                const int zr = p.out_step * i + a, zc = p.out_step * j + b;
-                                if (zr < p.OHf && zc < p.OWf)
-                                    Pair<T>::store(out + (((long long)n * p.OHf + zr) * p.OWf + zc) * p.C + c,
-                                                   make_float2(0.f, 0.f));
+                    if (OS == 1) {
+                        Pair<T>::store(img + ((long long)i * p.OWf + j) * p.C, acc[th][tw]);
+                    } else {
+                        // Every position of the OS x OS block: the computed phase
+                        // gets the sum, the others get zero.
+#pragma unroll
+                        for (int a = 0; a < OS; ++a)
+#pragma unroll
+                            for (int b = 0; b < OS; ++b) {
+                                const int orow = OS * i + a, ocol = OS * j + b;
+                                if (orow < p.OHf && ocol < p.OWf) {
+                                    const bool hit = a == p.out_off && b == p.out_off;
+                                    Pair<T>::store(img + ((long long)orow * p.OWf + ocol) * p.C,
+                                                   hit ? acc[th][tw] : make_float2(0.f, 0.f));
+                                }
                             }
                     }
                 }
             }
         }
-        __syncthreads();  // this buffer is restaged two units from now
+        __syncthreads();  // this buffer is refilled by the copy issued next iteration
     }
 }
 
-template <typename T, int FH, int FW, int TH, int TW, int MINB>
-cudaError_t run(const TiledConv &p, cudaStream_t st) {
-    auto kern = tiled_small_kernel<T, FH, FW, TH, TW, MINB>;
+template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS>
+cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    auto kern = tiled_small_kernel<T, FH, FW, TH, TW, MINB, OS>;
     const Geo g = make_geo(p, TH, TW, sizeof(T), false, 100 * 1024);
+    if (g.units == 0) return cudaErrorNotSupported;
     const size_t smem = stage_bytes(g, TH, TW, sizeof(T), false);
     if (smem > 220 * 1024) return cudaErrorNotSupported;
+    CUtensorMap map;
+    if (!make_halo_map(&map, p, g, dt, sizeof(T))) return cudaErrorNotSupported;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -148,17 +173,25 @@ cudaError_t run(const TiledConv &p, cudaStream_t st) {
     if (per_sm < 1) return cudaErrorNotSupported;
     const long long slots = (long long)sm_count() * per_sm;
     const int grid = (int)std::min<long long>(g.units, slots);
-    kern<<<grid, kThreads, smem, st>>>(p, g);
+    kern<<<grid, kThreads, smem, st>>>(map, p, g, device_error_word());
     note_launches(1);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t dispatch_filter(const TiledConv &p, cudaStream_t st) {
-    if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, 4, 7, 2>(p, st);
-    if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2>(p, st);
-    if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3>(p, st);
-    if (p.FH == 3 && p.FW == 5) return run<T, 3, 5, 4, 7, 3>(p, st);
+cudaError_t dispatch_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    if (p.zero_phases) {
+        if (p.out_step != 2) return cudaErrorNotSupported;
+        if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 2>(p, dt, st);
+        if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 2>(p, dt, st);
+        if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, 4, 7, 2, 2>(p, dt, st);
+        return cudaErrorNotSupported;
+    }
+    if (p.out_step != 1) return cudaErrorNotSupported;
+    if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, 4, 7, 2, 1>(p, dt, st);
+    if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 1>(p, dt, st);
+    if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 1>(p, dt, st);
+    if (p.FH == 3 && p.FW == 5) return run<T, 3, 5, 4, 7, 3, 1>(p, dt, st);
     return cudaErrorNotSupported;
 }
 
@@ -166,9 +199,9 @@ cudaError_t dispatch_filter(const TiledConv &p, cudaStream_t st) {
 
 cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     switch (dt) {
-        case DWCONV_FP32: return dispatch_filter<float>(p, st);
-        case DWCONV_FP16: return dispatch_filter<__half>(p, st);
-        case DWCONV_BF16: return dispatch_filter<__nv_bfloat16>(p, st);
+        case DWCONV_FP32: return dispatch_filter<float>(p, dt, st);
+        case DWCONV_FP16: return dispatch_filter<__half>(p, dt, st);
+        case DWCONV_BF16: return dispatch_filter<__nv_bfloat16>(p, dt, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -7,8 +7,9 @@
 // long, so the work is split along the accumulation axis (§5.1
 // "accumulation-axis parallelisation"):
 //   * grid = channel tiles x Zc; CTA (ctile, z) takes the work units
-//     z, z + Zc, z + 2 Zc, ... of its channel tile, staging each unit's x halo
-//     and dy tile in shared memory with cp.async (double-buffered);
+//     z, z + Zc, z + 2 Zc, ... of its channel tile; one thread stages each
+//     unit's x halo and dy tile in shared memory with two TMA tensor copies on
+//     one mbarrier (double-buffered, bounded waits);
 //   * every thread keeps the FH x FW fp32 accumulators of its channel pair in
 //     registers for the whole CTA, and walks its window row-stationary: each
 //     x row is read once and feeds every (dy row, filter row) pair using it;
@@ -29,8 +30,10 @@ constexpr int kTargetCtas = 304;  // two CTAs on each of the 152 SMs of a GB300
 
 template <typename T, int FH, int FW, int TH, int TW, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
-    tiled_wgrad_kernel(TiledConv p, Geo g, float *__restrict__ part, int Zc) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    tiled_wgrad_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap dy_map,
+                       TiledConv p, Geo g, float *__restrict__ part, int Zc, unsigned *err) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bars[2];
     constexpr int WW = TW + FW - 1;
 
     const int tid = threadIdx.x;
@@ -43,14 +46,30 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int tile_rows = g.RT * TH, tile_cols = g.CT * TW;
     const int halo_elems = g.HH * g.HW * 32;
     const int otile_elems = tile_rows * tile_cols * 32;
-    const int stage_elems = g.NI * (halo_elems + otile_elems);
-    T *st0 = reinterpret_cast<T *>(smem_raw);
-    T *st1 = st0 + stage_elems;
-    const T *dy = static_cast<const T *>(p.dy);
+    const unsigned hb = halo_box_bytes(g, sizeof(T)), tb = tile_box_bytes(g, TH, TW, sizeof(T));
+    const unsigned stage = align128(hb) + align128(tb);
 
     const int ctile = blockIdx.x / Zc;
     const int z = blockIdx.x % Zc;
-    const long long base = (long long)ctile * g.per_ctile;
+    const int base = ctile * g.per_ctile;
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    // One thread issues both boxes of a unit (x halo, dy tile) on one barrier.
+    auto issue = [&](int v, int b) {
+        const Unit un = decode(g, base + v);
+        mbar_arrive_expect_tx(&bars[b], hb + tb);
+        unsigned char *dst = smem_raw + b * stage;
+        tma_load_4d(dst, &halo_map, un.ctile * 32, un.twi * tile_cols - p.pad_w,
+                    un.band * tile_rows - p.pad_h, un.group * g.NI, &bars[b]);
+        tma_load_4d(dst + align128(hb), &dy_map, un.ctile * 32, un.twi * tile_cols, un.band * tile_rows,
+                    un.group * g.NI, &bars[b]);
+    };
 
     float2 acc[FH][FW];
 #pragma unroll
@@ -58,55 +77,45 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
         for (int fw = 0; fw < FW; ++fw) acc[fh][fw] = make_float2(0.f, 0.f);
 
-    long long v = z;
-    if (v < g.per_ctile) {
-        {
-            const Unit u0 = decode(g, base + v);
-            stage_halo<T, TH, TW>(p, g, st0, u0);
-            stage_out_tile<T, TH, TW>(p, g, dy, st0 + g.NI * halo_elems, u0);
+    int v = z;
+    if (tid == 0 && v < g.per_ctile) issue(v, 0);
+    for (int k = 0; v < g.per_ctile; ++k, v += Zc) {
+        const int vn = v + Zc;
+        if (tid == 0 && vn < g.per_ctile) issue(vn, (k + 1) & 1);
+        if (!mbar_wait(&bars[k & 1], (k >> 1) & 1)) {
+            report_timeout(err);
+            if (tid == 0 && vn < g.per_ctile) mbar_wait(&bars[(k + 1) & 1], ((k + 1) >> 1) & 1);
+            return;
         }
-        cp_async_commit();
-        for (int k = 0; v < g.per_ctile; ++k, v += Zc) {
-            const long long vn = v + Zc;
-            if (vn < g.per_ctile) {
-                T *nb = (k & 1) ? st0 : st1;
-                const Unit un = decode(g, base + vn);
-                stage_halo<T, TH, TW>(p, g, nb, un);
-                stage_out_tile<T, TH, TW>(p, g, dy, nb + g.NI * halo_elems, un);
-            }
-            cp_async_commit();
-            cp_async_wait_1();
-            __syncthreads();
 
-            const T *buf = (k & 1) ? st1 : st0;
-            const T *sx = buf + (long long)img_l * halo_elems;
-            const T *sy = buf + (long long)g.NI * halo_elems + (long long)img_l * otile_elems;
-            const int r0 = rt * TH, j0 = ct * TW;
-            float2 dyv[TH][TW];
+        const unsigned char *cur = smem_raw + (k & 1) * stage;
+        const T *sx = reinterpret_cast<const T *>(cur) + img_l * halo_elems;
+        const T *sy = reinterpret_cast<const T *>(cur + align128(hb)) + img_l * otile_elems;
+        const int r0 = rt * TH, j0 = ct * TW;
+        float2 dyv[TH][TW];
 #pragma unroll
-            for (int th = 0; th < TH; ++th)
+        for (int th = 0; th < TH; ++th)
 #pragma unroll
-                for (int tw = 0; tw < TW; ++tw)
-                    dyv[th][tw] = Pair<T>::load(sy + ((long long)(r0 + th) * tile_cols + j0 + tw) * 32 + 2 * cp);
+            for (int tw = 0; tw < TW; ++tw)
+                dyv[th][tw] = Pair<T>::load(sy + ((r0 + th) * tile_cols + j0 + tw) * 32 + 2 * cp);
 #pragma unroll
-            for (int r = 0; r < TH + FH - 1; ++r) {
-                float2 xv[WW];
-                const T *srow = sx + ((long long)(r0 + r) * g.HW + j0) * 32 + 2 * cp;
+        for (int r = 0; r < TH + FH - 1; ++r) {
+            float2 xv[WW];
+            const T *srow = sx + ((r0 + r) * g.HW + j0) * 32 + 2 * cp;
 #pragma unroll
-                for (int j = 0; j < WW; ++j) xv[j] = Pair<T>::load(srow + j * 32);
+            for (int j = 0; j < WW; ++j) xv[j] = Pair<T>::load(srow + j * 32);
 #pragma unroll
-                for (int th = 0; th < TH; ++th) {
-                    const int fh = r - th;
-                    if (fh < 0 || fh >= FH) continue;
+            for (int th = 0; th < TH; ++th) {
+                const int fh = r - th;
+                if (fh < 0 || fh >= FH) continue;
 #pragma unroll
-                    for (int fw = 0; fw < FW; ++fw)
+                for (int fw = 0; fw < FW; ++fw)
 #pragma unroll
-                        for (int tw = 0; tw < TW; ++tw)
-                            acc[fh][fw] = __ffma2_rn(dyv[th][tw], xv[tw + fw], acc[fh][fw]);
-                }
+                    for (int tw = 0; tw < TW; ++tw)
+                        acc[fh][fw] = __ffma2_rn(dyv[th][tw], xv[tw + fw], acc[fh][fw]);
             }
-            __syncthreads();  // this buffer is restaged two units from now
         }
+        __syncthreads();  // this buffer is refilled by the copy issued next iteration
     }
 
     // Sum the 8 thread tiles that share each channel pair: lanes l and l^16 of a
@@ -145,27 +154,32 @@ __global__ void __launch_bounds__(kThreads, MINB)
 template <typename T, int FH, int FW, int TH, int TW>
 bool plan_geo(const TiledConv &p, Geo &g, int &Zc, size_t &smem) {
     g = make_geo(p, TH, TW, sizeof(T), true, 110 * 1024);
+    if (g.units == 0) return false;
     smem = stage_bytes(g, TH, TW, sizeof(T), true);
     const size_t red_bytes = (size_t)(kThreads / 32) * FH * FW * 16 * sizeof(float2);
     if (smem < red_bytes) smem = red_bytes;
     if (smem > 220 * 1024) return false;
-    long long z = kTargetCtas / g.ctiles;
+    int z = kTargetCtas / g.ctiles;
     if (z > g.per_ctile) z = g.per_ctile;
     if (z < 1) z = 1;
-    Zc = (int)z;
+    Zc = z;
     return true;
 }
 
 template <typename T, int FH, int FW, int TH, int TW, int MINB>
-cudaError_t run(const TiledConv &p, float *part, cudaStream_t st) {
+cudaError_t run(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st) {
     Geo g;
     int Zc;
     size_t smem;
     if (!plan_geo<T, FH, FW, TH, TW>(p, g, Zc, smem)) return cudaErrorNotSupported;
     auto kern = tiled_wgrad_kernel<T, FH, FW, TH, TW, MINB>;
+    CUtensorMap halo_map, dy_map;
+    if (!make_halo_map(&halo_map, p, g, dt, sizeof(T)) ||
+        !make_tile_map(&dy_map, p.dy, p, g, TH, TW, dt, sizeof(T)))
+        return cudaErrorNotSupported;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<g.ctiles * Zc, kThreads, smem, st>>>(p, g, part, Zc);
+    kern<<<g.ctiles * Zc, kThreads, smem, st>>>(halo_map, dy_map, p, g, part, Zc, device_error_word());
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -173,7 +187,7 @@ cudaError_t run(const TiledConv &p, float *part, cudaStream_t st) {
 }
 
 template <typename T>
-cudaError_t dispatch(const TiledConv &p, float *part, cudaStream_t st, int *Zc_out) {
+cudaError_t dispatch(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st, int *Zc_out) {
     Geo g;
     size_t smem;
     int Zc = 0;
@@ -186,9 +200,9 @@ cudaError_t dispatch(const TiledConv &p, float *part, cudaStream_t st, int *Zc_o
         *Zc_out = Zc;
         return cudaSuccess;
     }
-    if (p.FH == 7) return run<T, 7, 7, 4, 7, 2>(p, part, st);
-    if (p.FH == 5) return run<T, 5, 5, 4, 7, 2>(p, part, st);
-    return run<T, 3, 3, 4, 7, 3>(p, part, st);
+    if (p.FH == 7) return run<T, 7, 7, 4, 7, 2>(p, dt, part, st);
+    if (p.FH == 5) return run<T, 5, 5, 4, 7, 2>(p, dt, part, st);
+    return run<T, 3, 3, 4, 7, 3>(p, dt, part, st);
 }
 
 template <typename F>
@@ -206,13 +220,13 @@ cudaError_t by_dtype(dwconv_dtype dt, F &&f) {
 int tiled_wgrad_slices(const TiledConv &p, dwconv_dtype dt) {
     int Zc = 0;
     cudaError_t e = by_dtype(dt, [&](auto tag) {
-        return dispatch<decltype(tag)>(p, nullptr, nullptr, &Zc);
+        return dispatch<decltype(tag)>(p, dt, nullptr, nullptr, &Zc);
     });
     return e == cudaSuccess ? Zc : 0;
 }
 
 cudaError_t launch_tiled_wgrad(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st) {
-    return by_dtype(dt, [&](auto tag) { return dispatch<decltype(tag)>(p, part, st, nullptr); });
+    return by_dtype(dt, [&](auto tag) { return dispatch<decltype(tag)>(p, dt, part, st, nullptr); });
 }
 
 }  // namespace dwc

@@ -148,6 +148,11 @@ def dwconv_bwd_filter_static(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=Non
     return out
 
 
+def dwconv_check_device_errors(stream=None) -> None:
+    """Wait for the stream; raise DwconvError if a library kernel gave up a bounded wait."""
+    _lib.check(_lib.load().dwconv_check_device_errors(_stream(stream)), "dwconv_check_device_errors")
+
+
 def dwconv_launch_count() -> int:
     """Kernels libdwconv has launched in this process."""
     return int(_lib.load().dwconv_launch_count())

@@ -54,7 +54,7 @@ typedef enum {
     DWCONV_ERR_UNSUPPORTED = 2,  /* dtype/pass pair not provided (int8 backward) */
     DWCONV_ERR_MISALIGNED = 3,   /* a pointer not aligned to its element size */
     DWCONV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
-    DWCONV_ERR_TIMEOUT = 5       /* reserved: a bounded device-side wait gave up */
+    DWCONV_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up (see dwconv_check_device_errors) */
 } dwconv_status;
 
 typedef enum {
@@ -155,6 +155,17 @@ dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int 
 dwconv_status dwconv_bwd_filter_static(int N, int H, int W, int C, int FH, int FW, int stride,
                                        int dilation, int pad, dwconv_dtype dtype, const void *x,
                                        const void *dy, float *dw, dwconv_stream stream);
+
+/*
+ * Waits for `stream`, then reports whether any kernel of this library on the
+ * current device gave up a bounded wait since the last check: the kernels
+ * that stage tiles with TMA wait on shared-memory barriers for a bounded
+ * number of polls (seconds), and on running out they record the fact and
+ * return instead of hanging.  Returns DWCONV_ERR_TIMEOUT (and clears the
+ * record) if that happened, DWCONV_ERR_CUDA if the stream reports an error,
+ * DWCONV_OK otherwise.
+ */
+dwconv_status dwconv_check_device_errors(dwconv_stream stream);
 
 /* A static, human-readable name for a status code. */
 const char *dwconv_status_string(dwconv_status status);

@@ -103,7 +103,7 @@ def check_fwd(d, dtype, S, D, P, images=None, what="fwd"):
     out_dtype = torch.int32 if dtype == "int8" else TORCH[dtype]
     g = Guarded((N, OH, OW, C), out_dtype)
     y = ops.dwconv_fwd(x.cuda(), w.cuda(), None if b is None else b.cuda(), S, D, P, out=g.t)
-    torch.cuda.synchronize()
+    ops.dwconv_check_device_errors()
     g.check(what)
     imgs = list(range(N)) if images is None else sorted(set(i % N for i in images))
     ref, mag = oracle.fwd(to64(x[imgs]), to64(w), None if b is None else to64(b), S, D, P)
@@ -115,7 +115,7 @@ def check_dgrad(d, dtype, S, D, P, images=None, what="dgrad"):
     N, H, W, C = d["x"].shape
     g = Guarded((N, H, W, C), TORCH[dtype])
     dx = ops.dwconv_bwd_data(dy.cuda(), w.cuda(), H, W, S, D, P, out=g.t)
-    torch.cuda.synchronize()
+    ops.dwconv_check_device_errors()
     g.check(what)
     imgs = list(range(N)) if images is None else sorted(set(i % N for i in images))
     ref, mag = oracle.dgrad(to64(dy[imgs]), to64(w), H, W, S, D, P)
@@ -127,7 +127,7 @@ def check_wgrad(d, dtype, S, D, P, what="wgrad"):
     FH, FW, C = d["w"].shape
     g = Guarded((FH, FW, C), torch.float32)
     dw = ops.dwconv_bwd_filter(x.cuda(), dy.cuda(), FH, FW, S, D, P, out=g.t)
-    torch.cuda.synchronize()
+    ops.dwconv_check_device_errors()
     g.check(what)
     ref, mag = oracle.wgrad(to64(x), to64(dy), FH, FW, S, D, P)
     return compare(to64(dw), ref, mag, dtype, False, what)
