@@ -39,7 +39,8 @@ class DwconvError(RuntimeError):
 
 
 def lib_path() -> str:
-    return _build.LIB
+    """The in-tree library, or the build named by DWCONV_LIB (for A/B timing)."""
+    return os.environ.get("DWCONV_LIB") or _build.LIB
 
 
 def load(build_if_missing: bool = True):
@@ -47,7 +48,7 @@ def load(build_if_missing: bool = True):
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB
+            path = lib_path()
             if not os.path.exists(path):
                 if not build_if_missing:
                     raise RuntimeError(f"libdwconv.so is not built ({path}); run "

@@ -54,6 +54,48 @@ template <> struct Pair<__nv_bfloat16> {
     }
 };
 
+// Multiply-accumulate on a channel pair, per storage type.  A pair is held in
+// registers as it is stored: fp32 data as float2, 16-bit data as one packed
+// 32-bit word.  fp32 uses the packed fma.rn.f32x2; 16-bit data uses the
+// sm_100+ mixed-precision fma.rn.f32.{f16,bf16}, whose 16 x 16-bit product is
+// exact in fp32 and is added to the fp32 accumulator with one rounding -- the
+// same result as widening first and using an fp32 FMA, without the widening
+// instructions.
+template <typename T> struct Mac;
+
+template <> struct Mac<float> {
+    using V = float2;
+    static __device__ __forceinline__ V load(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+    static __device__ __forceinline__ V zero() { return make_float2(0.f, 0.f); }
+    static __device__ __forceinline__ void fma(float2 &acc, V a, V b) { acc = __ffma2_rn(a, b, acc); }
+};
+
+template <> struct Mac<__half> {
+    using V = unsigned;
+    static __device__ __forceinline__ V load(const __half *p) { return *reinterpret_cast<const unsigned *>(p); }
+    static __device__ __forceinline__ V zero() { return 0u; }
+    static __device__ __forceinline__ void fma(float2 &acc, V a, V b) {
+        asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
+            " fma.rn.f32.f16 %0, al, bl, %0;\n fma.rn.f32.f16 %1, ah, bh, %1;\n}\n"
+            : "+f"(acc.x), "+f"(acc.y)
+            : "r"(a), "r"(b));
+    }
+};
+
+template <> struct Mac<__nv_bfloat16> {
+    using V = unsigned;
+    static __device__ __forceinline__ V load(const __nv_bfloat16 *p) {
+        return *reinterpret_cast<const unsigned *>(p);
+    }
+    static __device__ __forceinline__ V zero() { return 0u; }
+    static __device__ __forceinline__ void fma(float2 &acc, V a, V b) {
+        asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
+            " fma.rn.f32.bf16 %0, al, bl, %0;\n fma.rn.f32.bf16 %1, ah, bh, %1;\n}\n"
+            : "+f"(acc.x), "+f"(acc.y)
+            : "r"(a), "r"(b));
+    }
+};
+
 // Scalar widening / rounding (round to nearest even for 16-bit outputs).
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }

@@ -4,14 +4,15 @@
 //   * Work units, CTA shape and halo staging: see tiled_common.cuh.  Two
 //     stage buffers: thread 0 issues the next unit's halo as one TMA tensor
 //     copy while the CTA computes this one; mbarrier waits are bounded.
-//   * The channel pair's FH x FW filter lives in registers as fp32 pairs and
+//   * The channel pair's FH x FW filter lives in registers (as stored) and
 //     is reloaded only when the channel tile changes (filter reuse across all
 //     spatial positions a thread computes, §3.2).
 //   * Width-first register reuse (§3.3): the thread walks the TH+FH-1 input
 //     rows of its window once; each row's TW+FW-1 values are read from shared
 //     memory once, widened to fp32 once, and feed every (output row, filter
-//     row) pair that uses that input row.  Each multiply-add is a packed
-//     fma.rn.f32x2 over the channel pair, accumulating in fp32.
+//     row) pair that uses that input row.  Multiply-adds accumulate in fp32
+//     (Mac<T> in common.cuh: fma.rn.f32x2 for fp32 data, the mixed-precision
+//     fma.rn.f32.{f16,bf16} on packed 16-bit pairs otherwise).
 //   * Persistent grid: as many CTAs as fit on the SMs, each taking work units
 //     round-robin, so the last wave is at most one unit deep.
 //   * Epilogue: bias added once (forward only), round to the storage type,
@@ -23,6 +24,27 @@ namespace dwc {
 namespace {
 
 using namespace tiled;
+
+// Tile choices per dtype class: thread tile TH x TW, CTAs per SM the register
+// budget is sized for (MINB), and the cap on the double-buffered halo.
+#ifndef DWCONV_S16_MINB
+#define DWCONV_S16_MINB 4
+#endif
+#ifndef DWCONV_S16_SMEM_KB
+#define DWCONV_S16_SMEM_KB 48
+#endif
+#ifndef DWCONV_S16_TH
+#define DWCONV_S16_TH 2
+#endif
+#ifndef DWCONV_S16_TW
+#define DWCONV_S16_TW 7
+#endif
+
+template <typename T>
+size_t smem_cap() {
+    return sizeof(T) == 4 ? 100 * 1024 : DWCONV_S16_SMEM_KB * 1024;
+}
+
 
 template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS>
 __global__ void __launch_bounds__(kThreads, MINB)
@@ -60,7 +82,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     un.band * tile_rows - p.pad_h, un.group * g.NI, &bars[b]);
     };
 
-    float2 wr[FH][FW];
+    using M = Mac<T>;
+    typename M::V wr[FH][FW];
     float2 bias2 = make_float2(0.f, 0.f);
     int loaded_ctile = -1;
 
@@ -87,8 +110,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 for (int fw = 0; fw < FW; ++fw) {
                     const int sfh = p.flip ? FH - 1 - fh : fh;
                     const int sfw = p.flip ? FW - 1 - fw : fw;
-                    wr[fh][fw] = cvalid ? Pair<T>::load(wgt + (sfh * FW + sfw) * p.C + c)
-                                        : make_float2(0.f, 0.f);
+                    wr[fh][fw] = cvalid ? M::load(wgt + (sfh * FW + sfw) * p.C + c) : M::zero();
                 }
             bias2 = (p.bias && cvalid) ? make_float2(p.bias[c], p.bias[c + 1]) : make_float2(0.f, 0.f);
         }
@@ -103,10 +125,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
 #pragma unroll
         for (int r = 0; r < TH + FH - 1; ++r) {
-            float2 xv[WW];
+            typename M::V xv[WW];
             const T *srow = s + ((r0 + r) * g.HW + j0) * 32 + 2 * cp;
 #pragma unroll
-            for (int j = 0; j < WW; ++j) xv[j] = Pair<T>::load(srow + j * 32);
+            for (int j = 0; j < WW; ++j) xv[j] = M::load(srow + j * 32);
 #pragma unroll
             for (int th = 0; th < TH; ++th) {
                 const int fh = r - th;
@@ -115,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 for (int fw = 0; fw < FW; ++fw)
 #pragma unroll
                     for (int tw = 0; tw < TW; ++tw)
-                        acc[th][tw] = __ffma2_rn(wr[fh][fw], xv[tw + fw], acc[th][tw]);
+                        M::fma(acc[th][tw], wr[fh][fw], xv[tw + fw]);
             }
         }
 
@@ -159,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS>
 cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     auto kern = tiled_small_kernel<T, FH, FW, TH, TW, MINB, OS>;
-    const Geo g = make_geo(p, TH, TW, sizeof(T), false, 100 * 1024);
+    const Geo g = make_geo(p, TH, TW, sizeof(T), false, smem_cap<T>());
     if (g.units == 0) return cudaErrorNotSupported;
     const size_t smem = stage_bytes(g, TH, TW, sizeof(T), false);
     if (smem > 220 * 1024) return cudaErrorNotSupported;
@@ -180,15 +202,18 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
 
 template <typename T>
 cudaError_t dispatch_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    constexpr bool k16 = sizeof(T) == 2;
+    constexpr int TH7 = k16 ? DWCONV_S16_TH : 4, TW7 = k16 ? DWCONV_S16_TW : 7;
+    constexpr int MB7 = k16 ? DWCONV_S16_MINB : 2;
     if (p.zero_phases) {
         if (p.out_step != 2) return cudaErrorNotSupported;
         if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 2>(p, dt, st);
         if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 2>(p, dt, st);
-        if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, 4, 7, 2, 2>(p, dt, st);
+        if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7, 2>(p, dt, st);
         return cudaErrorNotSupported;
     }
     if (p.out_step != 1) return cudaErrorNotSupported;
-    if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, 4, 7, 2, 1>(p, dt, st);
+    if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7, 1>(p, dt, st);
     if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 1>(p, dt, st);
     if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 1>(p, dt, st);
     if (p.FH == 3 && p.FW == 5) return run<T, 3, 5, 4, 7, 3, 1>(p, dt, st);

@@ -13,7 +13,7 @@
 //   * every thread keeps the FH x FW fp32 accumulators of its channel pair in
 //     registers for the whole CTA, and walks its window row-stationary: each
 //     x row is read once and feeds every (dy row, filter row) pair using it;
-//     each multiply-add is a packed fma.rn.f32x2;
+//     multiply-adds accumulate in fp32 (Mac<T> in common.cuh);
 //   * at the end the 8 thread tiles sharing a channel pair are summed with a
 //     warp shuffle and a fixed-order pass through shared memory, and the CTA
 //     writes part[z][fh*FW+fw][c];
@@ -26,7 +26,23 @@ namespace {
 
 using namespace tiled;
 
-constexpr int kTargetCtas = 304;  // two CTAs on each of the 152 SMs of a GB300
+// Tile choices for 16-bit data: thread tile TH x TW, CTAs per SM the
+// register budget is sized for (MINB), cap on the double-buffered stage.
+#ifndef DWCONV_W16_MINB
+#define DWCONV_W16_MINB 3
+#endif
+#ifndef DWCONV_W16_SMEM_KB
+#define DWCONV_W16_SMEM_KB 72
+#endif
+#ifndef DWCONV_W16_TH
+#define DWCONV_W16_TH 2
+#endif
+#ifndef DWCONV_W16_TW
+#define DWCONV_W16_TW 7
+#endif
+
+// Work is split into about this many CTAs (resident CTAs x 152 SMs of a GB300).
+constexpr int kTargetCtas(bool k16) { return 152 * (k16 ? DWCONV_W16_MINB : 2); }
 
 template <typename T, int FH, int FW, int TH, int TW, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
@@ -92,18 +108,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const T *sx = reinterpret_cast<const T *>(cur) + img_l * halo_elems;
         const T *sy = reinterpret_cast<const T *>(cur + align128(hb)) + img_l * otile_elems;
         const int r0 = rt * TH, j0 = ct * TW;
-        float2 dyv[TH][TW];
+        using M = Mac<T>;
+        typename M::V dyv[TH][TW];
 #pragma unroll
         for (int th = 0; th < TH; ++th)
 #pragma unroll
             for (int tw = 0; tw < TW; ++tw)
-                dyv[th][tw] = Pair<T>::load(sy + ((r0 + th) * tile_cols + j0 + tw) * 32 + 2 * cp);
+                dyv[th][tw] = M::load(sy + ((r0 + th) * tile_cols + j0 + tw) * 32 + 2 * cp);
 #pragma unroll
         for (int r = 0; r < TH + FH - 1; ++r) {
-            float2 xv[WW];
+            typename M::V xv[WW];
             const T *srow = sx + ((r0 + r) * g.HW + j0) * 32 + 2 * cp;
 #pragma unroll
-            for (int j = 0; j < WW; ++j) xv[j] = Pair<T>::load(srow + j * 32);
+            for (int j = 0; j < WW; ++j) xv[j] = M::load(srow + j * 32);
 #pragma unroll
             for (int th = 0; th < TH; ++th) {
                 const int fh = r - th;
@@ -112,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 for (int fw = 0; fw < FW; ++fw)
 #pragma unroll
                     for (int tw = 0; tw < TW; ++tw)
-                        acc[fh][fw] = __ffma2_rn(dyv[th][tw], xv[tw + fw], acc[fh][fw]);
+                        M::fma(acc[fh][fw], dyv[th][tw], xv[tw + fw]);
             }
         }
         __syncthreads();  // this buffer is refilled by the copy issued next iteration
@@ -153,13 +170,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
 // Shape-only plan: which instance, its geometry, and the slice count Zc.
 template <typename T, int FH, int FW, int TH, int TW>
 bool plan_geo(const TiledConv &p, Geo &g, int &Zc, size_t &smem) {
-    g = make_geo(p, TH, TW, sizeof(T), true, 110 * 1024);
+    g = make_geo(p, TH, TW, sizeof(T), true, sizeof(T) == 2 ? DWCONV_W16_SMEM_KB * 1024 : 110 * 1024);
     if (g.units == 0) return false;
     smem = stage_bytes(g, TH, TW, sizeof(T), true);
     const size_t red_bytes = (size_t)(kThreads / 32) * FH * FW * 16 * sizeof(float2);
     if (smem < red_bytes) smem = red_bytes;
     if (smem > 220 * 1024) return false;
-    int z = kTargetCtas / g.ctiles;
+    int z = kTargetCtas(sizeof(T) == 2) / g.ctiles;
     if (z > g.per_ctile) z = g.per_ctile;
     if (z < 1) z = 1;
     Zc = z;
@@ -188,11 +205,14 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t s
 
 template <typename T>
 cudaError_t dispatch(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st, int *Zc_out) {
+    constexpr bool k16 = sizeof(T) == 2;
+    constexpr int TH7 = k16 ? DWCONV_W16_TH : 4, TW7 = k16 ? DWCONV_W16_TW : 7;
+    constexpr int MB7 = k16 ? DWCONV_W16_MINB : 2;
     Geo g;
     size_t smem;
     int Zc = 0;
     bool ok = false;
-    if (p.FH == 7 && p.FW == 7) ok = plan_geo<T, 7, 7, 4, 7>(p, g, Zc, smem);
+    if (p.FH == 7 && p.FW == 7) ok = plan_geo<T, 7, 7, TH7, TW7>(p, g, Zc, smem);
     else if (p.FH == 5 && p.FW == 5) ok = plan_geo<T, 5, 5, 4, 7>(p, g, Zc, smem);
     else if (p.FH == 3 && p.FW == 3) ok = plan_geo<T, 3, 3, 4, 7>(p, g, Zc, smem);
     if (!ok) return cudaErrorNotSupported;
@@ -200,7 +220,7 @@ cudaError_t dispatch(const TiledConv &p, dwconv_dtype dt, float *part, cudaStrea
         *Zc_out = Zc;
         return cudaSuccess;
     }
-    if (p.FH == 7) return run<T, 7, 7, 4, 7, 2>(p, dt, part, st);
+    if (p.FH == 7) return run<T, 7, 7, TH7, TW7, MB7>(p, dt, part, st);
     if (p.FH == 5) return run<T, 5, 5, 4, 7, 2>(p, dt, part, st);
     return run<T, 3, 3, 4, 7, 3>(p, dt, part, st);
 }
