@@ -149,6 +149,9 @@ struct TiledConv {
 // Returns cudaErrorNotSupported when no tiled instance covers the request.
 cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 
+// Large filters (FW >= 8, any FH), forward and stride-1 input gradient.
+cudaError_t launch_tiled_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
+
 // Weight gradient on the tiled path: slices of the accumulation axis for this
 // shape (0 if no tiled instance covers it; depends on the shape only), and the
 // launch (partials into part[Zc][FH*FW][C], then the fixed-order reduction

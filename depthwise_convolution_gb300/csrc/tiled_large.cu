@@ -1,0 +1,278 @@
+// Register-tiled forward pass and stride-1 input gradient for large filters
+// (FW >= 8, e.g. 31x31), any FH x FW at run time.
+//
+// The filter of a 32-channel slab (FH*FW*32 values) no longer fits in
+// registers, so the roles change relative to tiled_small.cu:
+//   * The slab's whole filter is staged once in shared memory by one TMA
+//     tensor copy and reloaded only when the CTA moves to another channel
+//     tile (filter reuse across every output the CTA computes, Flash-DWC §3.2).
+//   * Input rows stream through a ring of NS shared-memory slots, one TMA
+//     copy per row with zero fill outside the input (padding generated).  A
+//     CTA computes an output tile of RT*TH rows, so it walks RT*TH+FH-1 input
+//     rows; each row feeds every (output row, filter row) pair that uses it.
+//   * Width-first register reuse (§3.3, §3.4): for one input row a thread
+//     slides a TW-wide register window along the filter width -- one new input
+//     value per filter column -- and each filter value it reads from shared
+//     memory feeds TW multiply-adds; TH output rows share each input value.
+//   * CTA = 256 threads = 16 channel pairs x 16 thread tiles (NI images x RT
+//     rows x CT columns of TH x TW tiles; the two tiles of a warp share a tile
+//     row, so the filter reads of a warp are broadcasts).
+//   * Persistent CTAs take contiguous ranges of work units (channel tile
+//     slowest) so that filter reloads are rare.
+#include "tiled_common.cuh"
+
+namespace dwc {
+namespace {
+
+using namespace tiled;
+
+constexpr int kLThreads = 256;
+constexpr int kLTiles = kLThreads / kPairs;  // 16
+constexpr int kNS = 4;                       // input-row ring slots
+
+struct GeoL {
+    int NI, RT, CT;        // thread tiles: images x rows x columns (product 16)
+    int HW;                // halo columns per image
+    int R;                 // input rows walked per unit: RT*TH + FH - 1
+    int tiles_h, tiles_w, groups, ctiles;
+    int per_ctile, units;
+    unsigned filt_bytes;   // FH*FW*32 elements
+    unsigned row_bytes;    // NI*HW*32 elements
+};
+
+__device__ __forceinline__ Unit decode_l(const GeoL &g, int u) {
+    Unit r;
+    r.ctile = u / g.per_ctile;
+    int v = u - r.ctile * g.per_ctile;
+    r.band = v % g.tiles_h;
+    v /= g.tiles_h;
+    r.twi = v % g.tiles_w;
+    r.group = v / g.tiles_w;
+    return r;
+}
+
+template <typename T, int TH, int TW, int MINB>
+__global__ void __launch_bounds__(kLThreads, MINB)
+    tiled_large_kernel(const __grid_constant__ CUtensorMap row_map, const __grid_constant__ CUtensorMap filt_map,
+                       TiledConv p, GeoL g, unsigned *err) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bars[kNS + 1];  // ring slots, then the filter
+    using M = Mac<T>;
+    using V = typename M::V;
+
+    const int tid = threadIdx.x;
+    const int cp = tid % kPairs;
+    const int t = tid / kPairs;
+    const int ct = t % g.CT;
+    const int rt = (t / g.CT) % g.RT;
+    const int img_l = t / (g.CT * g.RT);
+
+    const T *filt = reinterpret_cast<const T *>(smem_raw);
+    unsigned char *ring = smem_raw + align128(g.filt_bytes);
+    const unsigned slot_bytes = align128(g.row_bytes);
+    T *out = static_cast<T *>(p.out);
+    const int tile_rows = g.RT * TH, tile_cols = g.CT * TW;
+
+    // Contiguous unit range of this CTA.
+    const int u_begin = (int)((long long)g.units * blockIdx.x / gridDim.x);
+    const int u_end = (int)((long long)g.units * (blockIdx.x + 1) / gridDim.x);
+    const int steps = (u_end - u_begin) * g.R;
+
+    if (tid == 0) {
+        for (int i = 0; i <= kNS; ++i) mbar_init(&bars[i], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    auto issue_row = [&](int q) {
+        const Unit un = decode_l(g, u_begin + q / g.R);
+        const int r = q % g.R;
+        const int s = q % kNS;
+        mbar_arrive_expect_tx(&bars[s], g.row_bytes);
+        tma_load_4d(ring + s * slot_bytes, &row_map, un.ctile * 32, un.twi * tile_cols - p.pad_w,
+                    un.band * tile_rows - p.pad_h + r, un.group * g.NI, &bars[s]);
+    };
+
+    if (tid == 0)
+        for (int q = 0; q < kNS - 1 && q < steps; ++q) issue_row(q);
+
+    int loaded_ctile = -1, filt_loads = 0;
+    float2 acc[TH][TW];
+    float2 bias2 = make_float2(0.f, 0.f);
+    Unit cur{};
+    int c = 0;
+
+    for (int q = 0; q < steps; ++q) {
+        const int r = q % g.R;
+        if (r == 0) {  // a new unit: filter (if the channel tile changed), bias, accumulators
+            cur = decode_l(g, u_begin + q / g.R);
+            c = cur.ctile * 32 + 2 * cp;
+            if (cur.ctile != loaded_ctile) {
+                // Every thread is past its last read of the old filter (the
+                // barrier at the end of the previous step).
+                if (tid == 0) {
+                    mbar_arrive_expect_tx(&bars[kNS], g.filt_bytes);
+                    tma_load_4d(smem_raw, &filt_map, cur.ctile * 32, 0, 0, 0, &bars[kNS]);
+                }
+                if (!mbar_wait(&bars[kNS], filt_loads & 1)) {
+                    report_timeout(err);
+                    return;
+                }
+                ++filt_loads;
+                loaded_ctile = cur.ctile;
+            }
+            bias2 = (p.bias && c < p.C) ? make_float2(p.bias[c], p.bias[c + 1]) : make_float2(0.f, 0.f);
+#pragma unroll
+            for (int th = 0; th < TH; ++th)
+#pragma unroll
+                for (int tw = 0; tw < TW; ++tw) acc[th][tw] = bias2;
+        }
+        if (tid == 0 && q + kNS - 1 < steps) issue_row(q + kNS - 1);
+        if (!mbar_wait(&bars[q % kNS], (q / kNS) & 1)) {
+            // Give up: record it, let the copies this thread issued land, leave.
+            report_timeout(err);
+            if (tid == 0)
+                for (int o = q + 1; o < q + kNS && o < steps; ++o) mbar_wait(&bars[o % kNS], (o / kNS) & 1);
+            return;
+        }
+
+        // Filter rows this thread's output rows need from input row r.
+        const int fh0 = r - rt * TH;  // filter row of output row th = 0
+        bool any = false;
+#pragma unroll
+        for (int th = 0; th < TH; ++th) any |= (fh0 - th >= 0 && fh0 - th < p.FH);
+        if (any) {
+            const T *xrow = reinterpret_cast<const T *>(ring + (q % kNS) * slot_bytes) +
+                            (img_l * g.HW + ct * TW) * 32 + 2 * cp;
+            const T *wrow[TH];
+            bool valid[TH];
+#pragma unroll
+            for (int th = 0; th < TH; ++th) {
+                const int fh = fh0 - th;
+                valid[th] = fh >= 0 && fh < p.FH;
+                const int sfh = p.flip ? p.FH - 1 - fh : fh;
+                wrow[th] = filt + ((valid[th] ? sfh : 0) * p.FW) * 32 + 2 * cp;
+            }
+            V xw[TW];
+#pragma unroll
+            for (int k = 0; k < TW; ++k) xw[k] = M::load(xrow + k * 32);
+            // Filter columns in blocks of TW so the window slot of each input
+            // value is a compile-time index.
+            for (int fb = 0; fb < p.FW; fb += TW) {
+#pragma unroll
+                for (int k = 0; k < TW; ++k) {
+                    const int fw = fb + k;
+                    if (fw < p.FW) {
+                        const int sfw = p.flip ? p.FW - 1 - fw : fw;
+                        V wv[TH];
+#pragma unroll
+                        for (int th = 0; th < TH; ++th)
+                            wv[th] = valid[th] ? M::load(wrow[th] + sfw * 32) : M::zero();
+#pragma unroll
+                        for (int th = 0; th < TH; ++th)
+#pragma unroll
+                            for (int tw = 0; tw < TW; ++tw) M::fma(acc[th][tw], wv[th], xw[(tw + k) % TW]);
+                        // x[fw] is no longer needed; its slot takes x[fw + TW].
+                        if (fw + TW < TW + p.FW - 1) xw[k] = M::load(xrow + (fw + TW) * 32);
+                    }
+                }
+            }
+        }
+
+        if (r == g.R - 1) {  // unit done: store
+            const int n = cur.group * g.NI + img_l;
+            if (c < p.C && n < p.N) {
+                const int i0 = cur.band * tile_rows + rt * TH;
+                const int j0 = cur.twi * tile_cols + ct * TW;
+                T *img = out + (long long)n * p.OHf * p.OWf * p.C + c;
+#pragma unroll
+                for (int th = 0; th < TH; ++th) {
+                    const int i = i0 + th;
+                    if (i >= p.OHs) break;
+#pragma unroll
+                    for (int tw = 0; tw < TW; ++tw) {
+                        const int j = j0 + tw;
+                        if (j >= p.OWs) break;
+                        Pair<T>::store(img + ((long long)i * p.OWf + j) * p.C, acc[th][tw]);
+                    }
+                }
+            }
+        }
+        __syncthreads();  // slot q % kNS is refilled at the next step; the filter may be too
+    }
+}
+
+template <typename T, int TH, int TW>
+bool plan(const TiledConv &p, GeoL &g, size_t &smem) {
+    g = GeoL{};
+    auto arrange = [&](int CT) {
+        g.CT = CT;
+        g.RT = std::min(kLTiles / g.CT, next_pow2((p.OHs + TH - 1) / TH));
+        g.NI = kLTiles / (g.CT * g.RT);
+    };
+    arrange(std::min(kLTiles, next_pow2((p.OWs + TW - 1) / TW)));
+    g.HW = g.CT * TW + p.FW - 1;
+    g.R = g.RT * TH + p.FH - 1;
+    g.tiles_h = (p.OHs + g.RT * TH - 1) / (g.RT * TH);
+    g.tiles_w = (p.OWs + g.CT * TW - 1) / (g.CT * TW);
+    g.groups = (p.N + g.NI - 1) / g.NI;
+    g.ctiles = (p.C + 31) / 32;
+    const long long per = (long long)g.groups * g.tiles_w * g.tiles_h;
+    if (per * g.ctiles >= (1LL << 30) || per * g.ctiles * g.R >= (1LL << 31)) return false;
+    g.per_ctile = (int)per;
+    g.units = (int)(per * g.ctiles);
+    g.filt_bytes = (unsigned)((size_t)p.FH * p.FW * 32 * sizeof(T));
+    g.row_bytes = (unsigned)((size_t)g.NI * g.HW * 32 * sizeof(T));
+    if (p.FH > 256 || p.FW > 256 || g.HW > 256) return false;  // TMA box limits
+    smem = align128(g.filt_bytes) + (size_t)kNS * align128(g.row_bytes);
+    return smem <= 220 * 1024;
+}
+
+template <typename T, int TH, int TW, int MINB>
+cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    GeoL g;
+    size_t smem;
+    if (!plan<T, TH, TW>(p, g, smem)) return cudaErrorNotSupported;
+    // Input rows: the taps' sub-grid of p.in, one row of the unit's halo per box.
+    const size_t es = sizeof(T);
+    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off * p.Wf + p.in_off) * p.C * es;
+    const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
+    const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
+                             (uint64_t)p.Hf * p.Wf * p.C * es};
+    const uint32_t box[4] = {32, (uint32_t)g.HW, 1, (uint32_t)g.NI};
+    // Filter [FH][FW][C] as a 4-D tensor with a unit outer dimension; one box =
+    // the whole filter of a 32-channel slab.
+    const uint64_t fdims[4] = {(uint64_t)p.C, (uint64_t)p.FW, (uint64_t)p.FH, 1};
+    const uint64_t fstr[3] = {(uint64_t)p.C * es, (uint64_t)p.FW * p.C * es, (uint64_t)p.FH * p.FW * p.C * es};
+    const uint32_t fbox[4] = {32, (uint32_t)p.FW, (uint32_t)p.FH, 1};
+    CUtensorMap row_map, filt_map;
+    if (!encode_tmap_4d(&row_map, dt, base, dims, str, box) ||
+        !encode_tmap_4d(&filt_map, dt, p.w, fdims, fstr, fbox))
+        return cudaErrorNotSupported;
+    auto kern = tiled_large_kernel<T, TH, TW, MINB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    const long long slots = (long long)sm_count() * per_sm;
+    const int grid = (int)std::min<long long>(g.units, slots);
+    kern<<<grid, kLThreads, smem, st>>>(row_map, filt_map, p, g, device_error_word());
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tiled_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    if (p.FW < 8 || p.zero_phases || p.out_step != 1) return cudaErrorNotSupported;
+    switch (dt) {
+        case DWCONV_FP32: return run<float, 2, 14, 1>(p, dt, st);
+        case DWCONV_FP16: return run<__half, 2, 14, 2>(p, dt, st);
+        case DWCONV_BF16: return run<__nv_bfloat16, 2, 14, 2>(p, dt, st);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace dwc

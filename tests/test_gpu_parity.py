@@ -32,6 +32,9 @@ SMALL = [
     (1, 6, 6, 16, 3, 3, 3, 1, 1),        # stride 3
     (2, 9, 8, 16, 3, 5, 1, 1, 2),        # FH != FW on the tiled path (pads differ by axis)
     (1, 11, 11, 2, 3, 3, 1, 1, 1),       # C = 2
+    (2, 20, 19, 40, 9, 13, 1, 1, 5),     # large-filter path, FH != FW, channel tail
+    (1, 33, 30, 64, 11, 11, 2, 2, 10),   # large filter on the stride-2 dilation-2 sub-grid
+    (3, 9, 30, 32, 15, 15, 1, 1, 7),     # large filter, map shorter than the filter
 ]
 
 
