@@ -10,6 +10,11 @@
 //     copy per row with zero fill outside the input (padding generated).  A
 //     CTA computes an output tile of RT*TH rows, so it walks RT*TH+FH-1 input
 //     rows; each row feeds every (output row, filter row) pair that uses it.
+//   * Warp-specialised pipeline: a ninth warp only issues copies; the eight
+//     compute warps wait on per-slot "full" mbarriers and release slots on
+//     "empty" mbarriers, so a warp whose output rows do not touch the current
+//     input row moves on instead of idling at a CTA-wide barrier.  All waits
+//     are bounded (tma.cuh).
 //   * Width-first register reuse (§3.3, §3.4): for one input row a thread
 //     slides a TW-wide register window along the filter width -- one new input
 //     value per filter column -- and each filter value it reads from shared
@@ -28,7 +33,28 @@ using namespace tiled;
 
 constexpr int kLThreads = 256;
 constexpr int kLTiles = kLThreads / kPairs;  // 16
-constexpr int kNS = 4;                       // input-row ring slots
+// Thread tile TH x TW; DWCONV_L_FW31 also builds a fully unrolled 31-wide
+// instance; DWCONV_L_SKIP_PAD_ROWS skips input rows that are all padding.
+#ifndef DWCONV_L_TH
+#define DWCONV_L_TH 2
+#endif
+#ifndef DWCONV_L_TW
+#define DWCONV_L_TW 14
+#endif
+#ifndef DWCONV_L_FW31
+#define DWCONV_L_FW31 0
+#endif
+#ifndef DWCONV_L_MAXR16
+#define DWCONV_L_MAXR16 96
+#endif
+#ifndef DWCONV_L_NS
+#define DWCONV_L_NS 8
+#endif
+#ifndef DWCONV_L_SKIP_PAD_ROWS
+#define DWCONV_L_SKIP_PAD_ROWS 0
+#endif
+
+constexpr int kNS = DWCONV_L_NS;                       // input-row ring slots
 
 struct GeoL {
     int NI, RT, CT;        // thread tiles: images x rows x columns (product 16)
@@ -51,154 +77,188 @@ __device__ __forceinline__ Unit decode_l(const GeoL &g, int u) {
     return r;
 }
 
-template <typename T, int TH, int TW, int MINB>
-__global__ void __launch_bounds__(kLThreads, MINB)
+// FWC: the filter width as a compile-time constant (0: read p.FW at run time).
+// FLIP: the filter is read rotated by 180 degrees (stride-1 input gradient).
+// MAXR: registers per thread, sized so the wanted number of 288-thread CTAs
+// fits an SM: each of the 4 sub-partitions holds 16K registers, and two
+// 9-warp CTAs put 5 warps on some sub-partition, so two CTAs need <= 102.
+template <typename T, int TH, int TW, int MAXR, int FWC, bool FLIP>
+__global__ void __maxnreg__(MAXR)
     tiled_large_kernel(const __grid_constant__ CUtensorMap row_map, const __grid_constant__ CUtensorMap filt_map,
                        TiledConv p, GeoL g, unsigned *err) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t bars[kNS + 1];  // ring slots, then the filter
+    // full[s]: a row has landed in slot s; empty[s]: all consumer warps are done
+    // with slot s; filt_full / filt_empty: the same for the filter slab.
+    __shared__ __align__(8) uint64_t full[kNS], empty[kNS], filt_full, filt_empty;
     using M = Mac<T>;
     using V = typename M::V;
+    constexpr int kConsumerWarps = kLThreads / 32;
+    const int FW = FWC ? FWC : p.FW;
 
     const int tid = threadIdx.x;
-    const int cp = tid % kPairs;
-    const int t = tid / kPairs;
-    const int ct = t % g.CT;
-    const int rt = (t / g.CT) % g.RT;
-    const int img_l = t / (g.CT * g.RT);
-
-    const T *filt = reinterpret_cast<const T *>(smem_raw);
-    unsigned char *ring = smem_raw + align128(g.filt_bytes);
     const unsigned slot_bytes = align128(g.row_bytes);
-    T *out = static_cast<T *>(p.out);
+    unsigned char *ring = smem_raw + align128(g.filt_bytes);
     const int tile_rows = g.RT * TH, tile_cols = g.CT * TW;
 
     // Contiguous unit range of this CTA.
     const int u_begin = (int)((long long)g.units * blockIdx.x / gridDim.x);
     const int u_end = (int)((long long)g.units * (blockIdx.x + 1) / gridDim.x);
-    const int steps = (u_end - u_begin) * g.R;
 
     if (tid == 0) {
-        for (int i = 0; i <= kNS; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        mbar_init(&filt_full, 1);
+        mbar_init(&filt_empty, kConsumerWarps);
         mbar_fence_init();
     }
     __syncthreads();
 
-    auto issue_row = [&](int q) {
-        const Unit un = decode_l(g, u_begin + q / g.R);
-        const int r = q % g.R;
-        const int s = q % kNS;
-        mbar_arrive_expect_tx(&bars[s], g.row_bytes);
-        tma_load_4d(ring + s * slot_bytes, &row_map, un.ctile * 32, un.twi * tile_cols - p.pad_w,
-                    un.band * tile_rows - p.pad_h + r, un.group * g.NI, &bars[s]);
-    };
-
-    if (tid == 0)
-        for (int q = 0; q < kNS - 1 && q < steps; ++q) issue_row(q);
-
-    int loaded_ctile = -1, filt_loads = 0;
-    float2 acc[TH][TW];
-    float2 bias2 = make_float2(0.f, 0.f);
-    Unit cur{};
-    int c = 0;
-
-    for (int q = 0; q < steps; ++q) {
-        const int r = q % g.R;
-        if (r == 0) {  // a new unit: filter (if the channel tile changed), bias, accumulators
-            cur = decode_l(g, u_begin + q / g.R);
-            c = cur.ctile * 32 + 2 * cp;
-            if (cur.ctile != loaded_ctile) {
-                // Every thread is past its last read of the old filter (the
-                // barrier at the end of the previous step).
-                if (tid == 0) {
-                    mbar_arrive_expect_tx(&bars[kNS], g.filt_bytes);
-                    tma_load_4d(smem_raw, &filt_map, cur.ctile * 32, 0, 0, 0, &bars[kNS]);
-                }
-                if (!mbar_wait(&bars[kNS], filt_loads & 1)) {
+    if (tid >= kLThreads) {  // ---------------- producer warp: one lane issues all copies
+        if (tid != kLThreads) return;
+        int q = 0, loaded = -1, reloads = 0;
+        for (int u = u_begin; u < u_end; ++u) {
+            const Unit un = decode_l(g, u);
+            if (un.ctile != loaded) {
+                if (reloads > 0 && !mbar_wait(&filt_empty, (reloads - 1) & 1)) {
                     report_timeout(err);
                     return;
                 }
-                ++filt_loads;
-                loaded_ctile = cur.ctile;
+                mbar_arrive_expect_tx(&filt_full, g.filt_bytes);
+                tma_load_4d(smem_raw, &filt_map, un.ctile * 32, 0, 0, 0, &filt_full);
+                loaded = un.ctile;
+                ++reloads;
             }
-            bias2 = (p.bias && c < p.C) ? make_float2(p.bias[c], p.bias[c + 1]) : make_float2(0.f, 0.f);
-#pragma unroll
-            for (int th = 0; th < TH; ++th)
-#pragma unroll
-                for (int tw = 0; tw < TW; ++tw) acc[th][tw] = bias2;
-        }
-        if (tid == 0 && q + kNS - 1 < steps) issue_row(q + kNS - 1);
-        if (!mbar_wait(&bars[q % kNS], (q / kNS) & 1)) {
-            // Give up: record it, let the copies this thread issued land, leave.
-            report_timeout(err);
-            if (tid == 0)
-                for (int o = q + 1; o < q + kNS && o < steps; ++o) mbar_wait(&bars[o % kNS], (o / kNS) & 1);
-            return;
-        }
-
-        // Filter rows this thread's output rows need from input row r.
-        const int fh0 = r - rt * TH;  // filter row of output row th = 0
-        bool any = false;
-#pragma unroll
-        for (int th = 0; th < TH; ++th) any |= (fh0 - th >= 0 && fh0 - th < p.FH);
-        if (any) {
-            const T *xrow = reinterpret_cast<const T *>(ring + (q % kNS) * slot_bytes) +
-                            (img_l * g.HW + ct * TW) * 32 + 2 * cp;
-            const T *wrow[TH];
-            bool valid[TH];
-#pragma unroll
-            for (int th = 0; th < TH; ++th) {
-                const int fh = fh0 - th;
-                valid[th] = fh >= 0 && fh < p.FH;
-                const int sfh = p.flip ? p.FH - 1 - fh : fh;
-                wrow[th] = filt + ((valid[th] ? sfh : 0) * p.FW) * 32 + 2 * cp;
-            }
-            V xw[TW];
-#pragma unroll
-            for (int k = 0; k < TW; ++k) xw[k] = M::load(xrow + k * 32);
-            // Filter columns in blocks of TW so the window slot of each input
-            // value is a compile-time index.
-            for (int fb = 0; fb < p.FW; fb += TW) {
-#pragma unroll
-                for (int k = 0; k < TW; ++k) {
-                    const int fw = fb + k;
-                    if (fw < p.FW) {
-                        const int sfw = p.flip ? p.FW - 1 - fw : fw;
-                        V wv[TH];
-#pragma unroll
-                        for (int th = 0; th < TH; ++th)
-                            wv[th] = valid[th] ? M::load(wrow[th] + sfw * 32) : M::zero();
-#pragma unroll
-                        for (int th = 0; th < TH; ++th)
-#pragma unroll
-                            for (int tw = 0; tw < TW; ++tw) M::fma(acc[th][tw], wv[th], xw[(tw + k) % TW]);
-                        // x[fw] is no longer needed; its slot takes x[fw + TW].
-                        if (fw + TW < TW + p.FW - 1) xw[k] = M::load(xrow + (fw + TW) * 32);
-                    }
+            for (int r = 0; r < g.R; ++r, ++q) {
+                const int s = q % kNS, k = q / kNS;
+                if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1)) {
+                    report_timeout(err);
+                    return;
                 }
+                mbar_arrive_expect_tx(&full[s], g.row_bytes);
+                tma_load_4d(ring + s * slot_bytes, &row_map, un.ctile * 32, un.twi * tile_cols - p.pad_w,
+                            un.band * tile_rows - p.pad_h + r, un.group * g.NI, &full[s]);
             }
         }
+        return;
+    }
 
-        if (r == g.R - 1) {  // unit done: store
-            const int n = cur.group * g.NI + img_l;
-            if (c < p.C && n < p.N) {
-                const int i0 = cur.band * tile_rows + rt * TH;
-                const int j0 = cur.twi * tile_cols + ct * TW;
-                T *img = out + (long long)n * p.OHf * p.OWf * p.C + c;
+    // ---------------------------------------- consumer warps
+    const int lane = tid % 32;
+    const int cp = tid % kPairs;
+    const int t = tid / kPairs;
+    const int ct = t % g.CT;
+    const int rt = (t / g.CT) % g.RT;
+    const int img_l = t / (g.CT * g.RT);
+    const T *filt = reinterpret_cast<const T *>(smem_raw);
+    T *out = static_cast<T *>(p.out);
+
+    int q = 0, loaded = -1, filt_seen = 0;
+    for (int u = u_begin; u < u_end; ++u) {
+        const Unit cur = decode_l(g, u);
+        if (cur.ctile != loaded) {
+            if (!mbar_wait(&filt_full, filt_seen & 1)) {
+                report_timeout(err);
+                return;
+            }
+            ++filt_seen;
+            loaded = cur.ctile;
+        }
+        const int c = cur.ctile * 32 + 2 * cp;
+        const float2 bias2 =
+            (p.bias && c < p.C) ? make_float2(p.bias[c], p.bias[c + 1]) : make_float2(0.f, 0.f);
+        float2 acc[TH][TW];
+#pragma unroll
+        for (int th = 0; th < TH; ++th)
+#pragma unroll
+            for (int tw = 0; tw < TW; ++tw) acc[th][tw] = bias2;
+
+        for (int r = 0; r < g.R; ++r, ++q) {
+            const int s = q % kNS;
+            // Filter rows this thread's output rows need from input row r; rows
+            // outside the input are all padding and contribute nothing.
+            const int fh0 = r - rt * TH;  // filter row of output row th = 0
+            bool any = false;
+#pragma unroll
+            for (int th = 0; th < TH; ++th) any |= (fh0 - th >= 0 && fh0 - th < p.FH);
+#if DWCONV_L_SKIP_PAD_ROWS
+            const int in_row = cur.band * tile_rows - p.pad_h + r;
+            any = any && in_row >= 0 && in_row < p.Hs;
+#endif
+            if (any) {
+                if (!mbar_wait(&full[s], (q / kNS) & 1)) {
+                    report_timeout(err);
+                    return;
+                }
+                const T *xrow = reinterpret_cast<const T *>(ring + s * slot_bytes) +
+                                (img_l * g.HW + ct * TW) * 32 + 2 * cp;
+                const T *wrow[TH];
+                bool valid[TH];
 #pragma unroll
                 for (int th = 0; th < TH; ++th) {
-                    const int i = i0 + th;
-                    if (i >= p.OHs) break;
+                    const int fh = fh0 - th;
+                    valid[th] = fh >= 0 && fh < p.FH;
+                    const int sfh = FLIP ? p.FH - 1 - fh : fh;
+                    // Row start; with FLIP the row is walked backwards from its end.
+                    wrow[th] = filt + ((valid[th] ? sfh : 0) * FW + (FLIP ? FW - 1 : 0)) * 32 + 2 * cp;
+                }
+                V xw[TW];
 #pragma unroll
-                    for (int tw = 0; tw < TW; ++tw) {
-                        const int j = j0 + tw;
-                        if (j >= p.OWs) break;
-                        Pair<T>::store(img + ((long long)i * p.OWf + j) * p.C, acc[th][tw]);
+                for (int k = 0; k < TW; ++k) xw[k] = M::load(xrow + k * 32);
+                // Filter columns in blocks of TW so the window slot of each input
+                // value is a compile-time index.
+#pragma unroll(FWC ? 1 : 0)
+                for (int fb = 0; fb < FW; fb += TW) {
+#pragma unroll
+                    for (int k = 0; k < TW; ++k) {
+                        const int fw = fb + k;
+                        if (fw < FW) {
+                            const int off = (FLIP ? -fw : fw) * 32;
+                            V wv[TH];
+#pragma unroll
+                            for (int th = 0; th < TH; ++th) wv[th] = valid[th] ? M::load(wrow[th] + off) : M::zero();
+#pragma unroll
+                            for (int th = 0; th < TH; ++th)
+#pragma unroll
+                                for (int tw = 0; tw < TW; ++tw) M::fma(acc[th][tw], wv[th], xw[(tw + k) % TW]);
+                            // x[fw] is no longer needed; its slot takes x[fw + TW].
+                            if (fw + TW < TW + FW - 1) xw[k] = M::load(xrow + (fw + TW) * 32);
+                        }
                     }
+                }
+            } else if (!mbar_wait(&full[s], (q / kNS) & 1)) {
+                // Not needed by this warp, but wait for it so that no warp runs
+                // more than a ring ahead of the slowest one.
+                report_timeout(err);
+                return;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
+        // Unit done: store, and release the filter if the next unit needs another.
+        const int n = cur.group * g.NI + img_l;
+        if (c < p.C && n < p.N) {
+            const int i0 = cur.band * tile_rows + rt * TH;
+            const int j0 = cur.twi * tile_cols + ct * TW;
+            T *img = out + (long long)n * p.OHf * p.OWf * p.C + c;
+#pragma unroll
+            for (int th = 0; th < TH; ++th) {
+                const int i = i0 + th;
+                if (i >= p.OHs) break;
+#pragma unroll
+                for (int tw = 0; tw < TW; ++tw) {
+                    const int j = j0 + tw;
+                    if (j >= p.OWs) break;
+                    Pair<T>::store(img + ((long long)i * p.OWf + j) * p.C, acc[th][tw]);
                 }
             }
         }
-        __syncthreads();  // slot q % kNS is refilled at the next step; the filter may be too
+        if (u + 1 < u_end && decode_l(g, u + 1).ctile != cur.ctile) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&filt_empty);
+        }
     }
 }
 
@@ -228,7 +288,7 @@ bool plan(const TiledConv &p, GeoL &g, size_t &smem) {
     return smem <= 220 * 1024;
 }
 
-template <typename T, int TH, int TW, int MINB>
+template <typename T, int TH, int TW, int MAXR, int FWC, bool FLIP>
 cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     GeoL g;
     size_t smem;
@@ -249,28 +309,37 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     if (!encode_tmap_4d(&row_map, dt, base, dims, str, box) ||
         !encode_tmap_4d(&filt_map, dt, p.w, fdims, fstr, fbox))
         return cudaErrorNotSupported;
-    auto kern = tiled_large_kernel<T, TH, TW, MINB>;
+    auto kern = tiled_large_kernel<T, TH, TW, MAXR, FWC, FLIP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLThreads + 32, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
     const long long slots = (long long)sm_count() * per_sm;
     const int grid = (int)std::min<long long>(g.units, slots);
-    kern<<<grid, kLThreads, smem, st>>>(row_map, filt_map, p, g, device_error_word());
+    kern<<<grid, kLThreads + 32, smem, st>>>(row_map, filt_map, p, g, device_error_word());
     note_launches(1);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+template <typename T, int MAXR>
+cudaError_t by_width(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    constexpr int TH = DWCONV_L_TH, TW = DWCONV_L_TW;
+#if DWCONV_L_FW31
+    if (p.FW == 31) return p.flip ? run<T, TH, TW, MAXR, 31, true>(p, dt, st) : run<T, TH, TW, MAXR, 31, false>(p, dt, st);
+#endif
+    return p.flip ? run<T, TH, TW, MAXR, 0, true>(p, dt, st) : run<T, TH, TW, MAXR, 0, false>(p, dt, st);
+}
+
 cudaError_t launch_tiled_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     if (p.FW < 8 || p.zero_phases || p.out_step != 1) return cudaErrorNotSupported;
     switch (dt) {
-        case DWCONV_FP32: return run<float, 2, 14, 1>(p, dt, st);
-        case DWCONV_FP16: return run<__half, 2, 14, 2>(p, dt, st);
-        case DWCONV_BF16: return run<__nv_bfloat16, 2, 14, 2>(p, dt, st);
+        case DWCONV_FP32: return by_width<float, 224>(p, dt, st);
+        case DWCONV_FP16: return by_width<__half, DWCONV_L_MAXR16>(p, dt, st);
+        case DWCONV_BF16: return by_width<__nv_bfloat16, DWCONV_L_MAXR16>(p, dt, st);
         default: return cudaErrorNotSupported;
     }
 }
