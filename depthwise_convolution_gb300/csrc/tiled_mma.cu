@@ -1,0 +1,410 @@
+// Tensor-core forward pass and stride-1 input gradient for 16-bit data and
+// 3x3, 5x5 and 7x7 filters on maps at least 17 columns wide.
+//
+// The GEMV of one channel (Flash-DWC §2.1) is packed into dense MMAs as in
+// Flash-DWC §4.2: 8 consecutive outputs of one output row ("a group") read a
+// window of 16 consecutive inputs, and for one filter row fh
+//
+//   Y[group m][n] += sum_{k<16} A[m][k] * B[k][n],   A[m][k] = X[ih][8j_m + k],
+//                                                    B[k][n] = w[fh][k - n] (0 outside [0, FW)),
+//
+// a 16 x 8 Toeplitz band of the filter row.  One warp-level mma.sync
+// m16n8k16 (bf16/fp16 in, fp32 accumulate) takes 16 groups at once: G groups
+// of each of 16/G output rows (G = 8 on maps wider than 32 columns, else 4).
+// A channel's output block needs FH such MMAs (one per filter row); the
+// accumulator stays in registers across them, so every partial sum is kept in
+// fp32 and the bias is added once, at the start.
+//
+// Work unit: 32 channels x OTH = 4 * 16/G output rows x OTW = 8G columns of
+// one image; 256 threads, each warp 4 channels; contiguous unit ranges per CTA.
+//   1. one TMA copy stages the NHWC input halo in shared memory with the
+//      64-byte swizzle (zeros outside the input: padding is generated); two
+//      staging buffers keep the next two units' loads in flight;
+//   2. ldmatrix.trans + stmatrix transpose it into a channel-major buffer
+//      T[channel][row][column], in which the 8 windows of 8 rows of an MMA
+//      operand are 8 rows of 16 bytes (one ldmatrix matrix);
+//   3. the A operands of the 4 row sets x FH filter rows overlap: the 8x8
+//      matrix of "8/G input rows starting at r" is the same whichever
+//      (row set, filter row) pair uses it, so each is loaded once per channel
+//      and reused from registers (about FH/2 times fewer shared loads than
+//      loading every MMA's operand);
+//   4. B (the Toeplitz bands of the warp's 4 channels) stays in registers for
+//      all units of a channel tile;
+//   5. the results, rounded to 16 bits, go to a separate 64B-swizzled NHWC
+//      output tile and leave with one TMA tensor store (clipped at the
+//      tensor edges by the copy engine).
+// Two CTA barriers per unit: "T and the output tile are ready" and "the
+// output tile is complete (and every warp is done with T)".
+#include "tiled_common.cuh"
+
+namespace dwc {
+namespace {
+
+using namespace tiled;
+
+constexpr int kMThreads = 256;  // 8 warps, 4 channels each
+constexpr int kChPerWarp = 4;
+constexpr int kNB = 4;  // MMA row sets per work unit
+
+// Tile geometry, fixed by the filter height and G.
+template <int FH, int G>
+struct Cfg {
+    static constexpr int OTH = kNB * 16 / G, OTW = 8 * G;  // output tile rows, columns
+    static constexpr int HR = OTH + FH - 1, SW = OTW + 8;  // staged halo rows, columns
+    static constexpr int RS = SW;                          // T row stride (halves)
+    // T channel stride: = 8 mod 16 halves, so stmatrix rows of 8 channels
+    // land in distinct banks.
+    static constexpr int CS = (HR * RS) % 16 == 8 ? HR * RS : (HR * RS) + ((8 - (HR * RS) % 16 + 16) % 16);
+    static constexpr unsigned s_bytes = HR * SW * 64;
+    static constexpr unsigned s_stride = (s_bytes + 1023u) & ~1023u;
+    static constexpr unsigned t_off = 2 * s_stride;
+    static constexpr unsigned o_off = t_off + ((32u * CS * 2 + 1023u) & ~1023u);
+    static constexpr unsigned smem = o_off + OTH * OTW * 64;  // + 1 KB alignment slack at launch
+    static_assert(CS % 16 == 8, "channel stride");
+};
+
+struct GeoM {
+    int tiles_h, tiles_w, per_ctile, units;
+};
+
+__device__ __forceinline__ void ldsm_x4_trans(unsigned &r0, unsigned &r1, unsigned &r2, unsigned &r3,
+                                              unsigned addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4(unsigned &r0, unsigned &r1, unsigned &r2, unsigned &r3,
+                                        unsigned addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(unsigned &r0, unsigned &r1, unsigned addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];\n"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void stsm_x4(unsigned addr, unsigned r0, unsigned r1, unsigned r2, unsigned r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
+template <typename T> struct MmaOp;
+template <> struct MmaOp<__nv_bfloat16> {
+    static __device__ __forceinline__ void run(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                               unsigned b0, unsigned b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+    static __device__ __forceinline__ unsigned pack(float lo, float hi) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<unsigned *>(&v);
+    }
+    static __device__ __forceinline__ unsigned pack_raw(__nv_bfloat16 lo, __nv_bfloat16 hi) {
+        return (unsigned)__bfloat16_as_ushort(lo) | ((unsigned)__bfloat16_as_ushort(hi) << 16);
+    }
+};
+template <> struct MmaOp<__half> {
+    static __device__ __forceinline__ void run(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                               unsigned b0, unsigned b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+    static __device__ __forceinline__ unsigned pack(float lo, float hi) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<unsigned *>(&v);
+    }
+    static __device__ __forceinline__ unsigned pack_raw(__half lo, __half hi) {
+        return (unsigned)__half_as_ushort(lo) | ((unsigned)__half_as_ushort(hi) << 16);
+    }
+};
+
+__device__ __forceinline__ Unit decode_m(const GeoM &g, int u) {
+    Unit r;
+    r.ctile = u / g.per_ctile;
+    int v = u - r.ctile * g.per_ctile;
+    r.band = v % g.tiles_h;
+    v /= g.tiles_h;
+    r.twi = v % g.tiles_w;
+    r.group = v / g.tiles_w;
+    return r;
+}
+
+template <typename T, int FH, int FW, int G>
+__global__ void __launch_bounds__(kMThreads, 1)
+    tiled_mma_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap out_map,
+                     TiledConv p, GeoM g, unsigned *err) {
+    constexpr int RB = 8 / G;                     // input rows of one 8x8 A matrix
+    constexpr int Rm = 16 / G;                    // output rows of one MMA
+    constexpr int NP = (kNB - 1) * Rm + RB + FH;  // distinct A matrices (pairs lo/hi) per channel
+    constexpr int NS = (NP + 1) / 2;              // load stages of two
+    using C = Cfg<FH, G>;
+    extern __shared__ __align__(1024) unsigned char smem_dyn[];
+    __shared__ __align__(8) uint64_t bar[2];
+    using Op = MmaOp<T>;
+
+    // Swizzled buffers start on 1024-byte boundaries (the launch adds 1 KB of slack).
+    unsigned char *smem_raw = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int gq = lane / 4, t4 = lane % 4;  // mma fragment coordinates
+    unsigned char *S = smem_raw;             // 2 staging buffers [HR][SW][32], s_stride apart
+    const unsigned s_addr = smem_addr(S);
+    const unsigned t_addr = s_addr + C::t_off;  // T [32][CS] halves
+    const unsigned o_addr = s_addr + C::o_off;  // output tile [OTH][OTW][32], 64B-swizzled
+    const T *wg = static_cast<const T *>(p.w);
+
+    // Contiguous unit range of this CTA (channel tile slowest: few B reloads).
+    const int u_begin = (int)((long long)g.units * blockIdx.x / gridDim.x);
+    const int u_end = (int)((long long)g.units * (blockIdx.x + 1) / gridDim.x);
+
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int u, int b) {
+        const Unit un = decode_m(g, u);
+        mbar_arrive_expect_tx(&bar[b], C::s_bytes);
+        tma_load_4d(S + b * C::s_stride, &halo_map, un.ctile * 32, un.twi * C::OTW - p.pad_w,
+                    un.band * C::OTH - p.pad_h, un.group, &bar[b]);
+    };
+    if (tid == 0) {
+        if (u_begin < u_end) issue(u_begin, 0);
+        if (u_begin + 1 < u_end) issue(u_begin + 1, 1);
+    }
+
+    // ldmatrix.x4 of the pair (r, r+1): lanes 8j..8j+7 address the rows of
+    // matrix j = (fragment r + j/2, k half j%2); row i of a matrix is window
+    // i % G of input row r + j/2 + i / G.
+    const int mj = lane / 8, mi = lane % 8;
+    const int lane_off = ((mj >> 1) + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj & 1);
+    // Transposition: this lane's row of its 8x8 matrix (matrix = channel chunk).
+    const int tr = lane % 8, tj = lane / 8;
+    // Output: lane (gq, t4) writes position (row gq / G, column 8 (gq % G) +
+    // 2t4 + e) of each row set; bits 7-8 of the offset are t4 (OTW is a
+    // multiple of 8), so the swizzled 16-byte chunk is (warp / 2) ^ t4.
+    const unsigned o_lane = o_addr + ((gq / G) * C::OTW + 8 * (gq % G) + 2 * t4) * 64 +
+                            ((((unsigned)warp >> 1) ^ (unsigned)t4) & 3u) * 16 + (warp & 1) * 8;
+    const unsigned o_lane0 = o_lane + (gq & 1) * 64, o_lane1 = o_lane + (1 - (gq & 1)) * 64;
+
+    int loaded_ctile = -1;
+    float bias_r[kChPerWarp];
+    unsigned bfr[kChPerWarp][FH][2];  // Toeplitz bands, B fragments (k 0-7, k 8-15)
+    for (int u = u_begin, k = 0; u < u_end; ++u, ++k) {
+        const Unit cur = decode_m(g, u);
+        if (cur.ctile != loaded_ctile) {
+            // B[k][n] = w[fh][k - n]: lane (gq, t4) holds k = 2t4, 2t4+1 (+8), n = gq.
+            // For the input gradient the filter is rotated by 180 degrees.
+            loaded_ctile = cur.ctile;
+#pragma unroll
+            for (int ci = 0; ci < kChPerWarp; ++ci) {
+                const int cc = cur.ctile * 32 + warp * kChPerWarp + ci;
+                const bool live = cc < p.C;
+                bias_r[ci] = (p.bias && live) ? p.bias[cc] : 0.f;
+#pragma unroll
+                for (int fh = 0; fh < FH; ++fh) {
+                    const int sfh = p.flip ? FH - 1 - fh : fh;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        T v[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int fw = 2 * t4 + e + 8 * h - gq;
+                            v[e] = from_f32<T>(0.f);
+                            if (live && fw >= 0 && fw < FW)
+                                v[e] = wg[(sfh * FW + (p.flip ? FW - 1 - fw : fw)) * p.C + cc];
+                        }
+                        bfr[ci][fh][h] = Op::pack_raw(v[0], v[1]);
+                    }
+                }
+            }
+        }
+        if (!mbar_wait(&bar[k & 1], (k >> 1) & 1)) {
+            report_timeout(err);
+            return;
+        }
+
+        // Transpose S[row][col][ch] -> T[ch][row][col], 8 cols x 32 ch per step:
+        // ldmatrix.trans gives lane (gq, t4) cols 2t4, 2t4+1 of channel 8j + gq;
+        // stmatrix writes them as the 16-byte row (channel, 8 cols).  Every warp
+        // finished reading T (previous unit) before the last barrier.
+        const unsigned s_buf = s_addr + (k & 1) * C::s_stride;
+        for (int b = warp; b < C::HR * (C::SW / 8); b += kMThreads / 32) {
+            const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
+            unsigned src = s_buf + (row * C::SW + col0 + tr) * 64 + 16 * tj;
+            src ^= ((src >> 7) & 3u) << 4;  // 64-byte swizzle
+            unsigned v0, v1, v2, v3;
+            ldsm_x4_trans(v0, v1, v2, v3, src);
+            stsm_x4(t_addr + 2u * ((8 * tj + tr) * C::CS + row * C::RS + col0), v0, v1, v2, v3);
+        }
+        // The previous unit's TMA store must have read the output tile.
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+        __syncthreads();  // T ready, output tile free, this staging buffer free
+        if (tid == 0 && u + 2 < u_end) issue(u + 2, k & 1);
+
+        // MMAs.  Fragment r (lo, hi) = input rows r .. r+RB-1 of the channel;
+        // MMA (row set rs, filter row fh) takes fragments rs*Rm + fh (M rows
+        // 0-7) and rs*Rm + RB + fh (M rows 8-15).  Stage s loads fragments 2s,
+        // 2s+1 (issued one stage ahead, also across channels) and then runs
+        // every MMA whose later fragment is one of them, row sets interleaved.
+        float d[kChPerWarp][kNB][4];
+        unsigned P[NS * 2][2];
+        auto load_stage = [&](int ci, int s) {
+            const unsigned a = t_addr + 2u * ((warp * kChPerWarp + ci) * C::CS + 2 * s * C::RS + lane_off);
+            if (2 * s + 1 < NP)
+                ldsm_x4(P[2 * s][0], P[2 * s][1], P[2 * s + 1][0], P[2 * s + 1][1], a);
+            else
+                ldsm_x2(P[2 * s][0], P[2 * s][1], a);
+        };
+        load_stage(0, 0);
+#pragma unroll
+        for (int ci = 0; ci < kChPerWarp; ++ci) {
+#pragma unroll
+            for (int rs = 0; rs < kNB; ++rs)
+                d[ci][rs][0] = d[ci][rs][1] = d[ci][rs][2] = d[ci][rs][3] = bias_r[ci];
+#pragma unroll
+            for (int s = 0; s < NS; ++s) {
+                if (s + 1 < NS)
+                    load_stage(ci, s + 1);
+                else if (ci + 1 < kChPerWarp)
+                    load_stage(ci + 1, 0);
+#pragma unroll
+                for (int r = 2 * s; r < 2 * s + 2; ++r)
+#pragma unroll
+                    for (int rs = 0; rs < kNB; ++rs) {
+                        const int fh = r - rs * Rm - RB;
+                        if (fh >= 0 && fh < FH) {
+                            const int r0 = rs * Rm + fh;
+                            Op::run(d[ci][rs], P[r0][0], P[r][0], P[r0][1], P[r][1], bfr[ci][fh][0],
+                                    bfr[ci][fh][1]);
+                        }
+                    }
+            }
+        }
+
+        // Output tile [OTH][OTW][32 ch], 64B-swizzled for the TMA store: this
+        // lane writes 8 bytes (its warp's 4 channels) per output position.  The
+        // two columns 2t4, 2t4+1 go out in the order set by gq's parity, so one
+        // store covers both 64-byte halves of a 128-byte line (4-way instead of
+        // 8-way bank conflicts).
+#pragma unroll
+        for (int rs = 0; rs < kNB; ++rs)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                for (int step = 0; step < 2; ++step) {
+                    const int e = step ^ (gq & 1);
+                    const float v0 = e ? d[0][rs][2 * half + 1] : d[0][rs][2 * half];
+                    const float v1 = e ? d[1][rs][2 * half + 1] : d[1][rs][2 * half];
+                    const float v2 = e ? d[2][rs][2 * half + 1] : d[2][rs][2 * half];
+                    const float v3 = e ? d[3][rs][2 * half + 1] : d[3][rs][2 * half];
+                    const unsigned a = (step ? o_lane1 : o_lane0) + (rs * Rm + half * RB) * C::OTW * 64;
+                    asm volatile("st.shared.v2.b32 [%0], {%1, %2};\n" ::"r"(a), "r"(Op::pack(v0, v1)),
+                                 "r"(Op::pack(v2, v3))
+                                 : "memory");
+                }
+            }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // visible to the TMA store
+        __syncthreads();  // output tile complete; every warp is done with T
+        if (tid == 0) {
+            asm volatile(
+                "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];\n" ::"l"(
+                    reinterpret_cast<uint64_t>(&out_map)),
+                "r"(cur.ctile * 32), "r"(cur.twi * C::OTW), "r"(cur.band * C::OTH), "r"(cur.group), "r"(o_addr)
+                : "memory");
+            asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+        }
+    }
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
+
+template <int FH, int G>
+bool plan(const TiledConv &p, GeoM &g) {
+    using C = Cfg<FH, G>;
+    g = GeoM{};
+    g.tiles_h = (p.OHs + C::OTH - 1) / C::OTH;
+    g.tiles_w = (p.OWs + C::OTW - 1) / C::OTW;
+    const long long per = (long long)p.N * g.tiles_w * g.tiles_h;
+    const long long units = per * ((p.C + 31) / 32);
+    if (units >= (1LL << 30)) return false;
+    g.per_ctile = (int)per;
+    g.units = (int)units;
+    return C::smem + 1024 <= 227 * 1024;
+}
+
+template <typename T, int FH, int FW, int G>
+cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    using C = Cfg<FH, G>;
+    GeoM g;
+    if (!plan<FH, G>(p, g)) return cudaErrorNotSupported;
+    // Halo map as for the CUDA-core kernels, one image per box, 64-byte swizzle
+    // (the inner box row is exactly one 32-channel pixel).  The output map
+    // covers y (or dx) directly; the TMA store clips the tile at the edges.
+    const size_t es = sizeof(T);
+    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off * p.Wf + p.in_off) * p.C * es;
+    const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
+    const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
+                             (uint64_t)p.Hf * p.Wf * p.C * es};
+    const uint32_t box[4] = {32, (uint32_t)C::SW, (uint32_t)C::HR, 1};
+    const uint64_t odims[4] = {(uint64_t)p.C, (uint64_t)p.OWf, (uint64_t)p.OHf, (uint64_t)p.N};
+    const uint64_t ostr[3] = {(uint64_t)p.C * es, (uint64_t)p.OWf * p.C * es, (uint64_t)p.OHf * p.OWf * p.C * es};
+    const uint32_t obox[4] = {32, (uint32_t)C::OTW, (uint32_t)C::OTH, 1};
+    CUtensorMap map, omap;
+    if (!encode_tmap_4d(&map, dt, base, dims, str, box, true) ||
+        !encode_tmap_4d(&omap, dt, p.out, odims, ostr, obox, true))
+        return cudaErrorNotSupported;
+    auto kern = tiled_mma_kernel<T, FH, FW, G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem + 1024);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMThreads, C::smem + 1024);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    const long long slots = (long long)sm_count() * per_sm;
+    const int grid = (int)std::min<long long>(g.units, slots);
+    kern<<<grid, kMThreads, C::smem + 1024, st>>>(map, omap, p, g, device_error_word());
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename T, int FH, int FW>
+cudaError_t by_width(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    if (p.OWs > 32) return run<T, FH, FW, 8>(p, dt, st);
+    if (p.OWs > 16) return run<T, FH, FW, 4>(p, dt, st);
+    return cudaErrorNotSupported;  // narrow maps stay on the CUDA-core kernel
+}
+
+template <typename T>
+cudaError_t by_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    if (p.FH == 7 && p.FW == 7) return by_width<T, 7, 7>(p, dt, st);
+    if (p.FH == 5 && p.FW == 5) return by_width<T, 5, 5>(p, dt, st);
+    if (p.FH == 3 && p.FW == 3) return by_width<T, 3, 3>(p, dt, st);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+#ifndef DWCONV_MMA
+#define DWCONV_MMA 1  // 0: leave every shape to the CUDA-core kernels
+#endif
+
+cudaError_t launch_tiled_mma(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    if (!DWCONV_MMA || p.zero_phases || p.out_step != 1) return cudaErrorNotSupported;
+    switch (dt) {
+        case DWCONV_FP16: return by_filter<__half>(p, dt, st);
+        case DWCONV_BF16: return by_filter<__nv_bfloat16>(p, dt, st);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace dwc

@@ -24,9 +24,11 @@ unsigned *device_error_word();
 cudaError_t take_device_error(cudaStream_t st, unsigned *value);
 
 // 4-D tiled tensor map, dims innermost first (C, W, H, N), strides in bytes
-// for dims 1..3, box in elements.  Returns false if the driver rejects it.
+// for dims 1..3, box in elements; swizzle64: 64-byte shared-memory swizzle
+// (the inner box row must then be 64 bytes).  Returns false if the driver
+// rejects it.
 bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const uint64_t dims[4],
-                    const uint64_t strides[3], const uint32_t box[4]);
+                    const uint64_t strides[3], const uint32_t box[4], bool swizzle64 = false);
 
 __device__ __forceinline__ unsigned smem_addr(const void *p) {
     return (unsigned)__cvta_generic_to_shared(p);
