@@ -141,10 +141,9 @@ template <typename T, int FH, int FW, int G>
 __global__ void __launch_bounds__(kMThreads, 1)
     tiled_mma_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap out_map,
                      TiledConv p, GeoM g, unsigned *err) {
-    constexpr int RB = 8 / G;                     // input rows of one 8x8 A matrix
-    constexpr int Rm = 16 / G;                    // output rows of one MMA
-    constexpr int NP = (kNB - 1) * Rm + RB + FH;  // distinct A matrices (pairs lo/hi) per channel
-    constexpr int NS = (NP + 1) / 2;              // load stages of two
+    constexpr int RB = 8 / G;                // output rows of one 8x8 block of M rows
+    constexpr int DH = kNB * RB;             // row offset of M rows 8-15 (half the tile)
+    constexpr int NQ = (kNB - 1) * RB + FH;  // distinct A operands per channel
     using C = Cfg<FH, G>;
     extern __shared__ __align__(1024) unsigned char smem_dyn[];
     __shared__ __align__(8) uint64_t bar[2];
@@ -172,26 +171,41 @@ __global__ void __launch_bounds__(kMThreads, 1)
     }
     __syncthreads();
 
-    auto issue = [&](int u, int b) {
-        const Unit un = decode_m(g, u);
+    // Unit cursors (row band fastest) for the loads (thread 0) and the compute.
+    Unit ld = decode_m(g, u_begin), cur = ld;
+    auto advance = [&](Unit &c) {
+        if (++c.band == g.tiles_h) {
+            c.band = 0;
+            if (++c.twi == g.tiles_w) {
+                c.twi = 0;
+                if (++c.group == p.N) {
+                    c.group = 0;
+                    ++c.ctile;
+                }
+            }
+        }
+    };
+    auto issue = [&](int b) {
+        const Unit un = ld;
+        advance(ld);
         mbar_arrive_expect_tx(&bar[b], C::s_bytes);
         tma_load_4d(S + b * C::s_stride, &halo_map, un.ctile * 32, un.twi * C::OTW - p.pad_w,
                     un.band * C::OTH - p.pad_h, un.group, &bar[b]);
     };
     if (tid == 0) {
-        if (u_begin < u_end) issue(u_begin, 0);
-        if (u_begin + 1 < u_end) issue(u_begin + 1, 1);
+        if (u_begin < u_end) issue(0);
+        if (u_begin + 1 < u_end) issue(1);
     }
 
-    // ldmatrix.x4 of the pair (r, r+1): lanes 8j..8j+7 address the rows of
-    // matrix j = (fragment r + j/2, k half j%2); row i of a matrix is window
-    // i % G of input row r + j/2 + i / G.
+    // A operand x of a channel = one ldmatrix.x4: matrix j (lanes 8j..8j+7
+    // give its row addresses) holds M rows 8(j%2)..+7 and k 8(j/2)..+7; M row
+    // i of block j%2 is window i % G of input row x + i / G + DH (j%2).
     const int mj = lane / 8, mi = lane % 8;
-    const int lane_off = ((mj >> 1) + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj & 1);
+    const int lane_off = ((mj & 1) * DH + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj >> 1);
     // Transposition: this lane's row of its 8x8 matrix (matrix = channel chunk).
     const int tr = lane % 8, tj = lane / 8;
-    // Output: lane (gq, t4) writes position (row gq / G, column 8 (gq % G) +
-    // 2t4 + e) of each row set; bits 7-8 of the offset are t4 (OTW is a
+    // Output: lane (gq, t4) writes position (row gq / G (+ DH for M rows
+    // 8-15), column 8 (gq % G) + 2t4 + e) of each row set; bits 7-8 of the offset are t4 (OTW is a
     // multiple of 8), so the swizzled 16-byte chunk is (warp / 2) ^ t4.
     const unsigned o_lane = o_addr + ((gq / G) * C::OTW + 8 * (gq % G) + 2 * t4) * 64 +
                             ((((unsigned)warp >> 1) ^ (unsigned)t4) & 3u) * 16 + (warp & 1) * 8;
@@ -200,8 +214,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
     int loaded_ctile = -1;
     float bias_r[kChPerWarp];
     unsigned bfr[kChPerWarp][FH][2];  // Toeplitz bands, B fragments (k 0-7, k 8-15)
-    for (int u = u_begin, k = 0; u < u_end; ++u, ++k) {
-        const Unit cur = decode_m(g, u);
+    for (int u = u_begin, k = 0; u < u_end; ++u, ++k, advance(cur)) {
         if (cur.ctile != loaded_ctile) {
             // B[k][n] = w[fh][k - n]: lane (gq, t4) holds k = 2t4, 2t4+1 (+8), n = gq.
             // For the input gradient the filter is rotated by 180 degrees.
@@ -250,45 +263,39 @@ __global__ void __launch_bounds__(kMThreads, 1)
         // The previous unit's TMA store must have read the output tile.
         if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
         __syncthreads();  // T ready, output tile free, this staging buffer free
-        if (tid == 0 && u + 2 < u_end) issue(u + 2, k & 1);
+        if (tid == 0 && u + 2 < u_end) issue(k & 1);
 
-        // MMAs.  Fragment r (lo, hi) = input rows r .. r+RB-1 of the channel;
-        // MMA (row set rs, filter row fh) takes fragments rs*Rm + fh (M rows
-        // 0-7) and rs*Rm + RB + fh (M rows 8-15).  Stage s loads fragments 2s,
-        // 2s+1 (issued one stage ahead, also across channels) and then runs
-        // every MMA whose later fragment is one of them, row sets interleaved.
+        // MMAs.  Row set j (j < kNB) covers output rows j*RB .. +RB-1 (M rows
+        // 0-7) and the same rows + DH (M rows 8-15); MMA (j, fh) reads input
+        // rows from x = j*RB + fh on, i.e. A operand x, which every (j, fh)
+        // with the same x shares.  Stage x loads operand x + 1 (one ahead,
+        // also across channels) and runs the MMAs of operand x, row sets
+        // interleaved (independent accumulators).
         float d[kChPerWarp][kNB][4];
-        unsigned P[NS * 2][2];
-        auto load_stage = [&](int ci, int s) {
-            const unsigned a = t_addr + 2u * ((warp * kChPerWarp + ci) * C::CS + 2 * s * C::RS + lane_off);
-            if (2 * s + 1 < NP)
-                ldsm_x4(P[2 * s][0], P[2 * s][1], P[2 * s + 1][0], P[2 * s + 1][1], a);
-            else
-                ldsm_x2(P[2 * s][0], P[2 * s][1], a);
+        unsigned A[2][4];  // slot = stage number (over all channels) mod 2
+        auto load_a = [&](int ci, int x) {
+            const int sl = (ci * NQ + x) & 1;
+            ldsm_x4(A[sl][0], A[sl][1], A[sl][2], A[sl][3],
+                    t_addr + 2u * ((warp * kChPerWarp + ci) * C::CS + x * C::RS + lane_off));
         };
-        load_stage(0, 0);
+        load_a(0, 0);
 #pragma unroll
         for (int ci = 0; ci < kChPerWarp; ++ci) {
 #pragma unroll
-            for (int rs = 0; rs < kNB; ++rs)
-                d[ci][rs][0] = d[ci][rs][1] = d[ci][rs][2] = d[ci][rs][3] = bias_r[ci];
+            for (int j = 0; j < kNB; ++j) d[ci][j][0] = d[ci][j][1] = d[ci][j][2] = d[ci][j][3] = bias_r[ci];
 #pragma unroll
-            for (int s = 0; s < NS; ++s) {
-                if (s + 1 < NS)
-                    load_stage(ci, s + 1);
+            for (int x = 0; x < NQ; ++x) {
+                if (x + 1 < NQ)
+                    load_a(ci, x + 1);
                 else if (ci + 1 < kChPerWarp)
-                    load_stage(ci + 1, 0);
+                    load_a(ci + 1, 0);
+                const int sl = (ci * NQ + x) & 1;
 #pragma unroll
-                for (int r = 2 * s; r < 2 * s + 2; ++r)
-#pragma unroll
-                    for (int rs = 0; rs < kNB; ++rs) {
-                        const int fh = r - rs * Rm - RB;
-                        if (fh >= 0 && fh < FH) {
-                            const int r0 = rs * Rm + fh;
-                            Op::run(d[ci][rs], P[r0][0], P[r][0], P[r0][1], P[r][1], bfr[ci][fh][0],
-                                    bfr[ci][fh][1]);
-                        }
-                    }
+                for (int j = 0; j < kNB; ++j) {
+                    const int fh = x - j * RB;
+                    if (fh >= 0 && fh < FH)
+                        Op::run(d[ci][j], A[sl][0], A[sl][1], A[sl][2], A[sl][3], bfr[ci][fh][0], bfr[ci][fh][1]);
+                }
             }
         }
 
@@ -298,21 +305,23 @@ __global__ void __launch_bounds__(kMThreads, 1)
         // store covers both 64-byte halves of a 128-byte line (4-way instead of
         // 8-way bank conflicts).
 #pragma unroll
-        for (int rs = 0; rs < kNB; ++rs)
+        for (int j = 0; j < kNB; ++j)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
+                unsigned lo[2], hi[2];  // column 2t4 + e: channels (0, 1), (2, 3)
 #pragma unroll
-                for (int step = 0; step < 2; ++step) {
-                    const int e = step ^ (gq & 1);
-                    const float v0 = e ? d[0][rs][2 * half + 1] : d[0][rs][2 * half];
-                    const float v1 = e ? d[1][rs][2 * half + 1] : d[1][rs][2 * half];
-                    const float v2 = e ? d[2][rs][2 * half + 1] : d[2][rs][2 * half];
-                    const float v3 = e ? d[3][rs][2 * half + 1] : d[3][rs][2 * half];
-                    const unsigned a = (step ? o_lane1 : o_lane0) + (rs * Rm + half * RB) * C::OTW * 64;
-                    asm volatile("st.shared.v2.b32 [%0], {%1, %2};\n" ::"r"(a), "r"(Op::pack(v0, v1)),
-                                 "r"(Op::pack(v2, v3))
-                                 : "memory");
+                for (int e = 0; e < 2; ++e) {
+                    lo[e] = Op::pack(d[0][j][2 * half + e], d[1][j][2 * half + e]);
+                    hi[e] = Op::pack(d[2][j][2 * half + e], d[3][j][2 * half + e]);
                 }
+                const bool odd = gq & 1;
+                const unsigned row = (j * RB + half * DH) * C::OTW * 64;
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};\n" ::"r"(o_lane0 + row), "r"(odd ? lo[1] : lo[0]),
+                             "r"(odd ? hi[1] : hi[0])
+                             : "memory");
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};\n" ::"r"(o_lane1 + row), "r"(odd ? lo[0] : lo[1]),
+                             "r"(odd ? hi[0] : hi[1])
+                             : "memory");
             }
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // visible to the TMA store
         __syncthreads();  // output tile complete; every warp is done with T

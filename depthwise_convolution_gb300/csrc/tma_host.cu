@@ -56,7 +56,7 @@ cudaError_t take_device_error(cudaStream_t st, unsigned *value) {
 }
 
 bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const uint64_t dims[4],
-                    const uint64_t strides[3], const uint32_t box[4], bool swizzle64) {
+                    const uint64_t strides[3], const uint32_t box[4], bool swizzle64, int l2_promotion) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     CUtensorMapDataType t;
@@ -75,9 +75,17 @@ bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const u
     const cuuint32_t bd[4] = {box[0], box[1], box[2], box[3]};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     if (swizzle64 && box[0] * (dt == DWCONV_FP32 ? 4u : 2u) != 64u) return false;
+    CUtensorMapL2promotion promo;
+    switch (l2_promotion) {
+        case 0: promo = CU_TENSOR_MAP_L2_PROMOTION_NONE; break;
+        case 64: promo = CU_TENSOR_MAP_L2_PROMOTION_L2_64B; break;
+        case 128: promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B; break;
+        case 256: promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B; break;
+        default: return false;
+    }
     CUresult r = fn(map, t, 4, const_cast<void *>(base), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
