@@ -42,9 +42,27 @@ namespace {
 
 using namespace tiled;
 
-constexpr int kMThreads = 256;  // 8 warps, 4 channels each
-constexpr int kChPerWarp = 4;
-constexpr int kNB = 4;  // MMA row sets per work unit
+#ifndef DWCONV_MMA_CH
+#define DWCONV_MMA_CH 32  // channels per work unit (16 or 32)
+#endif
+#ifndef DWCONV_MMA_NS
+#define DWCONV_MMA_NS 2  // halo staging buffers (1 or 2)
+#endif
+
+constexpr int kCh = DWCONV_MMA_CH;             // channels per work unit
+constexpr int kChPerWarp = 4;                  // channels per warp
+constexpr int kMThreads = kCh / kChPerWarp * 32;
+constexpr int kMinCtas = kCh == 16 ? 2 : 1;    // CTAs per SM the registers are capped for
+constexpr int kNS = DWCONV_MMA_NS;             // staging buffers
+constexpr int kPB = 2 * kCh;                   // bytes of one staged pixel (= swizzle span)
+constexpr unsigned kSwzMask = kPB / 16 - 1;    // 16-byte chunk bits the swizzle flips
+constexpr int kNB = 4;                         // MMA row sets per work unit
+static_assert(kCh == 16 || kCh == 32, "channels per unit");
+static_assert(kNS == 1 || kNS == 2, "staging buffers");
+
+// Shared-memory address of a byte offset inside a swizzled buffer (the TMA's
+// 32- or 64-byte swizzle: 16-byte chunk bits XOR address bits 7 and up).
+__device__ __forceinline__ unsigned swz(unsigned a) { return a ^ (((a >> 7) & kSwzMask) << 4); }
 
 // Tile geometry, fixed by the filter height and G.
 template <int FH, int G>
@@ -55,12 +73,13 @@ struct Cfg {
     // T channel stride: = 8 mod 16 halves, so stmatrix rows of 8 channels
     // land in distinct banks.
     static constexpr int CS = (HR * RS) % 16 == 8 ? HR * RS : (HR * RS) + ((8 - (HR * RS) % 16 + 16) % 16);
-    static constexpr unsigned s_bytes = HR * SW * 64;
+    static constexpr unsigned s_bytes = HR * SW * kPB;
     static constexpr unsigned s_stride = (s_bytes + 1023u) & ~1023u;
-    static constexpr unsigned t_off = 2 * s_stride;
-    static constexpr unsigned o_off = t_off + ((32u * CS * 2 + 1023u) & ~1023u);
-    static constexpr unsigned smem = o_off + OTH * OTW * 64;  // + 1 KB alignment slack at launch
+    static constexpr unsigned t_off = kNS * s_stride;
+    static constexpr unsigned o_off = t_off + ((unsigned)(kCh * CS * 2) + 1023u & ~1023u);
+    static constexpr unsigned smem = o_off + OTH * OTW * kPB;  // + 1 KB alignment slack at launch
     static_assert(CS % 16 == 8, "channel stride");
+    static_assert(HR % (4 / (kCh / 8)) == 0, "transposition steps cover whole row groups");
 };
 
 struct GeoM {
@@ -138,7 +157,7 @@ __device__ __forceinline__ Unit decode_m(const GeoM &g, int u) {
 }
 
 template <typename T, int FH, int FW, int G>
-__global__ void __launch_bounds__(kMThreads, 1)
+__global__ void __launch_bounds__(kMThreads, kMinCtas)
     tiled_mma_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap out_map,
                      TiledConv p, GeoM g, unsigned *err) {
     constexpr int RB = 8 / G;                // output rows of one 8x8 block of M rows
@@ -146,7 +165,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
     constexpr int NQ = (kNB - 1) * RB + FH;  // distinct A operands per channel
     using C = Cfg<FH, G>;
     extern __shared__ __align__(1024) unsigned char smem_dyn[];
-    __shared__ __align__(8) uint64_t bar[2];
+    __shared__ __align__(8) uint64_t bar[kNS];
     using Op = MmaOp<T>;
 
     // Swizzled buffers start on 1024-byte boundaries (the launch adds 1 KB of slack).
@@ -154,10 +173,10 @@ __global__ void __launch_bounds__(kMThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int gq = lane / 4, t4 = lane % 4;  // mma fragment coordinates
-    unsigned char *S = smem_raw;             // 2 staging buffers [HR][SW][32], s_stride apart
+    unsigned char *S = smem_raw;             // kNS staging buffers [HR][SW][kCh], s_stride apart
     const unsigned s_addr = smem_addr(S);
-    const unsigned t_addr = s_addr + C::t_off;  // T [32][CS] halves
-    const unsigned o_addr = s_addr + C::o_off;  // output tile [OTH][OTW][32], 64B-swizzled
+    const unsigned t_addr = s_addr + C::t_off;  // T [kCh][CS] halves
+    const unsigned o_addr = s_addr + C::o_off;  // output tile [OTH][OTW][kCh], swizzled
     const T *wg = static_cast<const T *>(p.w);
 
     // Contiguous unit range of this CTA (channel tile slowest: few B reloads).
@@ -165,8 +184,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
     const int u_end = (int)((long long)g.units * (blockIdx.x + 1) / gridDim.x);
 
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int b = 0; b < kNS; ++b) mbar_init(&bar[b], 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -189,27 +207,28 @@ __global__ void __launch_bounds__(kMThreads, 1)
         const Unit un = ld;
         advance(ld);
         mbar_arrive_expect_tx(&bar[b], C::s_bytes);
-        tma_load_4d(S + b * C::s_stride, &halo_map, un.ctile * 32, un.twi * C::OTW - p.pad_w,
+        tma_load_4d(S + b * C::s_stride, &halo_map, un.ctile * kCh, un.twi * C::OTW - p.pad_w,
                     un.band * C::OTH - p.pad_h, un.group, &bar[b]);
     };
-    if (tid == 0) {
-        if (u_begin < u_end) issue(0);
-        if (u_begin + 1 < u_end) issue(1);
-    }
+    if (tid == 0)
+        for (int b = 0; b < kNS && u_begin + b < u_end; ++b) issue(b);
 
     // A operand x of a channel = one ldmatrix.x4: matrix j (lanes 8j..8j+7
     // give its row addresses) holds M rows 8(j%2)..+7 and k 8(j/2)..+7; M row
     // i of block j%2 is window i % G of input row x + i / G + DH (j%2).
     const int mj = lane / 8, mi = lane % 8;
     const int lane_off = ((mj & 1) * DH + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj >> 1);
-    // Transposition: this lane's row of its 8x8 matrix (matrix = channel chunk).
-    const int tr = lane % 8, tj = lane / 8;
+    // Transposition: one ldmatrix.x4 = kCh/8 16-byte channel chunks of each
+    // of 32/kCh rows; this lane addresses row tr of matrix tj.
+    constexpr int kChunks = kCh / 8, kTRows = 4 / kChunks;
+    const int tr = lane % 8, tj = lane / 8, t_chunk = tj % kChunks, t_row = tj / kChunks;
     // Output: lane (gq, t4) writes position (row gq / G (+ DH for M rows
-    // 8-15), column 8 (gq % G) + 2t4 + e) of each row set; bits 7-8 of the offset are t4 (OTW is a
-    // multiple of 8), so the swizzled 16-byte chunk is (warp / 2) ^ t4.
-    const unsigned o_lane = o_addr + ((gq / G) * C::OTW + 8 * (gq % G) + 2 * t4) * 64 +
-                            ((((unsigned)warp >> 1) ^ (unsigned)t4) & 3u) * 16 + (warp & 1) * 8;
-    const unsigned o_lane0 = o_lane + (gq & 1) * 64, o_lane1 = o_lane + (1 - (gq & 1)) * 64;
+    // 8-15), column 8 (gq % G) + 2t4 + e) of each row set; the bits the
+    // swizzle reads (7 and up) do not depend on the row set or on e, so the
+    // lane's swizzled chunk is fixed.
+    const unsigned o_pos = (unsigned)((gq / G) * C::OTW + 8 * (gq % G) + 2 * t4) * kPB;
+    const unsigned o_lane = o_addr + swz(o_pos + (unsigned)warp * 8);
+    const unsigned o_lane0 = o_lane + (gq & 1) * kPB, o_lane1 = o_lane + (1 - (gq & 1)) * kPB;
 
     int loaded_ctile = -1;
     float bias_r[kChPerWarp];
@@ -221,7 +240,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
             loaded_ctile = cur.ctile;
 #pragma unroll
             for (int ci = 0; ci < kChPerWarp; ++ci) {
-                const int cc = cur.ctile * 32 + warp * kChPerWarp + ci;
+                const int cc = cur.ctile * kCh + warp * kChPerWarp + ci;
                 const bool live = cc < p.C;
                 bias_r[ci] = (p.bias && live) ? p.bias[cc] : 0.f;
 #pragma unroll
@@ -242,28 +261,28 @@ __global__ void __launch_bounds__(kMThreads, 1)
                 }
             }
         }
-        if (!mbar_wait(&bar[k & 1], (k >> 1) & 1)) {
+        if (!mbar_wait(&bar[k % kNS], (k / kNS) & 1)) {
             report_timeout(err);
             return;
         }
 
-        // Transpose S[row][col][ch] -> T[ch][row][col], 8 cols x 32 ch per step:
-        // ldmatrix.trans gives lane (gq, t4) cols 2t4, 2t4+1 of channel 8j + gq;
-        // stmatrix writes them as the 16-byte row (channel, 8 cols).  Every warp
-        // finished reading T (previous unit) before the last barrier.
-        const unsigned s_buf = s_addr + (k & 1) * C::s_stride;
-        for (int b = warp; b < C::HR * (C::SW / 8); b += kMThreads / 32) {
-            const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
-            unsigned src = s_buf + (row * C::SW + col0 + tr) * 64 + 16 * tj;
-            src ^= ((src >> 7) & 3u) << 4;  // 64-byte swizzle
+        // Transpose S[row][col][ch] -> T[ch][row][col], 8 columns x kCh
+        // channels x kTRows rows per step: ldmatrix.trans gives lane (gq, t4)
+        // cols 2t4, 2t4+1 of channel 8 chunk + gq; stmatrix writes them as the
+        // 16-byte row (channel, row, 8 cols).  Every warp finished reading T
+        // (previous unit) before the last barrier.
+        const unsigned s_buf = s_addr + (k % kNS) * C::s_stride;
+        for (int b = warp; b < (C::HR / kTRows) * (C::SW / 8); b += kMThreads / 32) {
+            const int row = (b / (C::SW / 8)) * kTRows + t_row, col0 = (b % (C::SW / 8)) * 8;
+            const unsigned src = s_buf + swz((unsigned)((row * C::SW + col0 + tr) * kPB + 16 * t_chunk));
             unsigned v0, v1, v2, v3;
             ldsm_x4_trans(v0, v1, v2, v3, src);
-            stsm_x4(t_addr + 2u * ((8 * tj + tr) * C::CS + row * C::RS + col0), v0, v1, v2, v3);
+            stsm_x4(t_addr + 2u * ((8 * t_chunk + tr) * C::CS + row * C::RS + col0), v0, v1, v2, v3);
         }
         // The previous unit's TMA store must have read the output tile.
         if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
         __syncthreads();  // T ready, output tile free, this staging buffer free
-        if (tid == 0 && u + 2 < u_end) issue(k & 1);
+        if (tid == 0 && u + kNS < u_end) issue(k % kNS);
 
         // MMAs.  Row set j (j < kNB) covers output rows j*RB .. +RB-1 (M rows
         // 0-7) and the same rows + DH (M rows 8-15); MMA (j, fh) reads input
@@ -315,7 +334,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
                     hi[e] = Op::pack(d[2][j][2 * half + e], d[3][j][2 * half + e]);
                 }
                 const bool odd = gq & 1;
-                const unsigned row = (j * RB + half * DH) * C::OTW * 64;
+                const unsigned row = (j * RB + half * DH) * C::OTW * kPB;
                 asm volatile("st.shared.v2.b32 [%0], {%1, %2};\n" ::"r"(o_lane0 + row), "r"(odd ? lo[1] : lo[0]),
                              "r"(odd ? hi[1] : hi[0])
                              : "memory");
@@ -329,7 +348,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
             asm volatile(
                 "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];\n" ::"l"(
                     reinterpret_cast<uint64_t>(&out_map)),
-                "r"(cur.ctile * 32), "r"(cur.twi * C::OTW), "r"(cur.band * C::OTH), "r"(cur.group), "r"(o_addr)
+                "r"(cur.ctile * kCh), "r"(cur.twi * C::OTW), "r"(cur.band * C::OTH), "r"(cur.group), "r"(o_addr)
                 : "memory");
             asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
         }
@@ -344,7 +363,7 @@ bool plan(const TiledConv &p, GeoM &g) {
     g.tiles_h = (p.OHs + C::OTH - 1) / C::OTH;
     g.tiles_w = (p.OWs + C::OTW - 1) / C::OTW;
     const long long per = (long long)p.N * g.tiles_w * g.tiles_h;
-    const long long units = per * ((p.C + 31) / 32);
+    const long long units = per * ((p.C + kCh - 1) / kCh);
     if (units >= (1LL << 30)) return false;
     g.per_ctile = (int)per;
     g.units = (int)units;
@@ -364,13 +383,13 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
     const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
                              (uint64_t)p.Hf * p.Wf * p.C * es};
-    const uint32_t box[4] = {32, (uint32_t)C::SW, (uint32_t)C::HR, 1};
+    const uint32_t box[4] = {(uint32_t)kCh, (uint32_t)C::SW, (uint32_t)C::HR, 1};
     const uint64_t odims[4] = {(uint64_t)p.C, (uint64_t)p.OWf, (uint64_t)p.OHf, (uint64_t)p.N};
     const uint64_t ostr[3] = {(uint64_t)p.C * es, (uint64_t)p.OWf * p.C * es, (uint64_t)p.OHf * p.OWf * p.C * es};
-    const uint32_t obox[4] = {32, (uint32_t)C::OTW, (uint32_t)C::OTH, 1};
+    const uint32_t obox[4] = {(uint32_t)kCh, (uint32_t)C::OTW, (uint32_t)C::OTH, 1};
     CUtensorMap map, omap;
-    if (!encode_tmap_4d(&map, dt, base, dims, str, box, true) ||
-        !encode_tmap_4d(&omap, dt, p.out, odims, ostr, obox, true))
+    if (!encode_tmap_4d(&map, dt, base, dims, str, box, kPB) ||
+        !encode_tmap_4d(&omap, dt, p.out, odims, ostr, obox, kPB))
         return cudaErrorNotSupported;
     auto kern = tiled_mma_kernel<T, FH, FW, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem + 1024);

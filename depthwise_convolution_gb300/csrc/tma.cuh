@@ -24,9 +24,10 @@ unsigned *device_error_word();
 cudaError_t take_device_error(cudaStream_t st, unsigned *value);
 
 // 4-D tiled tensor map, dims innermost first (C, W, H, N), strides in bytes
-// for dims 1..3, box in elements; swizzle64: 64-byte shared-memory swizzle
-// (the inner box row must then be 64 bytes); l2_promotion: L2 fetch size in
-// bytes (0, 64, 128 or 256).  Returns false if the driver rejects it.
+// for dims 1..3, box in elements; swizzle: shared-memory swizzle span in
+// bytes (0 = none, 32 or 64; the inner box row must then be exactly that
+// long); l2_promotion: L2 fetch size in bytes (0, 64, 128 or 256).  Returns
+// false if the driver rejects it.
 //
 // 64 is the default: a unit's box row is one 32-channel slice (64 bytes for
 // 16-bit data) of a pixel, and with 128-byte promotion the halo rows that
@@ -36,7 +37,7 @@ cudaError_t take_device_error(cudaStream_t st, unsigned *value);
 #define DWCONV_L2_PROMO 64
 #endif
 bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const uint64_t dims[4],
-                    const uint64_t strides[3], const uint32_t box[4], bool swizzle64 = false,
+                    const uint64_t strides[3], const uint32_t box[4], int swizzle = 0,
                     int l2_promotion = DWCONV_L2_PROMO);
 
 __device__ __forceinline__ unsigned smem_addr(const void *p) {

@@ -56,7 +56,7 @@ cudaError_t take_device_error(cudaStream_t st, unsigned *value) {
 }
 
 bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const uint64_t dims[4],
-                    const uint64_t strides[3], const uint32_t box[4], bool swizzle64, int l2_promotion) {
+                    const uint64_t strides[3], const uint32_t box[4], int swizzle, int l2_promotion) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     CUtensorMapDataType t;
@@ -74,7 +74,14 @@ bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const u
     const cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
     const cuuint32_t bd[4] = {box[0], box[1], box[2], box[3]};
     const cuuint32_t es[4] = {1, 1, 1, 1};
-    if (swizzle64 && box[0] * (dt == DWCONV_FP32 ? 4u : 2u) != 64u) return false;
+    CUtensorMapSwizzle swz;
+    switch (swizzle) {
+        case 0: swz = CU_TENSOR_MAP_SWIZZLE_NONE; break;
+        case 32: swz = CU_TENSOR_MAP_SWIZZLE_32B; break;
+        case 64: swz = CU_TENSOR_MAP_SWIZZLE_64B; break;
+        default: return false;
+    }
+    if (swizzle && box[0] * (dt == DWCONV_FP32 ? 4u : 2u) != (unsigned)swizzle) return false;
     CUtensorMapL2promotion promo;
     switch (l2_promotion) {
         case 0: promo = CU_TENSOR_MAP_L2_PROMOTION_NONE; break;
@@ -84,7 +91,7 @@ bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const u
         default: return false;
     }
     CUresult r = fn(map, t, 4, const_cast<void *>(base), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    swz,
                     promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
