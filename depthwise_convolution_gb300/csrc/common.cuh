@@ -152,6 +152,8 @@ cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t
 // Tensor-core (mma.sync) forward and stride-1 input gradient for 16-bit data,
 // 3x3 / 5x5 / 7x7 filters, maps more than 16 columns wide.
 cudaError_t launch_tiled_mma(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
+// Tensor-core Toeplitz kernel for large 16-bit filters (tiled_mma_large.cu).
+cudaError_t launch_tiled_mma_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 
 // Large filters (FW >= 8, any FH), forward and stride-1 input gradient.
 cudaError_t launch_tiled_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);

@@ -193,6 +193,7 @@ dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride,
         p.OHf = s.OH; p.OWf = s.OW; p.OHs = s.OH; p.OWs = s.OW;
         p.out_step = 1; p.out_off = 0; p.zero_phases = 0;
         cudaError_t e = launch_tiled_mma(p, dtype, cs);
+        if (e == cudaErrorNotSupported) e = launch_tiled_mma_large(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_small(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
@@ -232,6 +233,7 @@ dwconv_status dwconv_bwd_data(int N, int H, int W, int C, int FH, int FW, int st
         p.OHs = (H + S - 1) / S; p.OWs = (W + S - 1) / S;
         p.out_step = S; p.out_off = ph; p.zero_phases = S > 1 ? 1 : 0;
         cudaError_t e = launch_tiled_mma(p, dtype, cs);
+        if (e == cudaErrorNotSupported) e = launch_tiled_mma_large(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_small(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);

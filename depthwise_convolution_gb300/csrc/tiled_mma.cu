@@ -35,12 +35,13 @@
 //      tensor edges by the copy engine).
 // Two CTA barriers per unit: "T and the output tile are ready" and "the
 // output tile is complete (and every warp is done with T)".
-#include "tiled_common.cuh"
+#include "mma_common.cuh"
 
 namespace dwc {
 namespace {
 
 using namespace tiled;
+using namespace mma;
 
 #ifndef DWCONV_MMA_CH
 #define DWCONV_MMA_CH 32  // channels per work unit (16 or 32)
@@ -72,7 +73,7 @@ struct Cfg {
     static constexpr int RS = SW;                          // T row stride (halves)
     // T channel stride: = 8 mod 16 halves, so stmatrix rows of 8 channels
     // land in distinct banks.
-    static constexpr int CS = (HR * RS) % 16 == 8 ? HR * RS : (HR * RS) + ((8 - (HR * RS) % 16 + 16) % 16);
+    static constexpr int CS = channel_stride(HR * RS);
     static constexpr unsigned s_bytes = HR * SW * kPB;
     static constexpr unsigned s_stride = (s_bytes + 1023u) & ~1023u;
     static constexpr unsigned t_off = kNS * s_stride;
@@ -81,80 +82,6 @@ struct Cfg {
     static_assert(CS % 16 == 8, "channel stride");
     static_assert(HR % (4 / (kCh / 8)) == 0, "transposition steps cover whole row groups");
 };
-
-struct GeoM {
-    int tiles_h, tiles_w, per_ctile, units;
-};
-
-__device__ __forceinline__ void ldsm_x4_trans(unsigned &r0, unsigned &r1, unsigned &r2, unsigned &r3,
-                                              unsigned addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4(unsigned &r0, unsigned &r1, unsigned &r2, unsigned &r3,
-                                        unsigned addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(unsigned &r0, unsigned &r1, unsigned addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];\n"
-                 : "=r"(r0), "=r"(r1)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void stsm_x4(unsigned addr, unsigned r0, unsigned r1, unsigned r2, unsigned r3) {
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(r0),
-                 "r"(r1), "r"(r2), "r"(r3)
-                 : "memory");
-}
-
-template <typename T> struct MmaOp;
-template <> struct MmaOp<__nv_bfloat16> {
-    static __device__ __forceinline__ void run(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
-                                               unsigned b0, unsigned b1) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%2,%3};\n"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-    static __device__ __forceinline__ unsigned pack(float lo, float hi) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<unsigned *>(&v);
-    }
-    static __device__ __forceinline__ unsigned pack_raw(__nv_bfloat16 lo, __nv_bfloat16 hi) {
-        return (unsigned)__bfloat16_as_ushort(lo) | ((unsigned)__bfloat16_as_ushort(hi) << 16);
-    }
-};
-template <> struct MmaOp<__half> {
-    static __device__ __forceinline__ void run(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
-                                               unsigned b0, unsigned b1) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%2,%3};\n"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-    static __device__ __forceinline__ unsigned pack(float lo, float hi) {
-        __half2 v = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<unsigned *>(&v);
-    }
-    static __device__ __forceinline__ unsigned pack_raw(__half lo, __half hi) {
-        return (unsigned)__half_as_ushort(lo) | ((unsigned)__half_as_ushort(hi) << 16);
-    }
-};
-
-__device__ __forceinline__ Unit decode_m(const GeoM &g, int u) {
-    Unit r;
-    r.ctile = u / g.per_ctile;
-    int v = u - r.ctile * g.per_ctile;
-    r.band = v % g.tiles_h;
-    v /= g.tiles_h;
-    r.twi = v % g.tiles_w;
-    r.group = v / g.tiles_w;
-    return r;
-}
 
 template <typename T, int FH, int FW, int G>
 __global__ void __launch_bounds__(kMThreads, kMinCtas)
@@ -190,22 +117,10 @@ __global__ void __launch_bounds__(kMThreads, kMinCtas)
     __syncthreads();
 
     // Unit cursors (row band fastest) for the loads (thread 0) and the compute.
-    Unit ld = decode_m(g, u_begin), cur = ld;
-    auto advance = [&](Unit &c) {
-        if (++c.band == g.tiles_h) {
-            c.band = 0;
-            if (++c.twi == g.tiles_w) {
-                c.twi = 0;
-                if (++c.group == p.N) {
-                    c.group = 0;
-                    ++c.ctile;
-                }
-            }
-        }
-    };
+    Unit ld = decode(g, u_begin), cur = ld;
     auto issue = [&](int b) {
         const Unit un = ld;
-        advance(ld);
+        advance(g, p.N, ld);
         mbar_arrive_expect_tx(&bar[b], C::s_bytes);
         tma_load_4d(S + b * C::s_stride, &halo_map, un.ctile * kCh, un.twi * C::OTW - p.pad_w,
                     un.band * C::OTH - p.pad_h, un.group, &bar[b]);
@@ -233,7 +148,7 @@ __global__ void __launch_bounds__(kMThreads, kMinCtas)
     int loaded_ctile = -1;
     float bias_r[kChPerWarp];
     unsigned bfr[kChPerWarp][FH][2];  // Toeplitz bands, B fragments (k 0-7, k 8-15)
-    for (int u = u_begin, k = 0; u < u_end; ++u, ++k, advance(cur)) {
+    for (int u = u_begin, k = 0; u < u_end; ++u, ++k, advance(g, p.N, cur)) {
         if (cur.ctile != loaded_ctile) {
             // B[k][n] = w[fh][k - n]: lane (gq, t4) holds k = 2t4, 2t4+1 (+8), n = gq.
             // For the input gradient the filter is rotated by 180 degrees.

@@ -35,6 +35,10 @@ SMALL = [
     (2, 20, 19, 40, 9, 13, 1, 1, 5),     # large-filter path, FH != FW, channel tail
     (1, 33, 30, 64, 11, 11, 2, 2, 10),   # large filter on the stride-2 dilation-2 sub-grid
     (3, 9, 30, 32, 15, 15, 1, 1, 7),     # large filter, map shorter than the filter
+    (2, 24, 21, 40, 31, 31, 1, 1, 15),   # 31x31 tensor-core path on a narrow map, 5 channel tiles
+    (1, 30, 45, 24, 13, 13, 1, 1, 6),    # 13x13 tensor-core path, ragged row band
+    (2, 19, 20, 16, 13, 9, 1, 1, 4),     # FH != FW on the large tensor-core path
+    (1, 41, 41, 16, 13, 13, 2, 2, 12),   # 13x13 on the stride-2 dilation-2 sub-grid
 ]
 
 
