@@ -11,9 +11,13 @@ value     nominal GFLOP/s (2*N*OH*OW*C*FH*FW per pass, three passes) over the
           over ranks (each rank runs its own batch: weak scaling, no exchange).
 e2e       the same metric with host (pinned) buffers: each step copies x, w, dy
           to the device and y, dx, dw back, inside the timed region.
-roofline  for the pass that takes the most time: valid-tap flops per launch over
-          its CUDA-event duration, against the fp32 FMA peak derived from the
-          SM count and maximum SM clock (the passes run on the FMA pipe).
+roofline  per pass: min(compute peak, HBM bandwidth x arithmetic intensity from
+          unique bytes), where the compute peak is that of the unit the pass's
+          kernel runs on (reported by the library): the measured dense bf16
+          tensor peak for the tensor-core kernels, the fp32 FMA peak derived
+          from the SM count and maximum SM clock for the others.  The
+          top-level object is the pass that takes the most time, in its
+          binding unit (TFLOP/s for a compute bound, GB/s for HBM).
 cpu_baseline  the oracle (float64 direct loops) timed on this host's cores on a
           bounded sample of the same workload (rank 0, N=1 only).
 --impl reference  times that oracle alone, as the reference arm.
@@ -42,6 +46,7 @@ DEFAULT_WORKLOAD = "fp16-train-7x7-128x56x56x96"
 METRIC = "DWC fwd/dgrad/wgrad GFLOP/s and HBM GB/s as % of roofline on 1xGB300"
 L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2, written between timed steps
 FMA_LANES_PER_SM = 128              # fp32 FMA units per SM on Blackwell
+TENSOR_KERNELS = {"tiled_mma", "tiled_mma_large"}   # kernel families on the tensor pipe
 
 
 # ----------------------------------------------------------------- helpers
@@ -55,13 +60,27 @@ def dist_env():
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    out = {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+    out = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "source": "fallback"}
     if os.path.exists(path):
         with open(path) as f:
             m = json.load(f)
-        out.update({"hbm_gbs": float(m["hbm_gbs"]), "sm_max_mhz": float(m.get("sm_max_mhz", 2070.0)),
-                    "source": "measured"})
+        out.update({"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m.get("bf16_tflops", 1900.0)),
+                    "sm_max_mhz": float(m.get("sm_max_mhz", 2070.0)), "source": "measured"})
     return out
+
+
+def pass_roofline(kernel, valid_flops, unique_bytes, t_ms, pk, fma_peak_tflops):
+    """Roofline of one pass: the binding unit, its peak, what was achieved, the fraction."""
+    tensor = kernel in TENSOR_KERNELS
+    peak_tf = pk["bf16_tflops"] if tensor else fma_peak_tflops
+    t_compute = valid_flops / (peak_tf * 1e12)
+    t_memory = unique_bytes / (pk["hbm_gbs"] * 1e9)
+    t = t_ms * 1e-3
+    if t_compute >= t_memory:
+        return {"bound": "tensor" if tensor else "alu", "achieved": round(valid_flops / t / 1e12, 3),
+                "peak": round(peak_tf, 2), "unit": "TFLOP/s", "frac": round(t_compute / t, 4)}
+    return {"bound": "hbm", "achieved": round(unique_bytes / t / 1e9, 1), "peak": round(pk["hbm_gbs"], 1),
+            "unit": "GB/s", "frac": round(t_memory / t, 4)}
 
 
 def csrc_sha():
@@ -188,9 +207,12 @@ def time_layer(layer, steps, warmup, flush):
     """Per-pass CUDA-event times (ms) over `steps` steps, L2 flushed before each."""
     passes = layer.wl.passes
     stream = torch.cuda.current_stream()
-    for _ in range(warmup):
+    layer.kernel = {}
+    for i in range(warmup):
         for p in passes:
             layer.run_pass(p)
+            if i == 0:
+                layer.kernel[p] = ops.dwconv_last_kernel()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)] for _ in range(steps)]
     launches0 = ops.dwconv_launch_count()
@@ -348,21 +370,22 @@ def main():
     for p in wl.passes:
         t_ms = statistics.mean(per_pass[p])
         ub = layer.unique(p)
-        t_roof = max(layer.valid / (fma_peak_tflops * 1e12), ub / (pk["hbm_gbs"] * 1e9))
+        rf = pass_roofline(layer.kernel[p], layer.valid, ub, t_ms, pk, fma_peak_tflops)
         passes[p] = {"ms": round(t_ms, 4), "ms_median": round(statistics.median(per_pass[p]), 4),
+                     "kernel": layer.kernel[p],
                      "gflops_nominal": round(layer.nominal / t_ms / 1e6, 1),
                      "gflops_valid": round(layer.valid / t_ms / 1e6, 1),
                      "gbs_unique": round(ub / t_ms / 1e6, 1),
-                     "roofline_frac": round(t_roof / (t_ms * 1e-3), 4)}
+                     "bound": rf["bound"], "roofline_frac": rf["frac"]}
     dom = max(passes, key=lambda p: passes[p]["ms"])
-    achieved = layer.valid / (passes[dom]["ms"] * 1e-3) / 1e12
-    roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(fma_peak_tflops, 2),
-                "unit": "TFLOP/s", "frac": round(achieved / fma_peak_tflops, 4),
-                "traffic": recorded_traffic(wl.name, dom), "kernel": f"{dom} ({wl.name})",
-                "peak_source": f"derived: {sms} SMs x {FMA_LANES_PER_SM} fp32 FMA lanes x 2 flop x "
-                               f"{pk['sm_max_mhz']:.0f} MHz (max SM clock)",
-                "flops_per_launch": layer.valid,
-                "hbm_peak_gbs": pk["hbm_gbs"], "hbm_peak_source": pk["source"]}
+    rf = pass_roofline(layer.kernel[dom], layer.valid, layer.unique(dom), passes[dom]["ms"], pk, fma_peak_tflops)
+    tensor = layer.kernel[dom] in TENSOR_KERNELS
+    roofline = dict(rf, traffic=recorded_traffic(wl.name, dom), kernel=f"{dom}: {layer.kernel[dom]} ({wl.name})",
+                    peak_source=(f"measured dense bf16 (cuBLAS) {pk['bf16_tflops']} TFLOP/s" if tensor else
+                                 f"derived: {sms} SMs x {FMA_LANES_PER_SM} fp32 FMA lanes x 2 flop x "
+                                 f"{pk['sm_max_mhz']:.0f} MHz (max SM clock)") + f"; HBM {pk['hbm_gbs']} GB/s",
+                    peak_kind=pk["source"], flops_per_launch=layer.valid,
+                    unique_bytes_per_launch=layer.unique(dom))
 
     e2e_ms, h2d, d2h = time_e2e(layer, max(10, args.steps // 10))
     if ws > 1:
@@ -384,10 +407,11 @@ def main():
                 for p in other.passes:
                     t_ms = statistics.mean(pp[p])
                     ub = lay.unique(p)
-                    t_roof = max(lay.valid / (fma_peak_tflops * 1e12), ub / (pk["hbm_gbs"] * 1e9))
-                    entry[p] = {"ms": round(t_ms, 4), "gflops_nominal": round(lay.nominal / t_ms / 1e6, 1),
+                    rf = pass_roofline(lay.kernel[p], lay.valid, ub, t_ms, pk, fma_peak_tflops)
+                    entry[p] = {"ms": round(t_ms, 4), "kernel": lay.kernel[p],
+                                "gflops_nominal": round(lay.nominal / t_ms / 1e6, 1),
                                 "gbs_unique": round(ub / t_ms / 1e6, 1),
-                                "roofline_frac": round(t_roof / (t_ms * 1e-3), 4)}
+                                "bound": rf["bound"], "roofline_frac": rf["frac"]}
                 sweep[name] = entry
                 del lay
             except Exception as e:  # report, do not hide

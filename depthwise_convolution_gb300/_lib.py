@@ -29,6 +29,7 @@ SIGNATURES = {
     "dwconv_check_device_errors": (_I, [_P]),
     "dwconv_status_string": (ctypes.c_char_p, [_I]),
     "dwconv_launch_count": (ctypes.c_ulonglong, []),
+    "dwconv_last_kernel": (ctypes.c_char_p, []),
 }
 
 

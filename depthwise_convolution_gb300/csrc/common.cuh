@@ -18,6 +18,9 @@ struct Shape {
 
 // Counts kernel launches for dwconv_launch_count().
 void note_launches(int n);
+// Records the kernel family of the calling thread's latest pass for
+// dwconv_last_kernel() (a static string).
+void note_kernel(const char *family);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -191,6 +191,7 @@ cudaError_t launch_fwd_direct(const Shape &s, dwconv_dtype dt, const void *x, co
             return cudaErrorInvalidValue;
     }
     note_launches(1);
+    note_kernel("direct_fwd");
     return cudaGetLastError();
 }
 
@@ -215,6 +216,7 @@ cudaError_t launch_dgrad_direct(const Shape &s, dwconv_dtype dt, const void *dy,
             return cudaErrorInvalidValue;
     }
     note_launches(1);
+    note_kernel("direct_dgrad");
     return cudaGetLastError();
 }
 
@@ -236,6 +238,7 @@ cudaError_t launch_wgrad_direct(const Shape &s, dwconv_dtype dt, const void *x, 
             return cudaErrorInvalidValue;
     }
     note_launches(1);
+    note_kernel("direct_wgrad");
     return cudaGetLastError();
 }
 

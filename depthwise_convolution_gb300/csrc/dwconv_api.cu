@@ -18,6 +18,11 @@ std::atomic<int> g_sm_count[kMaxDevices];
 
 void note_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
+namespace {
+thread_local const char *t_last_kernel = "none";
+}
+void note_kernel(const char *family) { t_last_kernel = family; }
+
 int sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
@@ -154,6 +159,8 @@ const char *dwconv_status_string(dwconv_status status) {
 }
 
 unsigned long long dwconv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *dwconv_last_kernel(void) { return dwc::t_last_kernel; }
 
 dwconv_status dwconv_check_device_errors(dwconv_stream stream) {
     unsigned v = 0;

@@ -320,6 +320,7 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     const int grid = (int)std::min<long long>(g.units, slots);
     kern<<<grid, kLThreads + 32, smem, st>>>(row_map, filt_map, p, g, device_error_word());
     note_launches(1);
+    note_kernel("tiled_large");
     return cudaGetLastError();
 }
 

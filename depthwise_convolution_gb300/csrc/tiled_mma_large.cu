@@ -118,20 +118,24 @@ __global__ void __launch_bounds__(kLThreads, 1)
     float bias_c = 0.f;
     for (int u = u_begin, k = 0; u < u_end; ++u, ++k, advance(g, p.N, cur)) {
         if (cur.ctile != loaded_ctile) {
-            // Every warp finished reading F (previous unit) before the last barrier.
+            // Every warp finished reading F (previous unit) before the last
+            // barrier.  Zero the table, then scatter the filter: value (fh, fw)
+            // of channel c goes to index fw + 8 - q of copy q of row fh (rows
+            // rotated by 180 degrees for the input gradient).
             loaded_ctile = cur.ctile;
-            for (int row = tid; row < kLCh * FH * 2; row += kLThreads) {
-                const int q = row % 2, fh = (row / 2) % FH, c = row / (2 * FH);
+            constexpr int kWords = kLCh * FH * 2 * C::FP / 8;  // 16-byte words
+            for (int i = tid; i < kWords; i += kLThreads) reinterpret_cast<uint4 *>(F)[i] = make_uint4(0, 0, 0, 0);
+            __syncthreads();
+            const int nw = kLCh * FH * p.FW;
+            for (int i = tid; i < nw; i += kLThreads) {
+                const int c = i % kLCh, t = i / kLCh, fw = t % p.FW, fh = t / p.FW;
                 const int cc = cur.ctile * kLCh + c;
-                const int sfh = p.flip ? FH - 1 - fh : fh;
-                T *dst = F + row * C::FP;
-                for (int i = 0; i < C::FP; ++i) {
-                    const int fw = i + q - 8;
-                    T v = from_f32<T>(0.f);
-                    if (fw >= 0 && fw < p.FW && cc < p.C)
-                        v = wg[(sfh * p.FW + (p.flip ? p.FW - 1 - fw : fw)) * p.C + cc];
-                    dst[i] = v;
-                }
+                if (cc >= p.C) continue;
+                const T v = __ldg(wg + (size_t)t * p.C + cc);
+                const int dfh = p.flip ? FH - 1 - fh : fh, dfw = p.flip ? p.FW - 1 - fw : fw;
+                T *row = F + (c * FH + dfh) * 2 * C::FP;
+                row[dfw + 8] = v;            // copy 0
+                row[C::FP + dfw + 7] = v;    // copy 1
             }
             const int cc = cur.ctile * kLCh + warp;
             bias_c = (p.bias && cc < p.C) ? p.bias[cc] : 0.f;
@@ -245,6 +249,7 @@ cudaError_t run_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     const int grid = (int)std::min<long long>(g.units, (long long)sm_count() * per_sm);
     kern<<<grid, kLThreads, C::smem + 1024, st>>>(map, omap, p, g, device_error_word());
     note_launches(1);
+    note_kernel("tiled_mma_large");
     return cudaGetLastError();
 }
 

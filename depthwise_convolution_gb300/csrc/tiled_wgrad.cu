@@ -198,6 +198,7 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t s
     if (e != cudaSuccess) return e;
     kern<<<g.ctiles * Zc, kThreads, smem, st>>>(halo_map, dy_map, p, g, part, Zc, device_error_word());
     note_launches(1);
+    note_kernel("tiled_wgrad");
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_wgrad_reduce(part, Zc, (long long)p.FH * p.FW * p.C, static_cast<float *>(p.out), st);

@@ -156,3 +156,8 @@ def dwconv_check_device_errors(stream=None) -> None:
 def dwconv_launch_count() -> int:
     """Kernels libdwconv has launched in this process."""
     return int(_lib.load().dwconv_launch_count())
+
+
+def dwconv_last_kernel() -> str:
+    """Kernel family of the latest pass launched from this thread."""
+    return _lib.load().dwconv_last_kernel().decode()

@@ -176,6 +176,19 @@ const char *dwconv_status_string(dwconv_status status);
  */
 unsigned long long dwconv_launch_count(void);
 
+/*
+ * Kernel family of the latest pass this host thread launched, as a static
+ * string: "tiled_mma" (tensor-core Toeplitz, 16-bit 3x3/5x5/7x7),
+ * "tiled_mma_large" (tensor-core Toeplitz, large 16-bit filters),
+ * "tiled_small" / "tiled_large" (register-tiled FMA kernels), "tiled_wgrad"
+ * (tiled weight gradient), "direct_fwd" / "direct_dgrad" / "direct_wgrad"
+ * (one output per thread), or "none" before the first launch.  The host-side
+ * dispatch sets it when it launches; it says nothing about completion.  For
+ * reporting which kernel ran (e.g. against which roofline to measure it).
+ * No counterpart in the method's description: introspection only.
+ */
+const char *dwconv_last_kernel(void);
+
 #ifdef __cplusplus
 }
 #endif

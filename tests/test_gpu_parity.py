@@ -125,3 +125,27 @@ def test_zero_input_gives_bias_only():
     b = torch.randn(32, device="cuda")
     y = ops.dwconv_fwd(x, w, b, 1, 1, 3)
     assert torch.equal(y.float(), b.to(torch.bfloat16).float().expand_as(y))
+
+
+@pytest.mark.parametrize("dtype,case,pass_name,family", [
+    ("fp16", (2, 40, 40, 32, 7, 7, 1, 1, 3), "fwd", "tiled_mma"),
+    ("bf16", (2, 40, 40, 32, 7, 7, 1, 1, 3), "dgrad", "tiled_mma"),
+    ("bf16", (1, 40, 40, 32, 31, 31, 1, 1, 15), "fwd", "tiled_mma_large"),
+    ("fp32", (2, 40, 40, 32, 7, 7, 1, 1, 3), "fwd", "tiled_small"),
+    ("bf16", (1, 30, 30, 32, 15, 15, 1, 1, 7), "fwd", "tiled_large"),
+    ("fp16", (2, 40, 40, 32, 7, 7, 1, 1, 3), "wgrad", "tiled_wgrad"),
+    ("bf16", (2, 10, 10, 5, 3, 3, 1, 1, 1), "fwd", "direct_fwd"),
+])
+def test_kernel_family_reported(dtype, case, pass_name, family):
+    """The dispatch picks the intended kernel family, and says so."""
+    N, H, W, C, FH, FW, S, D, P = case
+    d = random_inputs(dtype, N, H, W, C, FH, FW, S, D, P, seed=11)
+    x, w, dy = d["x"].cuda(), d["w"].cuda(), d["dy"].cuda()
+    if pass_name == "fwd":
+        ops.dwconv_fwd(x, w, None, S, D, P)
+    elif pass_name == "dgrad":
+        ops.dwconv_bwd_data(dy, w, H, W, S, D, P)
+    else:
+        ops.dwconv_bwd_filter(x, dy, FH, FW, S, D, P)
+    torch.cuda.synchronize()
+    assert ops.dwconv_last_kernel() == family
