@@ -152,14 +152,26 @@ __global__ void __launch_bounds__(kThreads) wgrad_direct(Shape s, const T *__res
     }
 }
 
-__global__ void __launch_bounds__(kThreads) wgrad_reduce(const float *__restrict__ part, int Z,
-                                                         long long count,
-                                                         float *__restrict__ dw) {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < count;
-         i += (long long)gridDim.x * blockDim.x) {
-        float sum = 0.f;
-        for (int z = 0; z < Z; ++z) sum += part[(long long)z * count + i];
-        dw[i] = sum;
+// dw[i] = sum over slices z of part[z][i], in a fixed order: warp r of a
+// block sums the slices z = r, r + 8, r + 16, ... (increasing), then the 8
+// warp sums are added in warp order.  A block covers 32 consecutive elements
+// (coalesced loads per slice); 8 independent chains per element keep enough
+// loads in flight for a grid of count/32 blocks.
+constexpr int kReduceWarps = 8;
+__global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce(const float *__restrict__ part, int Z,
+                                                                  long long count, float *__restrict__ dw) {
+    __shared__ float acc[kReduceWarps][32];
+    const int lane = threadIdx.x % 32, r = threadIdx.x / 32;
+    const long long i = blockIdx.x * 32LL + lane;
+    float sum = 0.f;
+    if (i < count)
+        for (int z = r; z < Z; z += kReduceWarps) sum += part[(long long)z * count + i];
+    acc[r][lane] = sum;
+    __syncthreads();
+    if (r == 0 && i < count) {
+        float t = acc[0][lane];
+        for (int q = 1; q < kReduceWarps; ++q) t += acc[q][lane];
+        dw[i] = t;
     }
 }
 
@@ -244,7 +256,9 @@ cudaError_t launch_wgrad_direct(const Shape &s, dwconv_dtype dt, const void *x, 
 
 cudaError_t launch_wgrad_reduce(const float *part, int Z, long long count, float *dw,
                                 cudaStream_t st) {
-    wgrad_reduce<<<grid_for(count), kThreads, 0, st>>>(part, Z, count, dw);
+    const long long blocks = (count + 31) / 32;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    wgrad_reduce<<<(unsigned)blocks, 32 * kReduceWarps, 0, st>>>(part, Z, count, dw);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -26,6 +26,11 @@ __device__ __forceinline__ void ldsm_x4(unsigned &r0, unsigned &r1, unsigned &r2
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
 }
+__device__ __forceinline__ void ldsm_x2(unsigned &r0, unsigned &r1, unsigned addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];\n"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(addr));
+}
 __device__ __forceinline__ void stsm_x4(unsigned addr, unsigned r0, unsigned r1, unsigned r2, unsigned r3) {
     asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(r0),
                  "r"(r1), "r"(r2), "r"(r3)

@@ -46,6 +46,9 @@ using namespace mma;
 #ifndef DWCONV_MMA_CH
 #define DWCONV_MMA_CH 32  // channels per work unit (16 or 32)
 #endif
+#ifndef DWCONV_MMA_REUSE
+#define DWCONV_MMA_REUSE 4  // G for which half of each A operand is rebuilt from registers (0: none)
+#endif
 #ifndef DWCONV_MMA_NS
 #define DWCONV_MMA_NS 2  // halo staging buffers (1 or 2)
 #endif
@@ -133,6 +136,8 @@ __global__ void __launch_bounds__(kMThreads, kMinCtas)
     // i of block j%2 is window i % G of input row x + i / G + DH (j%2).
     const int mj = lane / 8, mi = lane % 8;
     const int lane_off = ((mj & 1) * DH + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj >> 1);
+    // ldmatrix.x2 of rows x + DH alone: matrix mj & 1 = k half.
+    const int lane_off2 = (DH + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj & 1);
     // Transposition: one ldmatrix.x4 = kCh/8 16-byte channel chunks of each
     // of 32/kCh rows; this lane addresses row tr of matrix tj.
     constexpr int kChunks = kCh / 8, kTRows = 4 / kChunks;
@@ -206,11 +211,26 @@ __global__ void __launch_bounds__(kMThreads, kMinCtas)
         // also across channels) and runs the MMAs of operand x, row sets
         // interleaved (independent accumulators).
         float d[kChPerWarp][kNB][4];
-        unsigned A[2][4];  // slot = stage number (over all channels) mod 2
+        // With kReuse, operand x >= DH shares its rows-x half with operand
+        // x - DH (whose rows-(x - DH + DH) half it is): that half is copied
+        // from registers and only rows x + DH are loaded (one ldmatrix.x2).
+        // Measured: a gain for G = 4; for G = 8 the extra registers spill.
+        constexpr bool kReuse = DWCONV_MMA_REUSE == G;
+        unsigned A[kReuse ? kChPerWarp : 1][kReuse ? NQ : 2][4];
         auto load_a = [&](int ci, int x) {
-            const int sl = (ci * NQ + x) & 1;
-            ldsm_x4(A[sl][0], A[sl][1], A[sl][2], A[sl][3],
-                    t_addr + 2u * ((warp * kChPerWarp + ci) * C::CS + x * C::RS + lane_off));
+            const unsigned base = t_addr + 2u * ((warp * kChPerWarp + ci) * C::CS + x * C::RS);
+            if constexpr (kReuse) {
+                if (x < DH) {
+                    ldsm_x4(A[ci][x][0], A[ci][x][1], A[ci][x][2], A[ci][x][3], base + 2u * lane_off);
+                } else {
+                    A[ci][x][0] = A[ci][x - DH][1];
+                    A[ci][x][2] = A[ci][x - DH][3];
+                    ldsm_x2(A[ci][x][1], A[ci][x][3], base + 2u * lane_off2);
+                }
+            } else {
+                const int sl = (ci * NQ + x) & 1;  // stage number (over all channels) mod 2
+                ldsm_x4(A[0][sl][0], A[0][sl][1], A[0][sl][2], A[0][sl][3], base + 2u * lane_off);
+            }
         };
         load_a(0, 0);
 #pragma unroll
@@ -223,12 +243,16 @@ __global__ void __launch_bounds__(kMThreads, kMinCtas)
                     load_a(ci, x + 1);
                 else if (ci + 1 < kChPerWarp)
                     load_a(ci + 1, 0);
-                const int sl = (ci * NQ + x) & 1;
+                const unsigned *a;
+                if constexpr (kReuse)
+                    a = A[ci][x];
+                else
+                    a = A[0][(ci * NQ + x) & 1];
 #pragma unroll
                 for (int j = 0; j < kNB; ++j) {
                     const int fh = x - j * RB;
                     if (fh >= 0 && fh < FH)
-                        Op::run(d[ci][j], A[sl][0], A[sl][1], A[sl][2], A[sl][3], bfr[ci][fh][0], bfr[ci][fh][1]);
+                        Op::run(d[ci][j], a[0], a[1], a[2], a[3], bfr[ci][fh][0], bfr[ci][fh][1]);
                 }
             }
         }
