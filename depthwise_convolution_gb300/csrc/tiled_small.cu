@@ -40,9 +40,19 @@ using namespace tiled;
 #define DWCONV_S16_TW 7
 #endif
 
+#ifndef DWCONV_S32_MINB
+#define DWCONV_S32_MINB 3
+#endif
+#ifndef DWCONV_S32_SMEM_KB
+#define DWCONV_S32_SMEM_KB 72
+#endif
+#ifndef DWCONV_S32_TH
+#define DWCONV_S32_TH 2
+#endif
+
 template <typename T>
 size_t smem_cap() {
-    return sizeof(T) == 4 ? 100 * 1024 : DWCONV_S16_SMEM_KB * 1024;
+    return sizeof(T) == 4 ? DWCONV_S32_SMEM_KB * 1024 : DWCONV_S16_SMEM_KB * 1024;
 }
 
 
@@ -204,8 +214,8 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
 template <typename T>
 cudaError_t dispatch_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     constexpr bool k16 = sizeof(T) == 2;
-    constexpr int TH7 = k16 ? DWCONV_S16_TH : 4, TW7 = k16 ? DWCONV_S16_TW : 7;
-    constexpr int MB7 = k16 ? DWCONV_S16_MINB : 2;
+    constexpr int TH7 = k16 ? DWCONV_S16_TH : DWCONV_S32_TH, TW7 = k16 ? DWCONV_S16_TW : 7;
+    constexpr int MB7 = k16 ? DWCONV_S16_MINB : DWCONV_S32_MINB;
     if (p.zero_phases) {
         if (p.out_step != 2) return cudaErrorNotSupported;
         if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 2>(p, dt, st);
