@@ -11,7 +11,7 @@ namespace mma {
 using tiled::Unit;
 
 struct GeoM {
-    int tiles_h, tiles_w, per_ctile, units;
+    int tiles_h, tiles_w, groups, per_ctile, units;  // groups: image groups (images per unit apart)
 };
 
 __device__ __forceinline__ void ldsm_x4_trans(unsigned &r0, unsigned &r1, unsigned &r2, unsigned &r3,
@@ -90,13 +90,14 @@ __device__ __forceinline__ Unit decode(const GeoM &g, int u) {
     return r;
 }
 
-// Moves a unit cursor to the next unit (same order as decode).
-__device__ __forceinline__ void advance(const GeoM &g, int N, Unit &c) {
+// Moves a unit cursor to the next unit (same order as decode); `groups` is
+// the number of image groups.
+__device__ __forceinline__ void advance(const GeoM &g, int groups, Unit &c) {
     if (++c.band == g.tiles_h) {
         c.band = 0;
         if (++c.twi == g.tiles_w) {
             c.twi = 0;
-            if (++c.group == N) {
+            if (++c.group == groups) {
                 c.group = 0;
                 ++c.ctile;
             }

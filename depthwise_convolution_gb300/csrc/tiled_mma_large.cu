@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         mbar_arrive_expect_tx(&bar, C::s_bytes);
         tma_load_4d(S, &halo_map, ld.ctile * kLCh, ld.twi * C::OTW - p.pad_w, ld.band * C::OTH - p.pad_h,
                     ld.group, &bar);
-        advance(g, p.N, ld);
+        advance(g, g.groups, ld);
     };
     if (tid == 0 && u_begin < u_end) issue();
 
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
 
     int loaded_ctile = -1;
     float bias_c = 0.f;
-    for (int u = u_begin, k = 0; u < u_end; ++u, ++k, advance(g, p.N, cur)) {
+    for (int u = u_begin, k = 0; u < u_end; ++u, ++k, advance(g, g.groups, cur)) {
         if (cur.ctile != loaded_ctile) {
             // Every warp finished reading F (previous unit) before the last
             // barrier.  Zero the table, then scatter the filter: value (fh, fw)
@@ -222,6 +222,7 @@ cudaError_t run_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     GeoM g{};
     g.tiles_h = (p.OHs + C::OTH - 1) / C::OTH;
     g.tiles_w = (p.OWs + C::OTW - 1) / C::OTW;
+    g.groups = p.N;
     const long long per = (long long)p.N * g.tiles_w * g.tiles_h;
     const long long units = per * ((p.C + kLCh - 1) / kLCh);
     if (units >= (1LL << 30)) return cudaErrorNotSupported;
