@@ -10,7 +10,8 @@ value     nominal GFLOP/s (2*N*OH*OW*C*FH*FW per pass, three passes) over the
           timed steps, inputs resident in HBM, L2 flushed between steps; summed
           over ranks (each rank runs its own batch: weak scaling, no exchange).
 e2e       the same metric with host (pinned) buffers: each step copies x, w, dy
-          to the device and y, dx, dw back, inside the timed region.
+          to the device and y, dx, dw back, inside the timed region; the
+          copies of neighbouring steps overlap the passes (three streams).
 roofline  per pass: min(compute peak, HBM bandwidth x arithmetic intensity from
           unique bytes), where the compute peak is that of the unit the pass's
           kernel runs on (reported by the library): the measured dense bf16
@@ -199,6 +200,15 @@ class Layer:
             ops.dwconv_bwd_filter(self.x, self.dy, wl.FH, wl.FW, wl.stride, wl.dilation, wl.pad, out=self.dw,
                                   workspace=self.ws, stream=stream)
 
+    def twin(self):
+        """A second set of device buffers with the same inputs (for pipelining)."""
+        t = object.__new__(Layer)
+        t.__dict__.update(self.__dict__)
+        for k in ("x", "w", "bias", "dy", "y", "dx", "dw", "ws"):
+            v = getattr(self, k)
+            setattr(t, k, None if v is None else torch.empty_like(v).copy_(v))
+        return t
+
     def unique(self, name):
         return accounting.unique_bytes(name, self.wl.dtype, *self.wl.shape_args(), bias=self.bias is not None)
 
@@ -230,28 +240,52 @@ def time_layer(layer, steps, warmup, flush):
 
 
 def time_e2e(layer, steps):
-    """Steps through host buffers: H2D of the inputs, the passes, D2H of the results."""
-    h = {}
-    for k in ("x", "w", "dy"):
-        t = getattr(layer, k)
-        if t is not None:
-            h[k] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(layer.host[k])
-    outs = {k: getattr(layer, k) for k in ("y", "dx", "dw") if getattr(layer, k) is not None}
-    ho = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in outs.items()}
-    h2d = sum(t.numel() * t.element_size() for t in h.values())
-    d2h = sum(t.numel() * t.element_size() for t in ho.values())
-    stream = torch.cuda.current_stream()
+    """Steps through host buffers, as a pipeline: every step copies its inputs
+    (x, w, dy) from pinned host memory, runs the passes and copies its results
+    (y, dx, dw) back, with the copy-in of step i+1 and the copy-out of step
+    i-1 overlapping the passes of step i (three streams, two device buffer
+    sets, events for the hand-offs).  Returns (ms per step, H2D bytes, D2H
+    bytes per step)."""
+    sets = [layer, layer.twin()]
+    names_in = [k for k in ("x", "w", "dy") if getattr(layer, k) is not None]
+    names_out = [k for k in ("y", "dx", "dw") if getattr(layer, k) is not None]
+    h_in = {k: torch.empty(getattr(layer, k).shape, dtype=getattr(layer, k).dtype, pin_memory=True).copy_(
+        layer.host[k]) for k in names_in}
+    h_out = [{k: torch.empty(getattr(layer, k).shape, dtype=getattr(layer, k).dtype, pin_memory=True)
+              for k in names_out} for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_done, run_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
-        for k, t in h.items():
-            getattr(layer, k).copy_(t, non_blocking=True)
+    start.record(s_in)
+    s_run.wait_event(start)
+    s_out.wait_event(start)
+    for i in range(steps):
+        b = i % 2
+        L = sets[b]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(run_done[b])  # the passes of step i-2 no longer read set b's inputs
+            for k in names_in:
+                getattr(L, k).copy_(h_in[k], non_blocking=True)
+            in_done[b].record(s_in)
+        s_run.wait_event(in_done[b])
+        if i >= 2:
+            s_run.wait_event(out_done[b])     # step i-2's results have left set b
         for p in layer.wl.passes:
-            layer.run_pass(p)
-        for k, t in ho.items():
-            t.copy_(outs[k], non_blocking=True)
-    end.record(stream)
+            L.run_pass(p, stream=s_run)
+        run_done[b].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(run_done[b])
+            for k in names_out:
+                h_out[b][k].copy_(getattr(L, k), non_blocking=True)
+            out_done[b].record(s_out)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_run)
+    end.record(s_out)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps, h2d, d2h
 
