@@ -124,6 +124,12 @@ cudaError_t launch_wgrad_direct(const Shape &s, dwconv_dtype dt, const void *x, 
                                 float *part, int Z, cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const float *part, int Z, long long count, float *dw,
                                 cudaStream_t st);
+// Bias gradient, first pass: part[z][c] = sum of dy over the positions of
+// slice z of the P = N*OH*OW positions (the second pass is launch_wgrad_reduce
+// with count = C).  bias_slices() is a pure function of the shape.
+int bias_slices(long long P, int C);
+cudaError_t launch_bias_slices(long long P, int C, dwconv_dtype dt, const void *dy, float *part, int Z,
+                               cudaStream_t st);
 
 // Register-tiled kernels for small filters (the whole filter of a channel pair
 // held in registers).  The sub-grid description lets one kernel serve the

@@ -175,7 +175,55 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce(const float *_
     }
 }
 
+// Bias-gradient slices: block (channel block cb, slice z) sums dy over the
+// positions of slice z for channels 32 cb + lane; warp r takes positions
+// r, r + 8, ... of the slice (in increasing order) and the 8 warp sums are
+// added in warp order, so the result does not depend on scheduling.
+template <typename T>
+__global__ void __launch_bounds__(256) bias_slice_kernel(const T *__restrict__ dy, long long P, int C, int Z,
+                                                        float *__restrict__ part) {
+    __shared__ float acc[8][32];
+    const int lane = threadIdx.x % 32, r = threadIdx.x / 32;
+    const int c = blockIdx.x * 32 + lane;
+    const int z = blockIdx.y;
+    const long long p0 = P * z / Z, p1 = P * (z + 1) / Z;
+    float sum = 0.f;
+    if (c < C)
+        for (long long q = p0 + r; q < p1; q += 8) sum += to_f32(dy[q * C + c]);
+    acc[r][lane] = sum;
+    __syncthreads();
+    if (r == 0 && c < C) {
+        float t = acc[0][lane];
+        for (int q = 1; q < 8; ++q) t += acc[q][lane];
+        part[(long long)z * C + c] = t;
+    }
+}
+
 }  // namespace
+
+int bias_slices(long long P, int C) {
+    const long long cblocks = (C + 31) / 32;
+    long long z = (4LL * 152 + cblocks - 1) / cblocks;  // about 4 blocks per SM of a GB300
+    if (z > P) z = P;
+    if (z > 4096) z = 4096;
+    return (int)(z < 1 ? 1 : z);
+}
+
+cudaError_t launch_bias_slices(long long P, int C, dwconv_dtype dt, const void *dy, float *part, int Z,
+                               cudaStream_t st) {
+    const dim3 grid((unsigned)((C + 31) / 32), (unsigned)Z);
+    switch (dt) {
+        case DWCONV_FP32: bias_slice_kernel<float><<<grid, 256, 0, st>>>((const float *)dy, P, C, Z, part); break;
+        case DWCONV_FP16: bias_slice_kernel<__half><<<grid, 256, 0, st>>>((const __half *)dy, P, C, Z, part); break;
+        case DWCONV_BF16:
+            bias_slice_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)dy, P, C, Z, part);
+            break;
+        default: return cudaErrorInvalidValue;
+    }
+    note_launches(1);
+    note_kernel("bias_slices");
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fwd_direct(const Shape &s, dwconv_dtype dt, const void *x, const void *w,
                               const void *bias, void *y, cudaStream_t st) {

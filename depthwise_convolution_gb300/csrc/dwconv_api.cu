@@ -293,4 +293,28 @@ dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int 
     return cuda_status(launch_wgrad_reduce(part, Z, (long long)FH * FW * C, dw, cs));
 }
 
+size_t dwconv_bwd_bias_workspace_size(int N, int OH, int OW, int C) {
+    if (N < 1 || OH < 1 || OW < 1 || C < 1) return 0;
+    const long long P = (long long)N * OH * OW;
+    if (P > (1LL << 40) || (long long)C * P > (1LL << 50)) return 0;
+    return (size_t)bias_slices(P, C) * (size_t)C * sizeof(float);
+}
+
+dwconv_status dwconv_bwd_bias(int N, int OH, int OW, int C, dwconv_dtype dtype, const void *dy, float *db,
+                              void *workspace, size_t workspace_bytes, dwconv_stream stream) {
+    if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
+    const size_t need = dwconv_bwd_bias_workspace_size(N, OH, OW, C);
+    if (need == 0) return DWCONV_ERR_INVALID_ARG;
+    if (dtype == DWCONV_INT8) return DWCONV_ERR_UNSUPPORTED;
+    if (!dy || !db || !workspace || workspace_bytes < need) return DWCONV_ERR_INVALID_ARG;
+    if (!aligned(dy, elem_size(dtype)) || !aligned(db, 4) || !aligned(workspace, 16)) return DWCONV_ERR_MISALIGNED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const long long P = (long long)N * OH * OW;
+    const int Z = bias_slices(P, C);
+    float *part = static_cast<float *>(workspace);
+    cudaError_t e = launch_bias_slices(P, C, dtype, dy, part, Z, cs);
+    if (e != cudaSuccess) return cuda_status(e);
+    return cuda_status(launch_wgrad_reduce(part, Z, C, db, cs));
+}
+
 }  // extern "C"

@@ -59,6 +59,17 @@ bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const u
                     const uint64_t strides[3], const uint32_t box[4], int swizzle, int l2_promotion) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
+    // The encoder is a driver-API call and needs a context current in the
+    // calling thread.  A thread whose first CUDA call is into this library
+    // (e.g. a framework's backward-pass worker thread) may have none yet:
+    // bind the current device's primary context once per thread, or every
+    // tiled kernel would refuse the call and the direct kernel would run.
+    thread_local bool context_bound = false;
+    if (!context_bound) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return false;
+        context_bound = true;
+    }
     CUtensorMapDataType t;
     switch (dt) {
         case DWCONV_FP32: t = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;

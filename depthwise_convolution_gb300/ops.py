@@ -126,6 +126,28 @@ def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, work
     return out
 
 
+def dwconv_bwd_bias_workspace_size(N, OH, OW, C) -> int:
+    return int(_lib.load().dwconv_bwd_bias_workspace_size(N, OH, OW, C))
+
+
+def dwconv_bwd_bias(dy, out=None, workspace=None, stream=None):
+    """db [C] fp32 = the sum of dy [N,OH,OW,C] over N, OH, OW."""
+    N, OH, OW, C = dy.shape
+    dt = _code(dy)
+    if out is None:
+        out = torch.empty((C,), dtype=torch.float32, device=dy.device)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (C,):
+        raise ValueError("out must be [C] float32")
+    need = dwconv_bwd_bias_workspace_size(N, OH, OW, C)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dy.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(_lib.load().dwconv_bwd_bias(
+        N, OH, OW, C, dt, _dev(dy, "dy", 4), _dev(out, "out", 1), workspace.data_ptr(), ws_bytes,
+        _stream(stream)), "dwconv_bwd_bias")
+    return out
+
+
 def dwconv_bwd_filter_static(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, stream=None):
     """dw [FH,FW,C] fp32 like dwconv_bwd_filter, for callers that cannot allocate
     scratch: the library's built-in scratch array is used instead of a workspace.

@@ -124,6 +124,25 @@ dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int 
                                 const void *dy, float *dw, void *workspace,
                                 size_t workspace_bytes, dwconv_stream stream);
 
+/*
+ * Bytes of device scratch that dwconv_bwd_bias needs (per-slice partial sums).
+ * A pure function of the arguments; 0 if they are invalid.
+ */
+size_t dwconv_bwd_bias_workspace_size(int N, int OH, int OW, int C);
+
+/*
+ * Bias gradient: db[c] = sum over (n,oh,ow) of dy[n,oh,ow,c], the adjoint of
+ * adding bias[c] once to every output (the survey's NEXT list; the paper's
+ * training passes stop at the input and weight gradients).  dy [N][OH][OW][C]
+ * in the pass's dtype, db [C] float (fully overwritten).  The N*OH*OW axis is
+ * split into slices summed in parallel, then added in a fixed order, so
+ * repeated calls give bit-identical db.  `workspace`: caller-owned device
+ * memory of at least dwconv_bwd_bias_workspace_size() bytes, 16-byte aligned.
+ * Floating dtypes only; DWCONV_INT8 returns DWCONV_ERR_UNSUPPORTED.
+ */
+dwconv_status dwconv_bwd_bias(int N, int OH, int OW, int C, dwconv_dtype dtype, const void *dy,
+                              float *db, void *workspace, size_t workspace_bytes, dwconv_stream stream);
+
 /* Bytes of device scratch built into the library for dwconv_bwd_filter_static. */
 #define DWCONV_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
 

@@ -12,6 +12,8 @@ Contents
     and int64 for integer data, threaded over channel ranges.  Each returns the
     result and the per-element magnitude ``mag`` (sum of |products| plus |bias|)
     that the parity tolerance scales with.
+``dbias``
+    The adjoint of the bias term (sum of dy over n, oh, ow), in numpy.
 ``forms``
     Independent second forms used only to pin the direct loops: the
     per-channel im2col GEMV (Flash-DWC §2.1, Fig. 1), the tiled form with
@@ -170,6 +172,22 @@ def wgrad(x, dy, FH, FW, stride=1, dilation=1, pad=0, nthreads=None):
     return dw, mag
 
 
+def dbias(dy):
+    """Bias gradient.  dy [N,OH,OW,C] -> (db [C], mag [C]).
+
+    The forward pass adds bias[c] once to every output of channel c
+    ("Tiles, halos and partial sums"), so the adjoint of the bias term is
+    the plain sum of dy over n, oh and ow: db[c] = sum dy[n,oh,ow,c];
+    mag[c] = sum |dy[n,oh,ow,c]|.  float64 or int64.
+    """
+    integer = _is_integer(dy)
+    dy = _prep(dy, integer)
+    if dy.ndim != 4:
+        raise ValueError("dy must be [N,OH,OW,C]")
+    flat = dy.reshape(-1, dy.shape[3])
+    return flat.sum(axis=0), np.abs(flat).sum(axis=0)
+
+
 from . import forms, pages  # noqa: E402  (pure-Python helpers, no C needed)
 
-__all__ = ["build", "fwd", "dgrad", "wgrad", "out_extent", "default_threads", "forms", "pages"]
+__all__ = ["build", "fwd", "dgrad", "wgrad", "dbias", "out_extent", "default_threads", "forms", "pages"]

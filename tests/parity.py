@@ -122,6 +122,17 @@ def check_dgrad(d, dtype, S, D, P, images=None, what="dgrad"):
     return compare(to64(dx[imgs]), ref, mag, dtype, dtype in ("fp16", "bf16"), what)
 
 
+def check_dbias(d, dtype, what="dbias"):
+    dy = d["dy"]
+    C = dy.shape[3]
+    g = Guarded((C,), torch.float32)
+    db = ops.dwconv_bwd_bias(dy.cuda(), out=g.t)
+    ops.dwconv_check_device_errors()
+    g.check(what)
+    ref, mag = oracle.dbias(to64(dy))
+    return compare(to64(db), ref, mag, dtype, False, what)
+
+
 def check_wgrad(d, dtype, S, D, P, what="wgrad"):
     x, dy = d["x"], d["dy"]
     FH, FW, C = d["w"].shape

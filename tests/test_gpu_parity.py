@@ -7,8 +7,8 @@ import pytest
 import torch
 
 import oracle
-from depthwise_convolution_gb300 import ops, synthetic
-from parity import (TORCH, check_dgrad, check_fwd, check_wgrad, compare, random_inputs, to64)
+from depthwise_convolution_gb300 import DwconvError, ops, synthetic
+from parity import (TORCH, check_dbias, check_dgrad, check_fwd, check_wgrad, compare, random_inputs, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +52,7 @@ def test_small_shapes_all_passes(dtype, case):
     check_fwd(d_nobias, dtype, S, D, P, what="fwd-nobias")
     check_dgrad(d, dtype, S, D, P)
     check_wgrad(d, dtype, S, D, P)
+    check_dbias(d, dtype)
 
 
 def test_int8_tail_channels_bit_exact():
@@ -96,6 +97,16 @@ def test_full_size_workloads(wl):
         check_dgrad(d, wl.dtype, wl.stride, wl.dilation, wl.pad, images=images, what=f"{wl.name} dgrad")
     if "wgrad" in wl.passes:
         check_wgrad(d, wl.dtype, wl.stride, wl.dilation, wl.pad, what=f"{wl.name} wgrad")
+        check_dbias(d, wl.dtype, what=f"{wl.name} dbias")
+
+
+def test_dbias_is_deterministic_and_rejects_int8():
+    d = random_inputs("fp16", 8, 28, 28, 96, 7, 7, 1, 1, 3, seed=6)
+    dy = d["dy"].cuda()
+    a, b = ops.dwconv_bwd_bias(dy), ops.dwconv_bwd_bias(dy)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    with pytest.raises(DwconvError):
+        ops.dwconv_bwd_bias(torch.zeros(1, 2, 2, 4, dtype=torch.int8, device="cuda"))
 
 
 def test_wgrad_is_deterministic():
@@ -149,3 +160,25 @@ def test_kernel_family_reported(dtype, case, pass_name, family):
         ops.dwconv_bwd_filter(x, dy, FH, FW, S, D, P)
     torch.cuda.synchronize()
     assert ops.dwconv_last_kernel() == family
+
+
+def test_tiled_path_from_a_fresh_thread():
+    """A thread whose first CUDA work is a library call still gets the tiled
+    kernels (tensor-map encoding needs a context bound in that thread)."""
+    import threading
+    d = random_inputs("bf16", 2, 20, 22, 64, 7, 7, 1, 1, 3, seed=4)
+    dy, w = d["dy"].cuda(), d["w"].cuda()
+    torch.cuda.synchronize()
+    seen = {}
+
+    def worker():
+        dx = ops.dwconv_bwd_data(dy, w, 20, 22, 1, 1, 3)
+        seen["kernel"] = ops.dwconv_last_kernel()
+        torch.cuda.synchronize()
+        seen["dx"] = dx
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert seen["kernel"] == "tiled_mma"
+    assert torch.equal(seen["dx"], ops.dwconv_bwd_data(dy, w, 20, 22, 1, 1, 3))

@@ -180,6 +180,28 @@ def test_p8_adjoint_identity_exact(case):
     assert lhs == int(np.sum(w * dw))
 
 
+@pytest.mark.parametrize("case", CASES[::3])
+def test_dbias_is_the_adjoint_of_the_bias_term(case):
+    """<fwd(x,w,b) - fwd(x,w,None), dy> = <b, dbias(dy)>, exactly in int64."""
+    N, H, W, C, FH, FW, S, D, P = case
+    x, w, b = rint((N, H, W, C)), rint((FH, FW, C)), rint((C,))
+    y1, _ = oracle.fwd(x, w, b, S, D, P)
+    y0, _ = oracle.fwd(x, w, None, S, D, P)
+    dy = rint(y1.shape)
+    db, mag = oracle.dbias(dy)
+    assert int(np.sum((y1 - y0) * dy)) == int(np.sum(b * db))
+    assert np.all(mag >= np.abs(db))
+
+
+def test_dbias_closed_forms():
+    dy = np.ones((3, 5, 4, 6), dtype=np.int64)
+    db, mag = oracle.dbias(dy)
+    assert np.array_equal(db, np.full(6, 60)) and np.array_equal(mag, db)
+    alt = np.ones((2, 3, 3, 2), dtype=np.int64) * np.array([1, -1])   # channel 1 negative
+    db, mag = oracle.dbias(alt)
+    assert db.tolist() == [18, -18] and mag.tolist() == [18, 18]
+
+
 @pytest.mark.parametrize("case", CASES[::2])
 def test_dgrad_gather_form_equals_scatter_form(case):
     N, H, W, C, FH, FW, S, D, P = case
