@@ -158,9 +158,12 @@ struct TiledConv {
 // Returns cudaErrorNotSupported when no tiled instance covers the request.
 cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 
-// Tensor-core (mma.sync) forward and stride-1 input gradient for 16-bit data,
-// 3x3 / 5x5 / 7x7 filters, maps more than 16 columns wide.
+// Tensor-core (mma.sync) forward and input gradient for 16-bit data, 3x3 /
+// 5x5 / 7x7 filters, maps more than 8 columns wide; with out_step > 1 it
+// writes only the (out_step, out_off) grid (zero_phases must be 0: the
+// caller zeroes the rest).  tiled_mma_supports: the shape rules, no launch.
 cudaError_t launch_tiled_mma(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
+bool tiled_mma_supports(const TiledConv &p, dwconv_dtype dt);
 // Tensor-core Toeplitz kernel for large 16-bit filters (tiled_mma_large.cu).
 cudaError_t launch_tiled_mma_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 

@@ -239,6 +239,20 @@ dwconv_status dwconv_bwd_data(int N, int H, int W, int C, int FH, int FW, int st
         p.OHf = H; p.OWf = W;
         p.OHs = (H + S - 1) / S; p.OWs = (W + S - 1) / S;
         p.out_step = S; p.out_off = ph; p.zero_phases = S > 1 ? 1 : 0;
+        if (S > 1) {
+            // Tensor-core kernel on the one live phase (its exact extent, so the
+            // TMA store stays inside dx); the other phases are zeroed first.
+            TiledConv pm = p;
+            pm.zero_phases = 0;
+            pm.OHs = (H - ph + S - 1) / S;
+            pm.OWs = (W - ph + S - 1) / S;
+            if (pm.OHs > 0 && pm.OWs > 0 && tiled_mma_supports(pm, dtype)) {
+                cudaError_t e = cudaMemsetAsync(dx, 0, (size_t)N * H * W * C * es, cs);
+                if (e != cudaSuccess) return DWCONV_ERR_CUDA;
+                e = launch_tiled_mma(pm, dtype, cs);
+                if (e != cudaErrorNotSupported) return cuda_status(e);
+            }
+        }
         cudaError_t e = launch_tiled_mma(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma_large(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_small(p, dtype, cs);

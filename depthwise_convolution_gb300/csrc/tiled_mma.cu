@@ -311,12 +311,10 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
                              (uint64_t)p.Hf * p.Wf * p.C * es};
     const uint32_t box[4] = {(uint32_t)kCh, (uint32_t)C::SW, (uint32_t)C::HRI, (uint32_t)NI};
-    const uint64_t odims[4] = {(uint64_t)p.C, (uint64_t)p.OWf, (uint64_t)p.OHf, (uint64_t)p.N};
-    const uint64_t ostr[3] = {(uint64_t)p.C * es, (uint64_t)p.OWf * p.C * es, (uint64_t)p.OHf * p.OWf * p.C * es};
     const uint32_t obox[4] = {(uint32_t)kCh, (uint32_t)C::OTW, (uint32_t)C::OTH, (uint32_t)NI};
     CUtensorMap map, omap;
     if (!encode_tmap_4d(&map, dt, base, dims, str, box, kPB) ||
-        !encode_tmap_4d(&omap, dt, p.out, odims, ostr, obox, kPB))
+        !make_out_map(&omap, p, dt, es, obox, kPB))
         return cudaErrorNotSupported;
     auto kern = tiled_mma_kernel<T, FH, FW, G, NI, KNB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem + 1024);
@@ -360,8 +358,18 @@ cudaError_t by_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
 #define DWCONV_MMA 1  // 0: leave every shape to the CUDA-core kernels
 #endif
 
+bool tiled_mma_supports(const TiledConv &p, dwconv_dtype dt) {
+    if (!DWCONV_MMA || p.zero_phases || (dt != DWCONV_FP16 && dt != DWCONV_BF16)) return false;
+    if (!((p.FH == 7 && p.FW == 7) || (p.FH == 5 && p.FW == 5) || (p.FH == 3 && p.FW == 3))) return false;
+    if (p.OWs <= 8) return false;
+    const long long per = (long long)((p.N + 1) / 2) * ((p.OWs + 63) / 8) * p.OHs;  // generous bound
+    return per * ((p.C + kCh - 1) / kCh) < (1LL << 30);
+}
+
 cudaError_t launch_tiled_mma(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    if (!DWCONV_MMA || p.zero_phases || p.out_step != 1) return cudaErrorNotSupported;
+    // Output positions off the (out_step, out_off) grid are not written: a
+    // caller with out_step > 1 zeroes them itself.
+    if (!DWCONV_MMA || p.zero_phases) return cudaErrorNotSupported;
     switch (dt) {
         case DWCONV_FP16: return by_filter<__half>(p, dt, st);
         case DWCONV_BF16: return by_filter<__nv_bfloat16>(p, dt, st);

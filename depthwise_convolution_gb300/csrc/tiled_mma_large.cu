@@ -234,11 +234,9 @@ cudaError_t run_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
                              (uint64_t)p.Hf * p.Wf * p.C * es};
     const uint32_t box[4] = {(uint32_t)kLCh, (uint32_t)C::SW, (uint32_t)C::HR, 1};
-    const uint64_t odims[4] = {(uint64_t)p.C, (uint64_t)p.OWf, (uint64_t)p.OHf, (uint64_t)p.N};
-    const uint64_t ostr[3] = {(uint64_t)p.C * es, (uint64_t)p.OWf * p.C * es, (uint64_t)p.OHf * p.OWf * p.C * es};
     const uint32_t obox[4] = {(uint32_t)kLCh, (uint32_t)C::OTW, (uint32_t)C::OTH, 1};
     CUtensorMap map, omap;
-    if (!encode_tmap_4d(&map, dt, base, dims, str, box) || !encode_tmap_4d(&omap, dt, p.out, odims, ostr, obox))
+    if (!encode_tmap_4d(&map, dt, base, dims, str, box) || !make_out_map(&omap, p, dt, es, obox, 0))
         return cudaErrorNotSupported;
     auto kern = tiled_mma_large_kernel<T, FH, NKB, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem + 1024);

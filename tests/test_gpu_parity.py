@@ -39,6 +39,8 @@ SMALL = [
     (1, 30, 45, 24, 13, 13, 1, 1, 6),    # 13x13 tensor-core path, ragged row band
     (2, 19, 20, 16, 13, 9, 1, 1, 4),     # FH != FW on the large tensor-core path
     (1, 41, 41, 16, 13, 13, 2, 2, 12),   # 13x13 on the stride-2 dilation-2 sub-grid
+    (3, 30, 28, 32, 3, 3, 2, 2, 2),      # stride-2 dgrad on a narrow phase grid (two-image tiles)
+    (2, 45, 43, 32, 7, 7, 2, 2, 5),      # stride-2 dgrad, odd sizes, phase 1
 ]
 
 
