@@ -68,11 +68,11 @@ def _load():
             L, I, P = ctypes.c_long, ctypes.c_int, ctypes.c_void_p
             for name in ("dwo_fwd_f64", "dwo_fwd_i64"):
                 fn = getattr(lib, name)
-                fn.argtypes = [L] * 9 + [P, P, P, P, P, I]
+                fn.argtypes = [L] * 12 + [P, P, P, P, P, I]
                 fn.restype = I
             for name in ("dwo_dgrad_f64", "dwo_dgrad_i64", "dwo_wgrad_f64", "dwo_wgrad_i64"):
                 fn = getattr(lib, name)
-                fn.argtypes = [L] * 9 + [P, P, P, P, I]
+                fn.argtypes = [L] * 12 + [P, P, P, P, I]
                 fn.restype = I
             lib.dwo_out_extent.argtypes = [L] * 5
             lib.dwo_out_extent.restype = L
@@ -88,6 +88,20 @@ def default_threads() -> int:
 def out_extent(X: int, F: int, S: int, D: int, P: int) -> int:
     """floor((X + 2P - D(F-1) - 1)/S) + 1, the floor convention of the oracle."""
     return int(_load().dwo_out_extent(X, F, S, D, P))
+
+
+def _pair(v, what):
+    """An int (both axes) or an (h, w) pair -> (h, w)."""
+    if isinstance(v, (tuple, list)):
+        if len(v) != 2:
+            raise ValueError(f"{what} must be an int or an (h, w) pair")
+        return int(v[0]), int(v[1])
+    return int(v), int(v)
+
+
+def _axes(stride, dilation, pad):
+    (sh, sw), (dh, dw), (ph, pw) = _pair(stride, "stride"), _pair(dilation, "dilation"), _pair(pad, "pad")
+    return sh, sw, dh, dw, ph, pw
 
 
 def _ptr(a):
@@ -109,7 +123,8 @@ def _is_integer(*arrays) -> bool:
 
 
 def fwd(x, w, bias=None, stride=1, dilation=1, pad=0, nthreads=None):
-    """Forward DWC.  x [N,H,W,C], w [FH,FW,C], bias [C] or None.
+    """Forward DWC.  x [N,H,W,C], w [FH,FW,C], bias [C] or None; stride,
+    dilation and pad each an int (both axes) or an (h, w) pair.
 
     Returns (y [N,OH,OW,C], mag [N,OH,OW,C]) in float64 or int64.
     """
@@ -120,13 +135,14 @@ def fwd(x, w, bias=None, stride=1, dilation=1, pad=0, nthreads=None):
     FH, FW, Cw = w.shape
     if Cw != C or (b is not None and b.shape != (C,)):
         raise ValueError("channel mismatch")
-    OH, OW = out_extent(H, FH, stride, dilation, pad), out_extent(W, FW, stride, dilation, pad)
+    sh, sw, dh, dw, ph, pw = _axes(stride, dilation, pad)
+    OH, OW = out_extent(H, FH, sh, dh, ph), out_extent(W, FW, sw, dw, pw)
     if OH <= 0 or OW <= 0:
         raise ValueError("empty output")
     y = np.empty((N, OH, OW, C), dtype=x.dtype)
     mag = np.empty_like(y)
     fn = _load().dwo_fwd_i64 if integer else _load().dwo_fwd_f64
-    rc = fn(N, H, W, C, FH, FW, stride, dilation, pad, _ptr(x), _ptr(w), _ptr(b), _ptr(y),
+    rc = fn(N, H, W, C, FH, FW, sh, sw, dh, dw, ph, pw, _ptr(x), _ptr(w), _ptr(b), _ptr(y),
             _ptr(mag), nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle fwd rejected the arguments (code {rc})")
@@ -134,19 +150,21 @@ def fwd(x, w, bias=None, stride=1, dilation=1, pad=0, nthreads=None):
 
 
 def dgrad(dy, w, H, W, stride=1, dilation=1, pad=0, nthreads=None):
-    """Input gradient (adjoint scatter).  dy [N,OH,OW,C] -> (dx [N,H,W,C], mag)."""
+    """Input gradient (adjoint scatter).  dy [N,OH,OW,C] -> (dx [N,H,W,C], mag).
+    stride, dilation, pad: int or (h, w) pair."""
     integer = _is_integer(dy, w)
     dy, w = _prep(dy, integer), _prep(w, integer)
     N, OH, OW, C = dy.shape
     FH, FW, Cw = w.shape
     if Cw != C:
         raise ValueError("channel mismatch")
-    if (out_extent(H, FH, stride, dilation, pad), out_extent(W, FW, stride, dilation, pad)) != (OH, OW):
+    sh, sw, dh, dw, ph, pw = _axes(stride, dilation, pad)
+    if (out_extent(H, FH, sh, dh, ph), out_extent(W, FW, sw, dw, pw)) != (OH, OW):
         raise ValueError("dy shape does not match the forward output of an H x W input")
     dx = np.empty((N, H, W, C), dtype=dy.dtype)
     mag = np.empty_like(dx)
     fn = _load().dwo_dgrad_i64 if integer else _load().dwo_dgrad_f64
-    rc = fn(N, H, W, C, FH, FW, stride, dilation, pad, _ptr(dy), _ptr(w), _ptr(dx), _ptr(mag),
+    rc = fn(N, H, W, C, FH, FW, sh, sw, dh, dw, ph, pw, _ptr(dy), _ptr(w), _ptr(dx), _ptr(mag),
             nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle dgrad rejected the arguments (code {rc})")
@@ -154,18 +172,20 @@ def dgrad(dy, w, H, W, stride=1, dilation=1, pad=0, nthreads=None):
 
 
 def wgrad(x, dy, FH, FW, stride=1, dilation=1, pad=0, nthreads=None):
-    """Weight gradient.  x [N,H,W,C], dy [N,OH,OW,C] -> (dw [FH,FW,C], mag)."""
+    """Weight gradient.  x [N,H,W,C], dy [N,OH,OW,C] -> (dw [FH,FW,C], mag).
+    stride, dilation, pad: int or (h, w) pair."""
     integer = _is_integer(x, dy)
     x, dy = _prep(x, integer), _prep(dy, integer)
     N, H, W, C = x.shape
-    if (out_extent(H, FH, stride, dilation, pad), out_extent(W, FW, stride, dilation, pad)) != dy.shape[1:3]:
+    sh, sw, dh, dw_, ph, pw = _axes(stride, dilation, pad)
+    if (out_extent(H, FH, sh, dh, ph), out_extent(W, FW, sw, dw_, pw)) != dy.shape[1:3]:
         raise ValueError("dy shape does not match the forward output")
     if dy.shape[0] != N or dy.shape[3] != C:
         raise ValueError("batch/channel mismatch")
     dw = np.empty((FH, FW, C), dtype=x.dtype)
     mag = np.empty_like(dw)
     fn = _load().dwo_wgrad_i64 if integer else _load().dwo_wgrad_f64
-    rc = fn(N, H, W, C, FH, FW, stride, dilation, pad, _ptr(x), _ptr(dy), _ptr(dw), _ptr(mag),
+    rc = fn(N, H, W, C, FH, FW, sh, sw, dh, dw_, ph, pw, _ptr(x), _ptr(dy), _ptr(dw), _ptr(mag),
             nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle wgrad rejected the arguments (code {rc})")

@@ -43,7 +43,7 @@
 /* ---- shape ------------------------------------------------------------- */
 
 typedef struct {
-    long N, H, W, C, FH, FW, S, D, P, OH, OW;
+    long N, H, W, C, FH, FW, SH, SW, DH, DW, PH, PW, OH, OW;  /* stride, dilation, padding per axis */
 } dwo_shape;
 
 static long floor_div(long a, long b) { /* b > 0 */
@@ -59,13 +59,14 @@ long dwo_out_extent(long X, long F, long S, long D, long P) {
 }
 
 static int make_shape(dwo_shape *s, long N, long H, long W, long C, long FH, long FW,
-                      long S, long D, long P) {
-    if (N <= 0 || H <= 0 || W <= 0 || C <= 0 || FH <= 0 || FW <= 0 || S <= 0 || D <= 0 || P < 0)
+                      long SH, long SW, long DH, long DW, long PH, long PW) {
+    if (N <= 0 || H <= 0 || W <= 0 || C <= 0 || FH <= 0 || FW <= 0 || SH <= 0 || SW <= 0 || DH <= 0 ||
+        DW <= 0 || PH < 0 || PW < 0)
         return -1;
     s->N = N; s->H = H; s->W = W; s->C = C; s->FH = FH; s->FW = FW;
-    s->S = S; s->D = D; s->P = P;
-    s->OH = dwo_out_extent(H, FH, S, D, P);
-    s->OW = dwo_out_extent(W, FW, S, D, P);
+    s->SH = SH; s->SW = SW; s->DH = DH; s->DW = DW; s->PH = PH; s->PW = PW;
+    s->OH = dwo_out_extent(H, FH, SH, DH, PH);
+    s->OW = dwo_out_extent(W, FW, SW, DW, PW);
     if (s->OH <= 0 || s->OW <= 0) return -2;
     return 0;
 }
@@ -107,10 +108,10 @@ static void fwd_f64(const dwo_job *j) {
                     m[c - j->c0] = dabs(b);
                 }
                 for (long fh = 0; fh < s->FH; ++fh) {
-                    long ih = oh * s->S - s->P + fh * s->D;
+                    long ih = oh * s->SH - s->PH + fh * s->DH;
                     if (ih < 0 || ih >= s->H) continue;        /* zero padding */
                     for (long fw = 0; fw < s->FW; ++fw) {
-                        long iw = ow * s->S - s->P + fw * s->D;
+                        long iw = ow * s->SW - s->PW + fw * s->DW;
                         if (iw < 0 || iw >= s->W) continue;    /* zero padding */
                         for (long c = j->c0; c < j->c1; ++c) {
                             double p = w[WIDX(s, fh, fw, c)] * x[XIDX(s, n, ih, iw, c)];
@@ -141,10 +142,10 @@ static void fwd_i64(const dwo_job *j) {
                     int64_t acc = bias ? bias[c] : 0;
                     int64_t m = iabs64(acc);
                     for (long fh = 0; fh < s->FH; ++fh) {
-                        long ih = oh * s->S - s->P + fh * s->D;
+                        long ih = oh * s->SH - s->PH + fh * s->DH;
                         if (ih < 0 || ih >= s->H) continue;
                         for (long fw = 0; fw < s->FW; ++fw) {
-                            long iw = ow * s->S - s->P + fw * s->D;
+                            long iw = ow * s->SW - s->PW + fw * s->DW;
                             if (iw < 0 || iw >= s->W) continue;
                             int64_t p = w[WIDX(s, fh, fw, c)] * x[XIDX(s, n, ih, iw, c)];
                             acc += p;
@@ -172,10 +173,10 @@ static void dgrad_f64(const dwo_job *j) {
         for (long oh = 0; oh < s->OH; ++oh)
             for (long ow = 0; ow < s->OW; ++ow)
                 for (long fh = 0; fh < s->FH; ++fh) {
-                    long ih = oh * s->S - s->P + fh * s->D;
+                    long ih = oh * s->SH - s->PH + fh * s->DH;
                     if (ih < 0 || ih >= s->H) continue;
                     for (long fw = 0; fw < s->FW; ++fw) {
-                        long iw = ow * s->S - s->P + fw * s->D;
+                        long iw = ow * s->SW - s->PW + fw * s->DW;
                         if (iw < 0 || iw >= s->W) continue;
                         for (long c = j->c0; c < j->c1; ++c) {
                             double p = w[WIDX(s, fh, fw, c)] * dy[YIDX(s, n, oh, ow, c)];
@@ -201,10 +202,10 @@ static void dgrad_i64(const dwo_job *j) {
         for (long oh = 0; oh < s->OH; ++oh)
             for (long ow = 0; ow < s->OW; ++ow)
                 for (long fh = 0; fh < s->FH; ++fh) {
-                    long ih = oh * s->S - s->P + fh * s->D;
+                    long ih = oh * s->SH - s->PH + fh * s->DH;
                     if (ih < 0 || ih >= s->H) continue;
                     for (long fw = 0; fw < s->FW; ++fw) {
-                        long iw = ow * s->S - s->P + fw * s->D;
+                        long iw = ow * s->SW - s->PW + fw * s->DW;
                         if (iw < 0 || iw >= s->W) continue;
                         for (long c = j->c0; c < j->c1; ++c) {
                             int64_t p = w[WIDX(s, fh, fw, c)] * dy[YIDX(s, n, oh, ow, c)];
@@ -230,10 +231,10 @@ static void wgrad_f64(const dwo_job *j) {
         for (long oh = 0; oh < s->OH; ++oh)
             for (long ow = 0; ow < s->OW; ++ow)
                 for (long fh = 0; fh < s->FH; ++fh) {
-                    long ih = oh * s->S - s->P + fh * s->D;
+                    long ih = oh * s->SH - s->PH + fh * s->DH;
                     if (ih < 0 || ih >= s->H) continue;
                     for (long fw = 0; fw < s->FW; ++fw) {
-                        long iw = ow * s->S - s->P + fw * s->D;
+                        long iw = ow * s->SW - s->PW + fw * s->DW;
                         if (iw < 0 || iw >= s->W) continue;
                         for (long c = j->c0; c < j->c1; ++c) {
                             double p = dy[YIDX(s, n, oh, ow, c)] * x[XIDX(s, n, ih, iw, c)];
@@ -258,10 +259,10 @@ static void wgrad_i64(const dwo_job *j) {
         for (long oh = 0; oh < s->OH; ++oh)
             for (long ow = 0; ow < s->OW; ++ow)
                 for (long fh = 0; fh < s->FH; ++fh) {
-                    long ih = oh * s->S - s->P + fh * s->D;
+                    long ih = oh * s->SH - s->PH + fh * s->DH;
                     if (ih < 0 || ih >= s->H) continue;
                     for (long fw = 0; fw < s->FW; ++fw) {
-                        long iw = ow * s->S - s->P + fw * s->D;
+                        long iw = ow * s->SW - s->PW + fw * s->DW;
                         if (iw < 0 || iw >= s->W) continue;
                         for (long c = j->c0; c < j->c1; ++c) {
                             int64_t p = dy[YIDX(s, n, oh, ow, c)] * x[XIDX(s, n, ih, iw, c)];
@@ -288,10 +289,11 @@ static void *run_job(void *arg) {
 }
 
 static int dispatch(int kind, int integer, long N, long H, long W, long C, long FH, long FW,
-                    long S, long D, long P, const void *a, const void *b, const void *bias,
+                    long SH, long SW, long DH, long DW, long PH, long PW, const void *a, const void *b,
+                    const void *bias,
                     void *out, void *mag, int nthreads) {
     dwo_shape s;
-    int rc = make_shape(&s, N, H, W, C, FH, FW, S, D, P);
+    int rc = make_shape(&s, N, H, W, C, FH, FW, SH, SW, DH, DW, PH, PW);
     if (rc != 0) return rc;
     if (!a || !b || !out) return -3;
     if (nthreads < 1) nthreads = 1;
@@ -326,34 +328,40 @@ static int dispatch(int kind, int integer, long N, long H, long W, long C, long 
 
 /* ---- exported entry points (return 0 on success, <0 on bad arguments) --- */
 
-int dwo_fwd_f64(long N, long H, long W, long C, long FH, long FW, long S, long D, long P,
+int dwo_fwd_f64(long N, long H, long W, long C, long FH, long FW, long SH, long SW, long DH,
+                long DW, long PH, long PW,
                 const double *x, const double *w, const double *bias, double *y, double *mag,
                 int nthreads) {
-    return dispatch(0, 0, N, H, W, C, FH, FW, S, D, P, x, w, bias, y, mag, nthreads);
+    return dispatch(0, 0, N, H, W, C, FH, FW, SH, SW, DH, DW, PH, PW, x, w, bias, y, mag, nthreads);
 }
 
-int dwo_fwd_i64(long N, long H, long W, long C, long FH, long FW, long S, long D, long P,
+int dwo_fwd_i64(long N, long H, long W, long C, long FH, long FW, long SH, long SW, long DH,
+                long DW, long PH, long PW,
                 const int64_t *x, const int64_t *w, const int64_t *bias, int64_t *y,
                 int64_t *mag, int nthreads) {
-    return dispatch(0, 1, N, H, W, C, FH, FW, S, D, P, x, w, bias, y, mag, nthreads);
+    return dispatch(0, 1, N, H, W, C, FH, FW, SH, SW, DH, DW, PH, PW, x, w, bias, y, mag, nthreads);
 }
 
-int dwo_dgrad_f64(long N, long H, long W, long C, long FH, long FW, long S, long D, long P,
+int dwo_dgrad_f64(long N, long H, long W, long C, long FH, long FW, long SH, long SW, long DH,
+                long DW, long PH, long PW,
                   const double *dy, const double *w, double *dx, double *mag, int nthreads) {
-    return dispatch(1, 0, N, H, W, C, FH, FW, S, D, P, dy, w, NULL, dx, mag, nthreads);
+    return dispatch(1, 0, N, H, W, C, FH, FW, SH, SW, DH, DW, PH, PW, dy, w, NULL, dx, mag, nthreads);
 }
 
-int dwo_dgrad_i64(long N, long H, long W, long C, long FH, long FW, long S, long D, long P,
+int dwo_dgrad_i64(long N, long H, long W, long C, long FH, long FW, long SH, long SW, long DH,
+                long DW, long PH, long PW,
                   const int64_t *dy, const int64_t *w, int64_t *dx, int64_t *mag, int nthreads) {
-    return dispatch(1, 1, N, H, W, C, FH, FW, S, D, P, dy, w, NULL, dx, mag, nthreads);
+    return dispatch(1, 1, N, H, W, C, FH, FW, SH, SW, DH, DW, PH, PW, dy, w, NULL, dx, mag, nthreads);
 }
 
-int dwo_wgrad_f64(long N, long H, long W, long C, long FH, long FW, long S, long D, long P,
+int dwo_wgrad_f64(long N, long H, long W, long C, long FH, long FW, long SH, long SW, long DH,
+                long DW, long PH, long PW,
                   const double *x, const double *dy, double *dw, double *mag, int nthreads) {
-    return dispatch(2, 0, N, H, W, C, FH, FW, S, D, P, x, dy, NULL, dw, mag, nthreads);
+    return dispatch(2, 0, N, H, W, C, FH, FW, SH, SW, DH, DW, PH, PW, x, dy, NULL, dw, mag, nthreads);
 }
 
-int dwo_wgrad_i64(long N, long H, long W, long C, long FH, long FW, long S, long D, long P,
+int dwo_wgrad_i64(long N, long H, long W, long C, long FH, long FW, long SH, long SW, long DH,
+                long DW, long PH, long PW,
                   const int64_t *x, const int64_t *dy, int64_t *dw, int64_t *mag, int nthreads) {
-    return dispatch(2, 1, N, H, W, C, FH, FW, S, D, P, x, dy, NULL, dw, mag, nthreads);
+    return dispatch(2, 1, N, H, W, C, FH, FW, SH, SW, DH, DW, PH, PW, x, dy, NULL, dw, mag, nthreads);
 }

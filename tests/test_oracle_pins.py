@@ -353,3 +353,58 @@ def test_oracle_rejects_bad_shapes():
         oracle.fwd(np.zeros((1, 2, 2, 1)), np.zeros((5, 5, 1)), None, 1, 1, 0)
     with pytest.raises(ValueError):
         oracle.fwd(np.zeros((1, 4, 4, 2)), np.zeros((3, 3, 3)), None, 1, 1, 1)
+
+
+# ------------------------------------------------- per-axis stride/dilation/pad
+
+AXIS_CASES = [  # (N, H, W, C, FH, FW, (sh, sw), (dh, dw), (ph, pw))
+    (2, 7, 9, 3, 3, 2, (1, 2), (2, 1), (2, 0)),
+    (1, 6, 11, 2, 1, 5, (2, 1), (1, 2), (0, 4)),
+    (2, 9, 5, 3, 4, 1, (3, 1), (1, 1), (1, 0)),
+    (1, 8, 8, 2, 2, 3, (2, 3), (3, 1), (1, 2)),
+]
+
+
+@pytest.mark.parametrize("case", AXIS_CASES)
+def test_axes_swap_with_the_transpose(case):
+    """Swapping H and W swaps the per-axis parameters: exact in int64 for all three passes."""
+    N, H, W, C, FH, FW, S, D, P = case
+    x, w, b = rint((N, H, W, C)), rint((FH, FW, C)), rint((C,))
+    sw_ = lambda t: (t[1], t[0])  # noqa: E731
+    xt, wt = x.transpose(0, 2, 1, 3), w.transpose(1, 0, 2)
+    y, _ = oracle.fwd(x, w, b, S, D, P)
+    yt, _ = oracle.fwd(xt, wt, b, sw_(S), sw_(D), sw_(P))
+    assert np.array_equal(y, yt.transpose(0, 2, 1, 3))
+    dy = rint(y.shape)
+    dx, _ = oracle.dgrad(dy, w, H, W, S, D, P)
+    dxt, _ = oracle.dgrad(dy.transpose(0, 2, 1, 3), wt, W, H, sw_(S), sw_(D), sw_(P))
+    assert np.array_equal(dx, dxt.transpose(0, 2, 1, 3))
+    dw, _ = oracle.wgrad(x, dy, FH, FW, S, D, P)
+    dwt, _ = oracle.wgrad(xt, dy.transpose(0, 2, 1, 3), FW, FH, sw_(S), sw_(D), sw_(P))
+    assert np.array_equal(dw, dwt.transpose(1, 0, 2))
+
+
+@pytest.mark.parametrize("case", AXIS_CASES)
+def test_axes_adjoint_identity_exact(case):
+    N, H, W, C, FH, FW, S, D, P = case
+    x, w = rint((N, H, W, C)), rint((FH, FW, C))
+    y, _ = oracle.fwd(x, w, None, S, D, P)
+    dy = rint(y.shape)
+    dx, _ = oracle.dgrad(dy, w, H, W, S, D, P)
+    dw, _ = oracle.wgrad(x, dy, FH, FW, S, D, P)
+    lhs = int(np.sum(y * dy))
+    assert lhs == int(np.sum(x * dx)) == int(np.sum(w * dw))
+
+
+def test_strip_filter_is_a_1d_convolution_per_row():
+    """A 1 x K filter with pad (0, K//2), row stride 2: every output row is the
+    zero-padded 1-D convolution ("Outline of Programming Massively Parallel
+    Processors", Convolution) of every other input row."""
+    K = 5
+    x, w = rint((2, 6, 10, 3)), rint((1, K, 3))
+    y, _ = oracle.fwd(x, w, None, (2, 1), 1, (0, K // 2))
+    assert y.shape == (2, 3, 10, 3)
+    for n in range(2):
+        for oh in range(3):
+            for c in range(3):
+                assert y[n, oh, :, c].tolist() == forms.conv1d_zero_pad(x[n, 2 * oh, :, c], w[0, :, c])
