@@ -30,6 +30,11 @@ SIGNATURES = {
     "dwconv_status_string": (ctypes.c_char_p, [_I]),
     "dwconv_bwd_bias_workspace_size": (ctypes.c_size_t, [_I] * 4),
     "dwconv_bwd_bias": (_I, [_I] * 4 + [_I, _P, _P, _P, ctypes.c_size_t, _P]),
+    "dwconv_output_size_2d": (_I, [_I] * 10 + [ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "dwconv_fwd_2d": (_I, [_I] * 12 + [_I, _P, _P, _P, _P, _P]),
+    "dwconv_bwd_data_2d": (_I, [_I] * 12 + [_I, _P, _P, _P, _P]),
+    "dwconv_bwd_filter_workspace_size_2d": (_SZ, [_I] * 12 + [_I]),
+    "dwconv_bwd_filter_2d": (_I, [_I] * 12 + [_I, _P, _P, _P, _P, _SZ, _P]),
     "dwconv_launch_count": (ctypes.c_ulonglong, []),
     "dwconv_last_kernel": (ctypes.c_char_p, []),
 }

@@ -13,7 +13,9 @@ namespace dwc {
 // Problem geometry after validation.  H, W, C are input sizes; OH, OW the
 // forward output sizes (floor convention).
 struct Shape {
-    int N, H, W, C, FH, FW, S, D, P, OH, OW;
+    int N, H, W, C, FH, FW;
+    int SH, SW, DH, DW, PH, PW;  // stride, dilation, padding per axis
+    int OH, OW;
 };
 
 // Counts kernel launches for dwconv_launch_count().
@@ -145,22 +147,22 @@ struct TiledConv {
     int FH, FW;
     int flip;              // 1: filter rotated by 180 degrees
     // Input tensor [N][Hf][Wf][C]; taps read its sub-grid
-    //   (in_off + in_step*i, in_off + in_step*j), 0 <= i < Hs, 0 <= j < Ws.
-    int Hf, Wf, Hs, Ws, in_step, in_off;
+    //   (in_off_h + in_step_h*i, in_off_w + in_step_w*j), 0 <= i < Hs, 0 <= j < Ws.
+    int Hf, Wf, Hs, Ws, in_step_h, in_step_w, in_off_h, in_off_w;
     int pad_h, pad_w;      // sub-grid input row of output row i, tap fh: i - pad_h + fh (cols alike)
     // Output tensor [N][OHf][OWf][C]; computed element (i, j) of the OHs x OWs
-    // grid goes to (out_off + out_step*i, out_off + out_step*j).  With
-    // zero_phases, the other positions of each out_step x out_step block are
-    // written with zeros.
-    int OHf, OWf, OHs, OWs, out_step, out_off, zero_phases;
+    // grid goes to (out_off_h + out_step_h*i, out_off_w + out_step_w*j).  With
+    // zero_phases, the other positions of each out_step_h x out_step_w block
+    // are written with zeros.
+    int OHf, OWf, OHs, OWs, out_step_h, out_step_w, out_off_h, out_off_w, zero_phases;
 };
 
 // Returns cudaErrorNotSupported when no tiled instance covers the request.
 cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 
 // Tensor-core (mma.sync) forward and input gradient for 16-bit data, 3x3 /
-// 5x5 / 7x7 filters, maps more than 8 columns wide; with out_step > 1 it
-// writes only the (out_step, out_off) grid (zero_phases must be 0: the
+// 5x5 / 7x7 filters, maps more than 8 columns wide; with an output step > 1
+// it writes only the (out_step, out_off) grid (zero_phases must be 0: the
 // caller zeroes the rest).  tiled_mma_supports: the shape rules, no launch.
 cudaError_t launch_tiled_mma(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 bool tiled_mma_supports(const TiledConv &p, dwconv_dtype dt);

@@ -34,12 +34,12 @@ __global__ void __launch_bounds__(kThreads) fwd_direct_fp(Shape s, const T *__re
         long long n = t / s.OH;
         float acc = bias ? bias[c] : 0.f;
         for (int fh = 0; fh < s.FH; ++fh) {
-            int ih = oh * s.S - s.P + fh * s.D;
+            int ih = oh * s.SH - s.PH + fh * s.DH;
             if (ih < 0 || ih >= s.H) continue;
             const T *xrow = x + ((n * s.H + ih) * s.W) * (long long)s.C + c;
             const T *wrow = w + (long long)fh * s.FW * s.C + c;
             for (int fw = 0; fw < s.FW; ++fw) {
-                int iw = ow * s.S - s.P + fw * s.D;
+                int iw = ow * s.SW - s.PW + fw * s.DW;
                 if (iw < 0 || iw >= s.W) continue;
                 acc = fmaf(to_f32(wrow[(long long)fw * s.C]), to_f32(xrow[(long long)iw * s.C]), acc);
             }
@@ -66,10 +66,10 @@ __global__ void __launch_bounds__(kThreads) fwd_direct_i8(Shape s, const int8_t 
         long long n = t / s.OH;
         uint32_t acc = bias ? (uint32_t)bias[c] : 0u;
         for (int fh = 0; fh < s.FH; ++fh) {
-            int ih = oh * s.S - s.P + fh * s.D;
+            int ih = oh * s.SH - s.PH + fh * s.DH;
             if (ih < 0 || ih >= s.H) continue;
             for (int fw = 0; fw < s.FW; ++fw) {
-                int iw = ow * s.S - s.P + fw * s.D;
+                int iw = ow * s.SW - s.PW + fw * s.DW;
                 if (iw < 0 || iw >= s.W) continue;
                 int prod = (int)w[((long long)fh * s.FW + fw) * s.C + c] *
                            (int)x[((n * s.H + ih) * s.W + iw) * (long long)s.C + c];
@@ -96,16 +96,16 @@ __global__ void __launch_bounds__(kThreads) dgrad_direct(Shape s, const T *__res
         long long n = t / s.H;
         float acc = 0.f;
         for (int fh = 0; fh < s.FH; ++fh) {
-            int th = ih + s.P - fh * s.D;
+            int th = ih + s.PH - fh * s.DH;
             if (th < 0) break;                  // decreases with fh
-            if (th % s.S != 0) continue;
-            int oh = th / s.S;
+            if (th % s.SH != 0) continue;
+            int oh = th / s.SH;
             if (oh >= s.OH) continue;
             for (int fw = 0; fw < s.FW; ++fw) {
-                int tw = iw + s.P - fw * s.D;
+                int tw = iw + s.PW - fw * s.DW;
                 if (tw < 0) break;
-                if (tw % s.S != 0) continue;
-                int ow = tw / s.S;
+                if (tw % s.SW != 0) continue;
+                int ow = tw / s.SW;
                 if (ow >= s.OW) continue;
                 acc = fmaf(to_f32(w[((long long)fh * s.FW + fw) * s.C + c]),
                            to_f32(dy[((n * s.OH + oh) * s.OW + ow) * (long long)s.C + c]), acc);
@@ -136,8 +136,8 @@ __global__ void __launch_bounds__(kThreads) wgrad_direct(Shape s, const T *__res
             long long t = p / s.OW;
             int oh = (int)(t % s.OH);
             long long n = t / s.OH;
-            int ih = oh * s.S - s.P + fh * s.D;
-            int iw = ow * s.S - s.P + fw * s.D;
+            int ih = oh * s.SH - s.PH + fh * s.DH;
+            int iw = ow * s.SW - s.PW + fw * s.DW;
             if (ih < 0 || ih >= s.H || iw < 0 || iw >= s.W) continue;
             acc = fmaf(to_f32(dy[p * s.C + c]),
                        to_f32(x[((n * s.H + ih) * s.W + iw) * (long long)s.C + c]), acc);

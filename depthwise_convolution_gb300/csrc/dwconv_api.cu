@@ -58,16 +58,18 @@ int gcd(int a, int b) {
 
 // Validates sizes and fills the shape (OH, OW >= 1).  Elements per tensor are
 // bounded so that every offset fits comfortably in 64-bit arithmetic.
-dwconv_status make_shape(int N, int H, int W, int C, int FH, int FW, int S, int D, int P, Shape &s) {
-    if (N <= 0 || H <= 0 || W <= 0 || C <= 0 || FH <= 0 || FW <= 0 || S <= 0 || D <= 0 || P < 0)
+dwconv_status make_shape(int N, int H, int W, int C, int FH, int FW, int SH, int SW, int DH, int DW, int PH,
+                         int PW, Shape &s) {
+    if (N <= 0 || H <= 0 || W <= 0 || C <= 0 || FH <= 0 || FW <= 0 || SH <= 0 || SW <= 0 || DH <= 0 ||
+        DW <= 0 || PH < 0 || PW < 0)
         return DWCONV_ERR_INVALID_ARG;
-    const long long OH = out_extent(H, FH, S, D, P), OW = out_extent(W, FW, S, D, P);
+    const long long OH = out_extent(H, FH, SH, DH, PH), OW = out_extent(W, FW, SW, DW, PW);
     if (OH < 1 || OW < 1 || OH > INT_MAX || OW > INT_MAX) return DWCONV_ERR_INVALID_ARG;
     const long long limit = 1LL << 40;
     if ((long long)N * H * W > limit / C || (long long)N * OH * OW > limit / C ||
         (long long)FH * FW > limit / C)
         return DWCONV_ERR_INVALID_ARG;
-    s = Shape{N, H, W, C, FH, FW, S, D, P, (int)OH, (int)OW};
+    s = Shape{N, H, W, C, FH, FW, SH, SW, DH, DW, PH, PW, (int)OH, (int)OW};
     return DWCONV_OK;
 }
 
@@ -94,6 +96,24 @@ bool tiled_layout_ok(const Shape &s, dwconv_dtype dt, const void *in, const void
     return aligned(in, 16) && aligned(out, 2 * es) && aligned(w, 2 * es);
 }
 
+// Taps read the input rows oh*SH - PH + fh*DH.  With g = gcd(SH, DH) they all
+// lie in one residue class r0 = (-PH) mod g, so along H the pass is a stride
+// SH/g, dilation DH/g convolution over that sub-grid (columns alike).  When
+// both axes have unit stride and dilation on their sub-grids, fills the input
+// side of p (the sub-grid and its padding) and returns true.  This covers the
+// stride-2 dilation-2 layer, which reads only even rows and columns.
+bool unit_subgrid(const Shape &s, TiledConv &p) {
+    const int gh = gcd(s.SH, s.DH), gw = gcd(s.SW, s.DW);
+    const int rh = (gh - s.PH % gh) % gh, rw = (gw - s.PW % gw) % gw;
+    if (s.SH / gh != 1 || s.DH / gh != 1 || s.SW / gw != 1 || s.DW / gw != 1 || s.H <= rh || s.W <= rw)
+        return false;
+    p.Hf = s.H; p.Wf = s.W;
+    p.in_step_h = gh; p.in_step_w = gw; p.in_off_h = rh; p.in_off_w = rw;
+    p.Hs = (s.H - rh + gh - 1) / gh; p.Ws = (s.W - rw + gw - 1) / gw;
+    p.pad_h = (s.PH + rh) / gh; p.pad_w = (s.PW + rw) / gw;
+    return true;
+}
+
 // wgrad split: slices of the N*OH*OW axis.  A pure function of the shape so
 // that the workspace size can be computed without a device.
 int wgrad_slices(const Shape &s) {
@@ -115,17 +135,12 @@ int wgrad_slices(const Shape &s) {
 bool wgrad_tiled_params(const Shape &s, dwconv_dtype dt, const void *x, const void *dy, float *dw,
                         TiledConv &p) {
     if (dt == DWCONV_INT8 || (s.C * elem_size(dt)) % 16 != 0) return false;
-    const int g = gcd(s.S, s.D);
-    const int r0 = (g - s.P % g) % g;
-    if (s.S / g != 1 || s.D / g != 1 || s.H <= r0 || s.W <= r0) return false;
     p = TiledConv{};
+    if (!unit_subgrid(s, p)) return false;
     p.in = x; p.w = nullptr; p.bias = nullptr; p.out = dw; p.dy = dy;
     p.N = s.N; p.C = s.C; p.FH = s.FH; p.FW = s.FW; p.flip = 0;
-    p.Hf = s.H; p.Wf = s.W; p.in_step = g; p.in_off = r0;
-    p.Hs = (s.H - r0 + g - 1) / g; p.Ws = (s.W - r0 + g - 1) / g;
-    p.pad_h = p.pad_w = (s.P + r0) / g;
     p.OHf = s.OH; p.OWf = s.OW; p.OHs = s.OH; p.OWs = s.OW;
-    p.out_step = 1; p.out_off = 0; p.zero_phases = 0;
+    p.out_step_h = p.out_step_w = 1; p.out_off_h = p.out_off_w = 0; p.zero_phases = 0;
     return tiled_wgrad_slices(p, dt) > 0;
 }
 
@@ -136,14 +151,19 @@ using namespace dwc;
 
 extern "C" {
 
-dwconv_status dwconv_output_size(int H, int W, int FH, int FW, int stride, int dilation, int pad,
-                                 int *OH, int *OW) {
+dwconv_status dwconv_output_size_2d(int H, int W, int FH, int FW, int stride_h, int stride_w, int dilation_h,
+                                    int dilation_w, int pad_h, int pad_w, int *OH, int *OW) {
     Shape s;
-    dwconv_status st = make_shape(1, H, W, 1, FH, FW, stride, dilation, pad, s);
+    dwconv_status st = make_shape(1, H, W, 1, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s);
     if (st != DWCONV_OK) return st;
     if (OH) *OH = s.OH;
     if (OW) *OW = s.OW;
     return DWCONV_OK;
+}
+
+dwconv_status dwconv_output_size(int H, int W, int FH, int FW, int stride, int dilation, int pad, int *OH,
+                                 int *OW) {
+    return dwconv_output_size_2d(H, W, FH, FW, stride, stride, dilation, dilation, pad, pad, OH, OW);
 }
 
 const char *dwconv_status_string(dwconv_status status) {
@@ -168,12 +188,13 @@ dwconv_status dwconv_check_device_errors(dwconv_stream stream) {
     return v ? DWCONV_ERR_TIMEOUT : DWCONV_OK;
 }
 
-dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride, int dilation,
-                         int pad, dwconv_dtype dtype, const void *x, const void *w,
-                         const void *bias, void *y, dwconv_stream stream) {
+dwconv_status dwconv_fwd_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                            int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype, const void *x,
+                            const void *w, const void *bias, void *y, dwconv_stream stream) {
     if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
     Shape s;
-    dwconv_status st = make_shape(N, H, W, C, FH, FW, stride, dilation, pad, s);
+    dwconv_status st =
+        make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s);
     if (st != DWCONV_OK) return st;
     if (!x || !w || !y) return DWCONV_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
@@ -183,22 +204,14 @@ dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride,
         return DWCONV_ERR_MISALIGNED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
 
-    // Taps read the input rows oh*S - P + fh*D.  With g = gcd(S, D) they all lie
-    // in one residue class r0 = (-P) mod g, so the pass is a stride S/g,
-    // dilation D/g convolution over that sub-grid.  Unit stride and dilation
-    // on the sub-grid go to the tiled kernel (this covers the stride-2,
-    // dilation-2 layer, which reads only even rows and columns).
-    const int g = gcd(stride, dilation);
-    const int r0 = (int)((g - pad % g) % g);
-    if (stride / g == 1 && dilation / g == 1 && tiled_layout_ok(s, dtype, x, y, w) && H > r0 && W > r0) {
-        TiledConv p{};
+    // Unit stride and dilation on the taps' sub-grid (unit_subgrid) go to the
+    // tiled kernels.
+    TiledConv p{};
+    if (tiled_layout_ok(s, dtype, x, y, w) && unit_subgrid(s, p)) {
         p.in = x; p.w = w; p.bias = static_cast<const float *>(bias); p.out = y;
         p.N = N; p.C = C; p.FH = FH; p.FW = FW; p.flip = 0;
-        p.Hf = H; p.Wf = W; p.in_step = g; p.in_off = r0;
-        p.Hs = (H - r0 + g - 1) / g; p.Ws = (W - r0 + g - 1) / g;
-        p.pad_h = p.pad_w = (pad + r0) / g;
         p.OHf = s.OH; p.OWf = s.OW; p.OHs = s.OH; p.OWs = s.OW;
-        p.out_step = 1; p.out_off = 0; p.zero_phases = 0;
+        p.out_step_h = p.out_step_w = 1; p.out_off_h = p.out_off_w = 0; p.zero_phases = 0;
         cudaError_t e = launch_tiled_mma(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma_large(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_small(p, dtype, cs);
@@ -208,12 +221,20 @@ dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride,
     return cuda_status(launch_fwd_direct(s, dtype, x, w, bias, y, cs));
 }
 
-dwconv_status dwconv_bwd_data(int N, int H, int W, int C, int FH, int FW, int stride,
-                              int dilation, int pad, dwconv_dtype dtype, const void *dy,
-                              const void *w, void *dx, dwconv_stream stream) {
+dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride, int dilation, int pad,
+                         dwconv_dtype dtype, const void *x, const void *w, const void *bias, void *y,
+                         dwconv_stream stream) {
+    return dwconv_fwd_2d(N, H, W, C, FH, FW, stride, stride, dilation, dilation, pad, pad, dtype, x, w, bias, y,
+                         stream);
+}
+
+dwconv_status dwconv_bwd_data_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                                 int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                                 const void *dy, const void *w, void *dx, dwconv_stream stream) {
     if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
     Shape s;
-    dwconv_status st = make_shape(N, H, W, C, FH, FW, stride, dilation, pad, s);
+    dwconv_status st =
+        make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s);
     if (st != DWCONV_OK) return st;
     if (dtype == DWCONV_INT8) return DWCONV_ERR_UNSUPPORTED;
     if (!dy || !w || !dx) return DWCONV_ERR_INVALID_ARG;
@@ -221,31 +242,34 @@ dwconv_status dwconv_bwd_data(int N, int H, int W, int C, int FH, int FW, int st
     if (!aligned(dy, es) || !aligned(w, es) || !aligned(dx, es)) return DWCONV_ERR_MISALIGNED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
 
-    // When S divides D, every tap of input row ih satisfies ih = S*i + ph with
-    // ph = (-P) mod S, and dx on that phase is a unit-stride convolution of dy
-    // with the filter rotated by 180 degrees (Flash-DWC §5.1, generalised from
-    // S = 1), dilation D/S and padding (FH-1)*D/S - (ph+P)/S; every other
-    // phase receives no tap and is written as zero.
-    if (dilation % stride == 0 && dilation / stride == 1 && tiled_layout_ok(s, dtype, dy, dx, w)) {
-        const int S = stride;
-        const int ph = (S - pad % S) % S;
-        const int q = (ph + pad) / S;
+    // When S divides D (per axis), every tap of input row ih satisfies
+    // ih = S*i + ph with ph = (-P) mod S, and dx on that phase is a unit-stride
+    // convolution of dy with the filter rotated by 180 degrees (Flash-DWC §5.1,
+    // generalised from S = 1), dilation D/S and padding (F-1)*D/S - (ph+P)/S;
+    // every other phase receives no tap and is written as zero.
+    const int SH = stride_h, SW = stride_w;
+    if (dilation_h % SH == 0 && dilation_h / SH == 1 && dilation_w % SW == 0 && dilation_w / SW == 1 &&
+        tiled_layout_ok(s, dtype, dy, dx, w)) {
+        const int phh = (SH - pad_h % SH) % SH, phw = (SW - pad_w % SW) % SW;
+        const int qh = (phh + pad_h) / SH, qw = (phw + pad_w) / SW;
         TiledConv p{};
         p.in = dy; p.w = w; p.bias = nullptr; p.out = dx;
         p.N = N; p.C = C; p.FH = FH; p.FW = FW; p.flip = 1;
-        p.Hf = s.OH; p.Wf = s.OW; p.Hs = s.OH; p.Ws = s.OW; p.in_step = 1; p.in_off = 0;
-        p.pad_h = (FH - 1) * (dilation / S) - q;
-        p.pad_w = (FW - 1) * (dilation / S) - q;
+        p.Hf = s.OH; p.Wf = s.OW; p.Hs = s.OH; p.Ws = s.OW;
+        p.in_step_h = p.in_step_w = 1; p.in_off_h = p.in_off_w = 0;
+        p.pad_h = (FH - 1) * (dilation_h / SH) - qh;
+        p.pad_w = (FW - 1) * (dilation_w / SW) - qw;
         p.OHf = H; p.OWf = W;
-        p.OHs = (H + S - 1) / S; p.OWs = (W + S - 1) / S;
-        p.out_step = S; p.out_off = ph; p.zero_phases = S > 1 ? 1 : 0;
-        if (S > 1) {
+        p.OHs = (H + SH - 1) / SH; p.OWs = (W + SW - 1) / SW;
+        p.out_step_h = SH; p.out_step_w = SW; p.out_off_h = phh; p.out_off_w = phw;
+        p.zero_phases = (SH > 1 || SW > 1) ? 1 : 0;
+        if (p.zero_phases) {
             // Tensor-core kernel on the one live phase (its exact extent, so the
             // TMA store stays inside dx); the other phases are zeroed first.
             TiledConv pm = p;
             pm.zero_phases = 0;
-            pm.OHs = (H - ph + S - 1) / S;
-            pm.OWs = (W - ph + S - 1) / S;
+            pm.OHs = (H - phh + SH - 1) / SH;
+            pm.OWs = (W - phw + SW - 1) / SW;
             if (pm.OHs > 0 && pm.OWs > 0 && tiled_mma_supports(pm, dtype)) {
                 cudaError_t e = cudaMemsetAsync(dx, 0, (size_t)N * H * W * C * es, cs);
                 if (e != cudaSuccess) return DWCONV_ERR_CUDA;
@@ -262,11 +286,19 @@ dwconv_status dwconv_bwd_data(int N, int H, int W, int C, int FH, int FW, int st
     return cuda_status(launch_dgrad_direct(s, dtype, dy, w, dx, cs));
 }
 
-size_t dwconv_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW, int stride,
-                                        int dilation, int pad, dwconv_dtype dtype) {
+dwconv_status dwconv_bwd_data(int N, int H, int W, int C, int FH, int FW, int stride, int dilation, int pad,
+                              dwconv_dtype dtype, const void *dy, const void *w, void *dx, dwconv_stream stream) {
+    return dwconv_bwd_data_2d(N, H, W, C, FH, FW, stride, stride, dilation, dilation, pad, pad, dtype, dy, w, dx,
+                              stream);
+}
+
+size_t dwconv_bwd_filter_workspace_size_2d(int N, int H, int W, int C, int FH, int FW, int stride_h,
+                                           int stride_w, int dilation_h, int dilation_w, int pad_h, int pad_w,
+                                           dwconv_dtype dtype) {
     Shape s;
     if (!valid_dtype(dtype) || dtype == DWCONV_INT8) return 0;
-    if (make_shape(N, H, W, C, FH, FW, stride, dilation, pad, s) != DWCONV_OK) return 0;
+    if (make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s) != DWCONV_OK)
+        return 0;
     const size_t per_slice = (size_t)FH * FW * C * sizeof(float);
     size_t need = (size_t)wgrad_slices(s) * per_slice;
     TiledConv p;
@@ -277,20 +309,27 @@ size_t dwconv_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int 
     return need;
 }
 
-dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int stride,
-                                int dilation, int pad, dwconv_dtype dtype, const void *x,
-                                const void *dy, float *dw, void *workspace,
-                                size_t workspace_bytes, dwconv_stream stream) {
+size_t dwconv_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW, int stride, int dilation,
+                                        int pad, dwconv_dtype dtype) {
+    return dwconv_bwd_filter_workspace_size_2d(N, H, W, C, FH, FW, stride, stride, dilation, dilation, pad, pad,
+                                               dtype);
+}
+
+dwconv_status dwconv_bwd_filter_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                                   int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                                   const void *x, const void *dy, float *dw, void *workspace,
+                                   size_t workspace_bytes, dwconv_stream stream) {
     if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
     Shape s;
-    dwconv_status st = make_shape(N, H, W, C, FH, FW, stride, dilation, pad, s);
+    dwconv_status st =
+        make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s);
     if (st != DWCONV_OK) return st;
     if (dtype == DWCONV_INT8) return DWCONV_ERR_UNSUPPORTED;
     if (!x || !dy || !dw) return DWCONV_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     if (!aligned(x, es) || !aligned(dy, es) || !aligned(dw, 4)) return DWCONV_ERR_MISALIGNED;
-    const size_t need = dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation, pad,
-                                                         dtype);
+    const size_t need = dwconv_bwd_filter_workspace_size_2d(N, H, W, C, FH, FW, stride_h, stride_w,
+                                                            dilation_h, dilation_w, pad_h, pad_w, dtype);
     if (workspace_bytes < need || (need > 0 && !workspace)) return DWCONV_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return DWCONV_ERR_MISALIGNED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -305,6 +344,13 @@ dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int 
     cudaError_t e = launch_wgrad_direct(s, dtype, x, dy, part, Z, cs);
     if (e != cudaSuccess) return DWCONV_ERR_CUDA;
     return cuda_status(launch_wgrad_reduce(part, Z, (long long)FH * FW * C, dw, cs));
+}
+
+dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int stride, int dilation, int pad,
+                                dwconv_dtype dtype, const void *x, const void *dy, float *dw, void *workspace,
+                                size_t workspace_bytes, dwconv_stream stream) {
+    return dwconv_bwd_filter_2d(N, H, W, C, FH, FW, stride, stride, dilation, dilation, pad, pad, dtype, x, dy, dw,
+                                workspace, workspace_bytes, stream);
 }
 
 size_t dwconv_bwd_bias_workspace_size(int N, int OH, int OW, int C) {

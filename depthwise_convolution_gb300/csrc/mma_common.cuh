@@ -111,14 +111,14 @@ constexpr int channel_stride(int n) { return n % 16 == 8 ? n : n + ((8 - n % 16 
 
 constexpr unsigned align1k(unsigned b) { return (b + 1023u) & ~1023u; }
 
-// Tensor map of the kernel's output grid: positions (out_off + out_step i,
-// out_off + out_step j) of the [N][OHf][OWf][C] tensor p.out, i < OHs,
-// j < OWs (the step folded into the strides, the offset into the base).
+// Tensor map of the kernel's output grid: positions (out_off_h + out_step_h i,
+// out_off_w + out_step_w j) of the [N][OHf][OWf][C] tensor p.out, i < OHs,
+// j < OWs (the steps folded into the strides, the offsets into the base).
 inline bool make_out_map(CUtensorMap *m, const TiledConv &p, dwconv_dtype dt, size_t es, const uint32_t box[4],
                          int swizzle) {
-    const char *base = static_cast<const char *>(p.out) + ((size_t)p.out_off * p.OWf + p.out_off) * p.C * es;
+    const char *base = static_cast<const char *>(p.out) + ((size_t)p.out_off_h * p.OWf + p.out_off_w) * p.C * es;
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.OWs, (uint64_t)p.OHs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.out_step * p.C * es, (uint64_t)p.out_step * p.OWf * p.C * es,
+    const uint64_t str[3] = {(uint64_t)p.out_step_w * p.C * es, (uint64_t)p.out_step_h * p.OWf * p.C * es,
                              (uint64_t)p.OHf * p.OWf * p.C * es};
     return encode_tmap_4d(m, dt, base, dims, str, box, swizzle);
 }

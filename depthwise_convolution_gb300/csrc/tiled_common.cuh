@@ -54,9 +54,9 @@ __device__ __forceinline__ Unit decode(const Geo &g, int u) {
 // Elements outside the sub-grid (padding, channel tail, missing images) are
 // filled with zeros by the copy engine.
 inline bool make_halo_map(CUtensorMap *m, const TiledConv &p, const Geo &g, dwconv_dtype dt, size_t es) {
-    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off * p.Wf + p.in_off) * p.C * es;
+    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off_h * p.Wf + p.in_off_w) * p.C * es;
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
+    const uint64_t str[3] = {(uint64_t)p.in_step_w * p.C * es, (uint64_t)p.in_step_h * p.Wf * p.C * es,
                              (uint64_t)p.Hf * p.Wf * p.C * es};
     const uint32_t box[4] = {32, (uint32_t)g.HW, (uint32_t)g.HH, (uint32_t)g.NI};
     return encode_tmap_4d(m, dt, base, dims, str, box);

@@ -295,9 +295,9 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     if (!plan<T, TH, TW>(p, g, smem)) return cudaErrorNotSupported;
     // Input rows: the taps' sub-grid of p.in, one row of the unit's halo per box.
     const size_t es = sizeof(T);
-    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off * p.Wf + p.in_off) * p.C * es;
+    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off_h * p.Wf + p.in_off_w) * p.C * es;
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
+    const uint64_t str[3] = {(uint64_t)p.in_step_w * p.C * es, (uint64_t)p.in_step_h * p.Wf * p.C * es,
                              (uint64_t)p.Hf * p.Wf * p.C * es};
     const uint32_t box[4] = {32, (uint32_t)g.HW, 1, (uint32_t)g.NI};
     // Filter [FH][FW][C] as a 4-D tensor with a unit outer dimension; one box =
@@ -336,7 +336,7 @@ cudaError_t by_width(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
 }
 
 cudaError_t launch_tiled_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    if (p.FW < 8 || p.zero_phases || p.out_step != 1) return cudaErrorNotSupported;
+    if (p.FW < 8 || p.zero_phases || p.out_step_h != 1 || p.out_step_w != 1) return cudaErrorNotSupported;
     switch (dt) {
         case DWCONV_FP32: return by_width<float, 224>(p, dt, st);
         case DWCONV_FP16: return by_width<__half, DWCONV_L_MAXR16>(p, dt, st);

@@ -306,9 +306,9 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     // swizzle (the inner box row is exactly one 32-channel pixel).  The output
     // map covers y (or dx) directly; the TMA store clips the tile at the edges.
     const size_t es = sizeof(T);
-    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off * p.Wf + p.in_off) * p.C * es;
+    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off_h * p.Wf + p.in_off_w) * p.C * es;
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
+    const uint64_t str[3] = {(uint64_t)p.in_step_w * p.C * es, (uint64_t)p.in_step_h * p.Wf * p.C * es,
                              (uint64_t)p.Hf * p.Wf * p.C * es};
     const uint32_t box[4] = {(uint32_t)kCh, (uint32_t)C::SW, (uint32_t)C::HRI, (uint32_t)NI};
     const uint32_t obox[4] = {(uint32_t)kCh, (uint32_t)C::OTW, (uint32_t)C::OTH, (uint32_t)NI};

@@ -229,9 +229,9 @@ cudaError_t run_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     g.per_ctile = (int)per;
     g.units = (int)units;
     const size_t es = sizeof(T);
-    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off * p.Wf + p.in_off) * p.C * es;
+    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off_h * p.Wf + p.in_off_w) * p.C * es;
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.in_step * p.C * es, (uint64_t)p.in_step * p.Wf * p.C * es,
+    const uint64_t str[3] = {(uint64_t)p.in_step_w * p.C * es, (uint64_t)p.in_step_h * p.Wf * p.C * es,
                              (uint64_t)p.Hf * p.Wf * p.C * es};
     const uint32_t box[4] = {(uint32_t)kLCh, (uint32_t)C::SW, (uint32_t)C::HR, 1};
     const uint32_t obox[4] = {(uint32_t)kLCh, (uint32_t)C::OTW, (uint32_t)C::OTH, 1};
@@ -275,7 +275,7 @@ cudaError_t large_by_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st
 #endif
 
 cudaError_t launch_tiled_mma_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    if (!DWCONV_MMA_LARGE || p.zero_phases || p.out_step != 1) return cudaErrorNotSupported;
+    if (!DWCONV_MMA_LARGE || p.zero_phases || p.out_step_h != 1 || p.out_step_w != 1) return cudaErrorNotSupported;
     switch (dt) {
         case DWCONV_FP16: return large_by_filter<__half>(p, dt, st);
         case DWCONV_BF16: return large_by_filter<__nv_bfloat16>(p, dt, st);

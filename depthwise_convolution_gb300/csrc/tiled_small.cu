@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                             for (int b = 0; b < OS; ++b) {
                                 const int orow = OS * i + a, ocol = OS * j + b;
                                 if (orow < p.OHf && ocol < p.OWf) {
-                                    const bool hit = a == p.out_off && b == p.out_off;
+                                    const bool hit = a == p.out_off_h && b == p.out_off_w;
                                     Pair<T>::store(img + ((long long)orow * p.OWf + ocol) * p.C,
                                                    hit ? acc[th][tw] : make_float2(0.f, 0.f));
                                 }
@@ -217,13 +217,13 @@ cudaError_t dispatch_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st
     constexpr int TH7 = k16 ? DWCONV_S16_TH : DWCONV_S32_TH, TW7 = k16 ? DWCONV_S16_TW : 7;
     constexpr int MB7 = k16 ? DWCONV_S16_MINB : DWCONV_S32_MINB;
     if (p.zero_phases) {
-        if (p.out_step != 2) return cudaErrorNotSupported;
+        if (p.out_step_h != 2 || p.out_step_w != 2) return cudaErrorNotSupported;
         if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 2>(p, dt, st);
         if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 2>(p, dt, st);
         if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7, 2>(p, dt, st);
         return cudaErrorNotSupported;
     }
-    if (p.out_step != 1) return cudaErrorNotSupported;
+    if (p.out_step_h != 1 || p.out_step_w != 1) return cudaErrorNotSupported;
     if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7, 1>(p, dt, st);
     if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 1>(p, dt, st);
     if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 1>(p, dt, st);

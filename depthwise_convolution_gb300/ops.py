@@ -42,18 +42,34 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _pair(v, what):
+    if isinstance(v, (tuple, list)):
+        if len(v) != 2:
+            raise ValueError(f"{what} must be an int or an (h, w) pair")
+        return int(v[0]), int(v[1])
+    return int(v), int(v)
+
+
+def _axes(stride, dilation, pad):
+    """stride, dilation, pad (each an int or an (h, w) pair) -> the six per-axis ints."""
+    (sh, sw), (dh, dw), (ph, pw) = _pair(stride, "stride"), _pair(dilation, "dilation"), _pair(pad, "pad")
+    return sh, sw, dh, dw, ph, pw
+
+
 def dwconv_output_size(H, W, FH, FW, stride=1, dilation=1, pad=0):
-    """(OH, OW) of the forward pass; raises DwconvError on invalid sizes."""
+    """(OH, OW) of the forward pass; raises DwconvError on invalid sizes.
+    stride, dilation and pad: an int (both axes) or an (h, w) pair."""
     oh, ow = ctypes.c_int(0), ctypes.c_int(0)
-    _lib.check(_lib.load().dwconv_output_size(H, W, FH, FW, stride, dilation, pad,
-                                               ctypes.byref(oh), ctypes.byref(ow)),
+    _lib.check(_lib.load().dwconv_output_size_2d(H, W, FH, FW, *_axes(stride, dilation, pad),
+                                                  ctypes.byref(oh), ctypes.byref(ow)),
                "dwconv_output_size")
     return oh.value, ow.value
 
 
 def dwconv_fwd(x, w, bias=None, stride=1, dilation=1, pad=0, out=None, stream=None):
     """y = DWC(x, w) + bias.  x [N,H,W,C], w [FH,FW,C], bias [C] (fp32, or int32
-    for int8 data) or None.  Returns y [N,OH,OW,C] (int32 for int8 data)."""
+    for int8 data) or None; stride, dilation, pad: int or (h, w).  Returns
+    y [N,OH,OW,C] (int32 for int8 data)."""
     N, H, W, C = x.shape
     FH, FW = w.shape[0], w.shape[1]
     dt = _code(x)
@@ -68,15 +84,15 @@ def dwconv_fwd(x, w, bias=None, stride=1, dilation=1, pad=0, out=None, stream=No
         out = torch.empty((N, OH, OW, C), dtype=y_dtype, device=x.device)
     elif out.dtype != y_dtype or tuple(out.shape) != (N, OH, OW, C):
         raise ValueError("out has the wrong shape or dtype")
-    _lib.check(_lib.load().dwconv_fwd(
-        N, H, W, C, FH, FW, stride, dilation, pad, dt,
+    _lib.check(_lib.load().dwconv_fwd_2d(
+        N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
         _dev(x, "x", 4), _dev(w, "w", 3), None if bias is None else _dev(bias, "bias", 1),
         _dev(out, "out", 4), _stream(stream)), "dwconv_fwd")
     return out
 
 
 def dwconv_bwd_data(dy, w, H, W, stride=1, dilation=1, pad=0, out=None, stream=None):
-    """dx [N,H,W,C] from dy [N,OH,OW,C] and w [FH,FW,C]."""
+    """dx [N,H,W,C] from dy [N,OH,OW,C] and w [FH,FW,C]; stride, dilation, pad: int or (h, w)."""
     N, OH, OW, C = dy.shape
     FH, FW = w.shape[0], w.shape[1]
     dt = _code(dy)
@@ -88,8 +104,8 @@ def dwconv_bwd_data(dy, w, H, W, stride=1, dilation=1, pad=0, out=None, stream=N
         out = torch.empty((N, H, W, C), dtype=dy.dtype, device=dy.device)
     elif out.dtype != dy.dtype or tuple(out.shape) != (N, H, W, C):
         raise ValueError("out has the wrong shape or dtype")
-    _lib.check(_lib.load().dwconv_bwd_data(
-        N, H, W, C, FH, FW, stride, dilation, pad, dt,
+    _lib.check(_lib.load().dwconv_bwd_data_2d(
+        N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
         _dev(dy, "dy", 4), _dev(w, "w", 3), _dev(out, "out", 4), _stream(stream)), "dwconv_bwd_data")
     return out
 
@@ -97,8 +113,8 @@ def dwconv_bwd_data(dy, w, H, W, stride=1, dilation=1, pad=0, out=None, stream=N
 def dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation, pad, dtype) -> int:
     """Workspace bytes dwconv_bwd_filter needs (dtype: a torch dtype or ABI code)."""
     code = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
-    return int(_lib.load().dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation,
-                                                            pad, code))
+    return int(_lib.load().dwconv_bwd_filter_workspace_size_2d(N, H, W, C, FH, FW,
+                                                               *_axes(stride, dilation, pad), code))
 
 
 def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, workspace=None,
@@ -119,8 +135,8 @@ def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, work
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _lib.check(_lib.load().dwconv_bwd_filter(
-        N, H, W, C, FH, FW, stride, dilation, pad, dt,
+    _lib.check(_lib.load().dwconv_bwd_filter_2d(
+        N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
         _dev(x, "x", 4), _dev(dy, "dy", 4), _dev(out, "out", 3),
         workspace.data_ptr(), ws_bytes, _stream(stream)), "dwconv_bwd_filter")
     return out

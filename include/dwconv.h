@@ -186,6 +186,33 @@ dwconv_status dwconv_bwd_filter_static(int N, int H, int W, int C, int FH, int F
  */
 dwconv_status dwconv_check_device_errors(dwconv_stream stream);
 
+/*
+ * Per-axis forms.  Each _2d entry point is the operation of the entry point of
+ * the same name with the stride, dilation and padding given separately for
+ * the H and W axes: taps read x[n, oh*stride_h - pad_h + fh*dilation_h,
+ * ow*stride_w - pad_w + fw*dilation_w, c], and
+ * OH = floor((H + 2 pad_h - dilation_h (FH-1) - 1) / stride_h) + 1 (OW alike).
+ * (The pages give one stride, dilation and padding; the per-axis form is the
+ * same index formula per axis, needed e.g. for "same" padding of 1 x K strip
+ * filters.)  Arguments, layouts, ownership, workspace and errors are those of
+ * the symmetric entry points, which call these with equal values per axis.
+ */
+dwconv_status dwconv_output_size_2d(int H, int W, int FH, int FW, int stride_h, int stride_w, int dilation_h,
+                                    int dilation_w, int pad_h, int pad_w, int *OH, int *OW);
+dwconv_status dwconv_fwd_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                            int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype, const void *x,
+                            const void *w, const void *bias, void *y, dwconv_stream stream);
+dwconv_status dwconv_bwd_data_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                                 int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                                 const void *dy, const void *w, void *dx, dwconv_stream stream);
+size_t dwconv_bwd_filter_workspace_size_2d(int N, int H, int W, int C, int FH, int FW, int stride_h,
+                                           int stride_w, int dilation_h, int dilation_w, int pad_h, int pad_w,
+                                           dwconv_dtype dtype);
+dwconv_status dwconv_bwd_filter_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                                   int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                                   const void *x, const void *dy, float *dw, void *workspace,
+                                   size_t workspace_bytes, dwconv_stream stream);
+
 /* A static, human-readable name for a status code. */
 const char *dwconv_status_string(dwconv_status status);
 

@@ -83,10 +83,20 @@ class Guarded:
         assert bool((head == 0xA5).all()) and bool((tail == 0xA5).all()), f"{what}: guard band overwritten"
 
 
+def _pair(v):
+    return (int(v[0]), int(v[1])) if isinstance(v, (tuple, list)) else (int(v), int(v))
+
+
+def out_hw(H, W, FH, FW, S, D, P):
+    """Forward output size; S, D, P each an int or an (h, w) pair."""
+    (sh, sw), (dh, dw), (ph, pw) = _pair(S), _pair(D), _pair(P)
+    return oracle.out_extent(H, FH, sh, dh, ph), oracle.out_extent(W, FW, sw, dw, pw)
+
+
 def random_inputs(dtype, N, H, W, C, FH, FW, S, D, P, seed, bias=True):
     from depthwise_convolution_gb300 import synthetic as syn
     wl = syn.Workload("case", dtype, N, H, W, C, FH, FW, S, D, P, bias, ("fwd", "dgrad", "wgrad"), seed)
-    OH, OW = oracle.out_extent(H, FH, S, D, P), oracle.out_extent(W, FW, S, D, P)
+    OH, OW = out_hw(H, W, FH, FW, S, D, P)
     if dtype == "int8":
         d = syn.make_inputs(wl)
         d["dy"] = None
@@ -99,7 +109,7 @@ def check_fwd(d, dtype, S, D, P, images=None, what="fwd"):
     x, w, b = d["x"], d["w"], d["bias"]
     N, H, W, C = x.shape
     FH, FW = w.shape[:2]
-    OH, OW = oracle.out_extent(H, FH, S, D, P), oracle.out_extent(W, FW, S, D, P)
+    OH, OW = out_hw(H, W, FH, FW, S, D, P)
     out_dtype = torch.int32 if dtype == "int8" else TORCH[dtype]
     g = Guarded((N, OH, OW, C), out_dtype)
     y = ops.dwconv_fwd(x.cuda(), w.cuda(), None if b is None else b.cuda(), S, D, P, out=g.t)

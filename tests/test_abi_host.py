@@ -54,6 +54,35 @@ def test_output_size_rejects_bad_sizes(lib, args):
     assert oh.value == -7
 
 
+@pytest.mark.parametrize("H,W,FH,FW,axes", [(9, 40, 1, 31, (1, 1, 1, 1, 0, 15)), (21, 30, 3, 5, (2, 1, 1, 1, 1, 2)),
+                                             (17, 33, 5, 5, (1, 2, 2, 2, 4, 3)), (8, 8, 3, 3, (1, 3, 2, 1, 2, 0))])
+def test_per_axis_output_size_matches_the_oracle(lib, H, W, FH, FW, axes):
+    sh, sw, dh, dw, ph, pw = axes
+    got = ops.dwconv_output_size(H, W, FH, FW, (sh, sw), (dh, dw), (ph, pw))
+    assert got == (oracle.out_extent(H, FH, sh, dh, ph), oracle.out_extent(W, FW, sw, dw, pw))
+
+
+def test_symmetric_forms_equal_the_per_axis_forms(lib):
+    oh1, ow1, oh2, ow2 = (ctypes.c_int(0) for _ in range(4))
+    assert lib.dwconv_output_size(17, 13, 5, 5, 2, 3, 6, ctypes.byref(oh1), ctypes.byref(ow1)) == 0
+    assert lib.dwconv_output_size_2d(17, 13, 5, 5, 2, 2, 3, 3, 6, 6, ctypes.byref(oh2), ctypes.byref(ow2)) == 0
+    assert (oh1.value, ow1.value) == (oh2.value, ow2.value)
+    assert lib.dwconv_bwd_filter_workspace_size(4, 56, 56, 96, 7, 7, 1, 1, 3, _lib.FP16) == \
+        lib.dwconv_bwd_filter_workspace_size_2d(4, 56, 56, 96, 7, 7, 1, 1, 1, 1, 3, 3, _lib.FP16)
+
+
+def test_per_axis_validation_before_any_launch(lib):
+    before = lib.dwconv_launch_count()
+    A_ = 0x7F0000000000
+    args = (2, 8, 8, 16, 3, 3)
+    assert lib.dwconv_fwd_2d(*args, 1, 0, 1, 1, 1, 1, _lib.FP16, A_, A_, None, A_, None) == _lib.ERR_INVALID_ARG
+    assert lib.dwconv_fwd_2d(*args, 1, 1, 1, 1, 1, -1, _lib.FP16, A_, A_, None, A_, None) == _lib.ERR_INVALID_ARG
+    assert lib.dwconv_bwd_data_2d(*args, 1, 1, 1, 1, 1, 1, _lib.INT8, A_, A_, A_, None) == _lib.ERR_UNSUPPORTED
+    assert lib.dwconv_bwd_filter_2d(*args, 1, 1, 1, 1, 1, 1, _lib.FP16, A_, A_, A_, None, 0, None) == \
+        _lib.ERR_INVALID_ARG                                           # workspace too small
+    assert lib.dwconv_launch_count() == before
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert lib.dwconv_status_string(code).decode().startswith("DWCONV_")

@@ -44,6 +44,28 @@ SMALL = [
 ]
 
 
+# (N, H, W, C, FH, FW, (sh, sw), (dh, dw), (ph, pw)): per-axis stride, dilation, padding
+AXES = [
+    (2, 9, 40, 32, 1, 31, 1, 1, (0, 15)),             # 1 x 31 strip, "same" padding
+    (2, 40, 9, 32, 31, 1, 1, 1, (15, 0)),             # 31 x 1 strip
+    (2, 20, 40, 32, 5, 51, 1, 1, (2, 25)),            # 5 x 51 strip (large-filter path)
+    (2, 21, 30, 32, 3, 5, (2, 1), 1, (1, 2)),         # stride 2 along H only
+    (2, 24, 26, 32, 7, 7, (2, 2), (2, 2), (3, 4)),    # s2 d2 with unequal padding: phases (1, 0)
+    (1, 17, 33, 40, 5, 5, (1, 2), (2, 2), (4, 3)),    # stride 1 x 2, dilation 2: sub-grids differ by axis
+    (2, 15, 19, 16, 3, 3, (3, 1), (1, 2), (0, 2)),    # direct path
+]
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("case", AXES, ids=lambda c: "x".join(map(str, c)).replace(" ", ""))
+def test_per_axis_parameters_all_passes(dtype, case):
+    N, H, W, C, FH, FW, S, D, P = case
+    d = random_inputs(dtype, N, H, W, C, FH, FW, S, D, P, seed=abs(hash(case)) % 1000 + 3)
+    check_fwd(d, dtype, S, D, P)
+    check_dgrad(d, dtype, S, D, P)
+    check_wgrad(d, dtype, S, D, P)
+
+
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: "x".join(map(str, c)))
 def test_small_shapes_all_passes(dtype, case):
