@@ -101,6 +101,17 @@ template <> struct Mac<__nv_bfloat16> {
     }
 };
 
+// Widening variant: a channel pair is widened to float2 when loaded and every
+// multiply-add is one packed fma.rn.f32x2 (the same products and roundings as
+// Mac<T>; fewer FMA instructions per value, at the cost of the conversions
+// and twice the registers per held value).
+template <typename T> struct MacW {
+    using V = float2;
+    static __device__ __forceinline__ V load(const T *p) { return Pair<T>::load(p); }
+    static __device__ __forceinline__ V zero() { return make_float2(0.f, 0.f); }
+    static __device__ __forceinline__ void fma(float2 &acc, V a, V b) { acc = __ffma2_rn(a, b, acc); }
+};
+
 // Scalar widening / rounding (round to nearest even for 16-bit outputs).
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
