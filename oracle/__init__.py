@@ -14,6 +14,9 @@ Contents
     that the parity tolerance scales with.
 ``dbias``
     The adjoint of the bias term (sum of dy over n, oh, ow), in numpy.
+``fwd_fused`` / ``activation``
+    The forward pass followed by a per-channel affine map and an activation
+    (ReLU, ReLU6, SiLU, GELU), written from the activations' definitions.
 ``forms``
     Independent second forms used only to pin the direct loops: the
     per-channel im2col GEMV (Flash-DWC §2.1, Fig. 1), the tiled form with
@@ -192,6 +195,42 @@ def wgrad(x, dy, FH, FW, stride=1, dilation=1, pad=0, nthreads=None):
     return dw, mag
 
 
+ACTIVATIONS = ("none", "relu", "relu6", "silu", "gelu")
+
+
+def activation(v, act):
+    """float64 activation functions, from their definitions: ReLU max(v, 0),
+    ReLU6 min(max(v, 0), 6), SiLU v * sigmoid(v) = v / (1 + e^-v),
+    GELU v * Phi(v) = v/2 * (1 + erf(v / sqrt(2)))."""
+    import math
+    v = np.asarray(v, dtype=np.float64)
+    if act == "none":
+        return v.copy()
+    if act == "relu":
+        return np.maximum(v, 0.0)
+    if act == "relu6":
+        return np.minimum(np.maximum(v, 0.0), 6.0)
+    if act == "silu":
+        return v / (1.0 + np.exp(-v))
+    if act == "gelu":
+        return 0.5 * v * (1.0 + np.vectorize(math.erf)(v / math.sqrt(2.0)))
+    raise ValueError(f"unknown activation {act!r}")
+
+
+def fwd_fused(x, w, bias=None, scale=None, shift=None, act="none", stride=1, dilation=1, pad=0, nthreads=None):
+    """Forward pass with a per-channel affine map and an activation after it:
+    y = act(scale[c] * (DWC(x, w) + bias[c]) + shift[c]), float64.  scale
+    defaults to 1, shift to 0 (a BatchNorm in inference mode folds into them).
+    Returns (y, mag) with mag = |scale| * mag_conv + |shift|, the magnitude of
+    the activation's argument."""
+    z, mag = fwd(np.asarray(x, dtype=np.float64), np.asarray(w, dtype=np.float64),
+                 None if bias is None else np.asarray(bias, dtype=np.float64), stride, dilation, pad, nthreads)
+    C = z.shape[-1]
+    s = np.ones(C) if scale is None else np.asarray(scale, dtype=np.float64)
+    t = np.zeros(C) if shift is None else np.asarray(shift, dtype=np.float64)
+    return activation(s * z + t, act), np.abs(s) * mag + np.abs(t)
+
+
 def dbias(dy):
     """Bias gradient.  dy [N,OH,OW,C] -> (db [C], mag [C]).
 
@@ -210,4 +249,5 @@ def dbias(dy):
 
 from . import forms, pages  # noqa: E402  (pure-Python helpers, no C needed)
 
-__all__ = ["build", "fwd", "dgrad", "wgrad", "dbias", "out_extent", "default_threads", "forms", "pages"]
+__all__ = ["build", "fwd", "fwd_fused", "activation", "ACTIVATIONS", "dgrad", "wgrad", "dbias", "out_extent",
+           "default_threads", "forms", "pages"]

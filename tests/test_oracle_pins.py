@@ -408,3 +408,30 @@ def test_strip_filter_is_a_1d_convolution_per_row():
         for oh in range(3):
             for c in range(3):
                 assert y[n, oh, :, c].tolist() == forms.conv1d_zero_pad(x[n, 2 * oh, :, c], w[0, :, c])
+
+
+# ---------------------------------------------------------- fused epilogue
+
+def test_activation_closed_forms():
+    v = np.array([-7.0, -1.0, 0.0, 0.5, 3.0, 7.0])
+    assert oracle.activation(v, "relu").tolist() == [0, 0, 0, 0.5, 3, 7]
+    assert oracle.activation(v, "relu6").tolist() == [0, 0, 0, 0.5, 3, 6]
+    assert oracle.activation(np.array([0.0]), "silu")[0] == 0 and oracle.activation(np.array([0.0]), "gelu")[0] == 0
+    # x*f(x) - (-x)*f(-x) = x for f a symmetric CDF (sigmoid, Phi): act(x) - act(-x) = x
+    x = np.linspace(-6, 6, 49)
+    for act in ("relu", "silu", "gelu"):
+        assert np.allclose(oracle.activation(x, act) - oracle.activation(-x, act), x, atol=1e-12)
+    # GELU(1) = Phi(1) = 0.8413447460685429...; SiLU(1) = 1 / (1 + 1/e)
+    assert abs(oracle.activation(np.array([1.0]), "gelu")[0] - 0.8413447460685429) < 1e-15
+    assert abs(oracle.activation(np.array([1.0]), "silu")[0] - 1 / (1 + np.exp(-1.0))) < 1e-15
+
+
+def test_fused_affine_without_activation_is_exact():
+    x, w, b = rint((2, 7, 6, 4)), rint((3, 3, 4)), rint((4,))
+    s, t = rint((4,), -3, 3), rint((4,))
+    y, _ = oracle.fwd(x, w, b, 1, 1, 1)
+    yf, mag = oracle.fwd_fused(x, w, b, s, t, "none", 1, 1, 1)
+    assert np.array_equal(yf, (s * y + t).astype(np.float64))
+    assert np.all(mag >= np.abs(yf))
+    yr, _ = oracle.fwd_fused(x, w, b, s, t, "relu", 1, 1, 1)
+    assert np.array_equal(yr, np.maximum(s * y + t, 0).astype(np.float64))
