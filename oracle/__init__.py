@@ -14,9 +14,11 @@ Contents
     that the parity tolerance scales with.
 ``dbias``
     The adjoint of the bias term (sum of dy over n, oh, ow), in numpy.
-``fwd_fused`` / ``activation``
-    The forward pass followed by a per-channel affine map and an activation
-    (ReLU, ReLU6, SiLU, GELU), written from the activations' definitions.
+``fwd_fused`` / ``prologue`` / ``activation`` / ``round_to``
+    The forward pass with a BN+Act before it (x rounded back to its storage
+    format, as the unfused layer stores it) and an affine map plus activation
+    after it; ReLU, ReLU6, SiLU and GELU from their definitions; IEEE
+    round-to-nearest-even to fp32 / fp16 / bf16.
 ``forms``
     Independent second forms used only to pin the direct loops: the
     per-channel im2col GEMV (Flash-DWC §2.1, Fig. 1), the tiled form with
@@ -217,18 +219,65 @@ def activation(v, act):
     raise ValueError(f"unknown activation {act!r}")
 
 
-def fwd_fused(x, w, bias=None, scale=None, shift=None, act="none", stride=1, dilation=1, pad=0, nthreads=None):
-    """Forward pass with a per-channel affine map and an activation after it:
-    y = act(scale[c] * (DWC(x, w) + bias[c]) + shift[c]), float64.  scale
-    defaults to 1, shift to 0 (a BatchNorm in inference mode folds into them).
-    Returns (y, mag) with mag = |scale| * mag_conv + |shift|, the magnitude of
-    the activation's argument."""
-    z, mag = fwd(np.asarray(x, dtype=np.float64), np.asarray(w, dtype=np.float64),
-                 None if bias is None else np.asarray(bias, dtype=np.float64), stride, dilation, pad, nthreads)
+# Storage formats: significand bits p (hidden bit included) and the frexp
+# exponent e_min of the smallest normal number (v = m 2^e, 0.5 <= m < 1).
+FORMATS = {"fp32": (24, -125), "fp16": (11, -13), "bf16": (8, -125)}
+
+
+def round_to(v, fmt):
+    """Round float64 values to the nearest value of a storage format, ties to
+    even (IEEE 754 round-to-nearest-even), subnormals included; overflow is
+    not handled (values stay far below the formats' largest numbers).  The
+    integer significand q = rint(v 2^(p - e)) has p bits for a normal v."""
+    p, emin = FORMATS[fmt]
+    v = np.asarray(v, dtype=np.float64)
+    _, e = np.frexp(v)
+    e = np.maximum(e, emin)
+    return np.ldexp(np.rint(np.ldexp(v, p - e)), e - p)
+
+
+def affine_act(v, scale, shift, act, axis_len):
+    """act(scale[c] v + shift[c]) over the last (channel) axis, float64;
+    scale None = 1, shift None = 0."""
+    s = np.ones(axis_len) if scale is None else np.asarray(scale, dtype=np.float64)
+    t = np.zeros(axis_len) if shift is None else np.asarray(shift, dtype=np.float64)
+    return activation(s * np.asarray(v, dtype=np.float64) + t, act)
+
+
+def prologue(x, pre, fmt):
+    """The fused layer's input x' = round_fmt(act(scale[c] x + shift[c])) for
+    pre = (scale, shift, act), as the unfused BN+Act layer would store it in
+    the storage format fmt (None: no rounding).  The padding of the
+    convolution is applied to x', so padded positions stay zero."""
+    x = np.asarray(x, dtype=np.float64)
+    if pre is None:
+        return x
+    xa = affine_act(x, pre[0], pre[1], pre[2], x.shape[-1])
+    return xa if fmt is None else round_to(xa, fmt)
+
+
+def fwd_fused(x, w, bias=None, pre=None, post=None, fmt=None, stride=1, dilation=1, pad=0, nthreads=None):
+    """Forward pass fused with a BN+Act before it and an affine map plus
+    activation after it (Flash-DWC §5.2 "Kernel fusion": the BN+Act+DWC
+    pattern, BN in inference form folded into a per-channel scale and shift):
+
+        x' = round_fmt(act_pre(s_pre[c] x + t_pre[c]))            (pre)
+        z  = DWC(x', w) + bias[c]                                 (zero padding of x')
+        y  = act_post(s_post[c] z + t_post[c])                    (post)
+
+    pre / post = (scale, shift, act) or None; float64 throughout except the
+    rounding of x' to the storage format fmt.  Returns (y, mag) with mag =
+    |s_post| mag_conv + |t_post|, the magnitude of act_post's argument
+    (mag_conv = sum |w x'| + |bias|)."""
+    xq = prologue(x, pre, fmt)
+    z, mag = fwd(xq, np.asarray(w, dtype=np.float64), None if bias is None else np.asarray(bias, dtype=np.float64),
+                 stride, dilation, pad, nthreads)
+    if post is None:
+        return z, mag
     C = z.shape[-1]
-    s = np.ones(C) if scale is None else np.asarray(scale, dtype=np.float64)
-    t = np.zeros(C) if shift is None else np.asarray(shift, dtype=np.float64)
-    return activation(s * z + t, act), np.abs(s) * mag + np.abs(t)
+    s = np.ones(C) if post[0] is None else np.asarray(post[0], dtype=np.float64)
+    t = np.zeros(C) if post[1] is None else np.asarray(post[1], dtype=np.float64)
+    return activation(s * z + t, post[2]), np.abs(s) * mag + np.abs(t)
 
 
 def dbias(dy):
@@ -249,5 +298,5 @@ def dbias(dy):
 
 from . import forms, pages  # noqa: E402  (pure-Python helpers, no C needed)
 
-__all__ = ["build", "fwd", "fwd_fused", "activation", "ACTIVATIONS", "dgrad", "wgrad", "dbias", "out_extent",
+__all__ = ["build", "fwd", "fwd_fused", "prologue", "affine_act", "activation", "ACTIVATIONS", "round_to", "FORMATS", "dgrad", "wgrad", "dbias", "out_extent",
            "default_threads", "forms", "pages"]

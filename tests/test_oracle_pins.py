@@ -430,8 +430,56 @@ def test_fused_affine_without_activation_is_exact():
     x, w, b = rint((2, 7, 6, 4)), rint((3, 3, 4)), rint((4,))
     s, t = rint((4,), -3, 3), rint((4,))
     y, _ = oracle.fwd(x, w, b, 1, 1, 1)
-    yf, mag = oracle.fwd_fused(x, w, b, s, t, "none", 1, 1, 1)
+    yf, mag = oracle.fwd_fused(x, w, b, post=(s, t, "none"), stride=1, dilation=1, pad=1)
     assert np.array_equal(yf, (s * y + t).astype(np.float64))
     assert np.all(mag >= np.abs(yf))
-    yr, _ = oracle.fwd_fused(x, w, b, s, t, "relu", 1, 1, 1)
+    yr, _ = oracle.fwd_fused(x, w, b, post=(s, t, "relu"), stride=1, dilation=1, pad=1)
     assert np.array_equal(yr, np.maximum(s * y + t, 0).astype(np.float64))
+
+
+def test_round_to_matches_library_casts():
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-6, 5, 4000),
+                        rng.standard_normal(200) * 1e-6])          # fp16 subnormals
+    v = v[np.abs(v) < 65504]                                        # overflow is out of scope
+    assert np.array_equal(oracle.round_to(v, "fp16"), v.astype(np.float16).astype(np.float64))
+    assert np.array_equal(oracle.round_to(v, "fp32"), v.astype(np.float32).astype(np.float64))
+    # bf16: from float32 values (one rounding either way), against torch's cast
+    v32 = v.astype(np.float32)
+    ref = torch.from_numpy(v32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_to(v32.astype(np.float64), "bf16"), ref)
+    # ties go to even: 1 + 2^-8 lies halfway between bf16 1 and 1 + 2^-7
+    assert oracle.round_to(np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8]), "bf16").tolist() == [1.0, 1 + 2 * 2.0 ** -7]
+
+
+def test_prologue_padding_stays_zero():
+    # x' = act(0 * x + 5) = 5 inside the input; the padding of x' is zero, so a
+    # 3x3 box filter gives 45 inside, 30 on an edge and 20 in a corner.
+    x = np.zeros((1, 4, 5, 2))
+    w = np.ones((3, 3, 2))
+    y, _ = oracle.fwd_fused(x, w, pre=(np.zeros(2), np.full(2, 5.0), "none"), pad=1)
+    assert y[0, 1, 1, 0] == 45 and y[0, 0, 2, 1] == 30 and y[0, 0, 0, 0] == 20 and y[0, 3, 4, 1] == 20
+    # ReLU of a negative shift wipes the input: only the bias is left
+    b = np.array([1.5, -2.0])
+    y, _ = oracle.fwd_fused(rint((1, 4, 5, 2)), w, b, pre=(None, np.full(2, -100.0), "relu"), pad=1)
+    assert np.all(y == b)
+
+
+def test_prologue_affine_is_linear():
+    # DWC(s x + t) = s DWC(x) + t DWC(1), with 1 the all-ones input (zero padded)
+    x, w = rint((2, 6, 7, 3)), rint((3, 5, 3))
+    s, t = rint((3,), -3, 3), rint((3,))
+    for S, D, P in [(1, 1, (1, 2)), (2, 1, 2), (1, 2, 3)]:
+        y, _ = oracle.fwd_fused(x, w, pre=(s, t, "none"), stride=S, dilation=D, pad=P)
+        y1, _ = oracle.fwd(x, w, None, S, D, P)
+        y0, _ = oracle.fwd(np.ones_like(x), w, None, S, D, P)
+        assert np.array_equal(y, s * y1 + t * y0)
+
+
+def test_prologue_rounds_to_storage_format():
+    x = np.full((1, 3, 3, 1), 1.0)
+    w = np.zeros((1, 1, 1)); w[0, 0, 0] = 1.0
+    # 1 * 1 + 2^-9 rounds to 1 in bf16 (8 bits), stays in fp16 (11 bits)
+    pre = (None, np.array([2.0 ** -9]), "none")
+    assert np.all(oracle.fwd_fused(x, w, pre=pre, fmt="bf16")[0] == 1.0)
+    assert np.all(oracle.fwd_fused(x, w, pre=pre, fmt="fp16")[0] == 1 + 2.0 ** -9)
