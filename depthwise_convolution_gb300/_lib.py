@@ -16,6 +16,8 @@ _lib = None
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT = range(6)
 INT8, FP32, FP16, BF16 = range(4)
+ACT_NONE, ACT_RELU, ACT_RELU6, ACT_SILU, ACT_GELU = range(5)
+ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "relu6": ACT_RELU6, "silu": ACT_SILU, "gelu": ACT_GELU}
 
 # Exported symbols and their C signatures: name -> (restype, argtypes).
 _I, _P, _SZ = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
@@ -35,6 +37,8 @@ SIGNATURES = {
     "dwconv_bwd_data_2d": (_I, [_I] * 12 + [_I, _P, _P, _P, _P]),
     "dwconv_bwd_filter_workspace_size_2d": (_SZ, [_I] * 12 + [_I]),
     "dwconv_bwd_filter_2d": (_I, [_I] * 12 + [_I, _P, _P, _P, _P, _SZ, _P]),
+    "dwconv_fwd_fused": (_I, [_I] * 9 + [_I, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P]),
+    "dwconv_fwd_fused_2d": (_I, [_I] * 12 + [_I, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P]),
     "dwconv_launch_count": (ctypes.c_ulonglong, []),
     "dwconv_last_kernel": (ctypes.c_char_p, []),
 }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "dwconv.h"
 
 namespace dwc {
@@ -124,11 +126,82 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
+// ---- fused BN+Act prologue / affine+activation epilogue ---------------------
+
+// Flash-DWC §5.2 "Kernel fusion": per channel c, the forward pass may read
+//   x' = round_T(act_in(in_scale[c] * x + in_shift[c]))   at every input position
+// (the zero padding applies to x') and write
+//   y = round_T(act_out(out_scale[c] * (conv + bias[c]) + out_shift[c])).
+// Null scale = 1, null shift = 0, act 0 = identity; fp32 arithmetic, one
+// fmaf for the affine map.
+struct Fuse {
+    const float *in_scale, *in_shift;
+    int in_act;
+    const float *out_scale, *out_shift;
+    int out_act;
+    __host__ __device__ bool pre() const { return in_scale || in_shift || in_act; }
+    __host__ __device__ bool post() const { return out_scale || out_shift || out_act; }
+};
+
+__device__ __forceinline__ float activate(float v, int act) {
+    switch (act) {
+        case DWCONV_ACT_RELU: return fmaxf(v, 0.f);
+        case DWCONV_ACT_RELU6: return fminf(fmaxf(v, 0.f), 6.f);
+        case DWCONV_ACT_SILU: return v / (1.f + expf(-v));                        // v * sigmoid(v)
+        case DWCONV_ACT_GELU: return 0.5f * v * (1.f + erff(v * 0.7071067811865476f));  // v * Phi(v)
+        default: return v;
+    }
+}
+
+// Per-channel coefficients of one affine map (channel c must be valid).
+struct Affine {
+    float s, t;
+};
+__device__ __forceinline__ Affine affine_in(const Fuse &f, int c) {
+    return {f.in_scale ? __ldg(f.in_scale + c) : 1.f, f.in_shift ? __ldg(f.in_shift + c) : 0.f};
+}
+__device__ __forceinline__ Affine affine_out(const Fuse &f, int c) {
+    return {f.out_scale ? __ldg(f.out_scale + c) : 1.f, f.out_shift ? __ldg(f.out_shift + c) : 0.f};
+}
+__device__ __forceinline__ float apply(Affine a, float v, int act) { return activate(fmaf(a.s, v, a.t), act); }
+
+// Calls f(std::integral_constant<int, act>{}) so that loops over many values
+// see the activation as a compile-time constant (one branch per loop, not per
+// value).
+template <typename F>
+__device__ __forceinline__ void with_act(int act, F &&f) {
+    switch (act) {
+        case DWCONV_ACT_RELU: f(std::integral_constant<int, DWCONV_ACT_RELU>{}); break;
+        case DWCONV_ACT_RELU6: f(std::integral_constant<int, DWCONV_ACT_RELU6>{}); break;
+        case DWCONV_ACT_SILU: f(std::integral_constant<int, DWCONV_ACT_SILU>{}); break;
+        case DWCONV_ACT_GELU: f(std::integral_constant<int, DWCONV_ACT_GELU>{}); break;
+        default: f(std::integral_constant<int, DWCONV_ACT_NONE>{}); break;
+    }
+}
+
+// A channel pair of a 16-bit type packed in one 32-bit word <-> float2.
+template <typename T> __device__ __forceinline__ float2 unpack2(unsigned v);
+template <> __device__ __forceinline__ float2 unpack2<__half>(unsigned v) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&v));
+}
+template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(unsigned v) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v));
+}
+template <typename T> __device__ __forceinline__ unsigned pack2(float2 v);
+template <> __device__ __forceinline__ unsigned pack2<__half>(float2 v) {
+    const __half2 h = __float22half2_rn(v);
+    return *reinterpret_cast<const unsigned *>(&h);
+}
+template <> __device__ __forceinline__ unsigned pack2<__nv_bfloat16>(float2 v) {
+    const __nv_bfloat162 h = __float22bfloat162_rn(v);
+    return *reinterpret_cast<const unsigned *>(&h);
+}
+
 // ---- launchers (each returns the launch's cudaError_t) -----------------------
 
 // Direct kernels: any shape, any dtype the pass supports; one thread per output.
 cudaError_t launch_fwd_direct(const Shape &s, dwconv_dtype dt, const void *x, const void *w,
-                              const void *bias, void *y, cudaStream_t st);
+                              const void *bias, void *y, const Fuse &fz, cudaStream_t st);
 cudaError_t launch_dgrad_direct(const Shape &s, dwconv_dtype dt, const void *dy, const void *w,
                                 void *dx, cudaStream_t st);
 // wgrad, first pass: partial sums over Z slices of the N*OH*OW axis into
@@ -166,6 +239,7 @@ struct TiledConv {
     // zero_phases, the other positions of each out_step_h x out_step_w block
     // are written with zeros.
     int OHf, OWf, OHs, OWs, out_step_h, out_step_w, out_off_h, out_off_w, zero_phases;
+    Fuse fz;               // forward only; all null / zero: plain convolution
 };
 
 // Returns cudaErrorNotSupported when no tiled instance covers the request.
@@ -177,6 +251,8 @@ cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t
 // caller zeroes the rest).  tiled_mma_supports: the shape rules, no launch.
 cudaError_t launch_tiled_mma(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 bool tiled_mma_supports(const TiledConv &p, dwconv_dtype dt);
+// The same kernel with the fused forward pass (p.fz) compiled in.
+cudaError_t launch_tiled_mma_fused(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 // Tensor-core Toeplitz kernel for large 16-bit filters (tiled_mma_large.cu).
 cudaError_t launch_tiled_mma_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 

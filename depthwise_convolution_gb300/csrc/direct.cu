@@ -18,12 +18,15 @@ int grid_for(long long total) {
     return (int)(blocks < 1 ? 1 : blocks);
 }
 
-// Forward, floating point: fp32 accumulation, bias first, taps fh-major.
+// Forward, floating point: fp32 accumulation, bias first, taps fh-major;
+// optional BN+Act prologue on every input value read (rounded back to T, as
+// the unfused layer stores it) and affine+activation epilogue.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) fwd_direct_fp(Shape s, const T *__restrict__ x,
                                                           const T *__restrict__ w,
                                                           const float *__restrict__ bias,
-                                                          T *__restrict__ y, long long total) {
+                                                          T *__restrict__ y, long long total, Fuse fz) {
+    const bool pre = fz.pre(), post = fz.post();
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
         int c = (int)(idx % s.C);
@@ -33,6 +36,7 @@ __global__ void __launch_bounds__(kThreads) fwd_direct_fp(Shape s, const T *__re
         int oh = (int)(t % s.OH);
         long long n = t / s.OH;
         float acc = bias ? bias[c] : 0.f;
+        const Affine ain = pre ? affine_in(fz, c) : Affine{1.f, 0.f};
         for (int fh = 0; fh < s.FH; ++fh) {
             int ih = oh * s.SH - s.PH + fh * s.DH;
             if (ih < 0 || ih >= s.H) continue;
@@ -41,9 +45,12 @@ __global__ void __launch_bounds__(kThreads) fwd_direct_fp(Shape s, const T *__re
             for (int fw = 0; fw < s.FW; ++fw) {
                 int iw = ow * s.SW - s.PW + fw * s.DW;
                 if (iw < 0 || iw >= s.W) continue;
-                acc = fmaf(to_f32(wrow[(long long)fw * s.C]), to_f32(xrow[(long long)iw * s.C]), acc);
+                float xv = to_f32(xrow[(long long)iw * s.C]);
+                if (pre) xv = to_f32(from_f32<T>(apply(ain, xv, fz.in_act)));
+                acc = fmaf(to_f32(wrow[(long long)fw * s.C]), xv, acc);
             }
         }
+        if (post) acc = apply(affine_out(fz, c), acc, fz.out_act);
         y[idx] = from_f32<T>(acc);
     }
 }
@@ -226,7 +233,7 @@ cudaError_t launch_bias_slices(long long P, int C, dwconv_dtype dt, const void *
 }
 
 cudaError_t launch_fwd_direct(const Shape &s, dwconv_dtype dt, const void *x, const void *w,
-                              const void *bias, void *y, cudaStream_t st) {
+                              const void *bias, void *y, const Fuse &fz, cudaStream_t st) {
     const long long total = (long long)s.N * s.OH * s.OW * s.C;
     const int grid = grid_for(total);
     switch (dt) {
@@ -236,16 +243,16 @@ cudaError_t launch_fwd_direct(const Shape &s, dwconv_dtype dt, const void *x, co
             break;
         case DWCONV_FP32:
             fwd_direct_fp<float><<<grid, kThreads, 0, st>>>(s, (const float *)x, (const float *)w,
-                                                            (const float *)bias, (float *)y, total);
+                                                            (const float *)bias, (float *)y, total, fz);
             break;
         case DWCONV_FP16:
             fwd_direct_fp<__half><<<grid, kThreads, 0, st>>>(s, (const __half *)x, (const __half *)w,
-                                                             (const float *)bias, (__half *)y, total);
+                                                             (const float *)bias, (__half *)y, total, fz);
             break;
         case DWCONV_BF16:
             fwd_direct_fp<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
                 s, (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w, (const float *)bias,
-                (__nv_bfloat16 *)y, total);
+                (__nv_bfloat16 *)y, total, fz);
             break;
         default:
             return cudaErrorInvalidValue;

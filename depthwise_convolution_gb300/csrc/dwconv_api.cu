@@ -188,37 +188,80 @@ dwconv_status dwconv_check_device_errors(dwconv_stream stream) {
     return v ? DWCONV_ERR_TIMEOUT : DWCONV_OK;
 }
 
-dwconv_status dwconv_fwd_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
-                            int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype, const void *x,
-                            const void *w, const void *bias, void *y, dwconv_stream stream) {
+}  // extern "C"
+
+namespace dwc {
+namespace {
+
+dwconv_status fwd_impl(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w, int dilation_h,
+                       int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype, const void *x, const void *w,
+                       const void *bias, void *y, const Fuse &fz, dwconv_stream stream) {
     if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
     Shape s;
     dwconv_status st =
         make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s);
     if (st != DWCONV_OK) return st;
     if (!x || !w || !y) return DWCONV_ERR_INVALID_ARG;
+    auto act_ok = [](int a) { return a >= DWCONV_ACT_NONE && a <= DWCONV_ACT_GELU; };
+    if (!act_ok(fz.in_act) || !act_ok(fz.out_act)) return DWCONV_ERR_INVALID_ARG;
+    if (dtype == DWCONV_INT8 && (fz.pre() || fz.post())) return DWCONV_ERR_UNSUPPORTED;
     const size_t es = elem_size(dtype);
     const size_t bs = 4;  // int32 (int8 data) or float bias
     const size_t ys = dtype == DWCONV_INT8 ? 4 : es;
     if (!aligned(x, es) || !aligned(w, es) || !aligned(y, ys) || (bias && !aligned(bias, bs)))
         return DWCONV_ERR_MISALIGNED;
+    for (const float *v : {fz.in_scale, fz.in_shift, fz.out_scale, fz.out_shift})
+        if (v && !aligned(v, 4)) return DWCONV_ERR_MISALIGNED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
 
     // Unit stride and dilation on the taps' sub-grid (unit_subgrid) go to the
-    // tiled kernels.
+    // tiled kernels.  A kernel that does not provide a requested fusion
+    // declines it (cudaErrorNotSupported) and the next one is tried.
     TiledConv p{};
     if (tiled_layout_ok(s, dtype, x, y, w) && unit_subgrid(s, p)) {
         p.in = x; p.w = w; p.bias = static_cast<const float *>(bias); p.out = y;
         p.N = N; p.C = C; p.FH = FH; p.FW = FW; p.flip = 0;
         p.OHf = s.OH; p.OWf = s.OW; p.OHs = s.OH; p.OWs = s.OW;
         p.out_step_h = p.out_step_w = 1; p.out_off_h = p.out_off_w = 0; p.zero_phases = 0;
+        p.fz = fz;
         cudaError_t e = launch_tiled_mma(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma_large(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_small(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
-    return cuda_status(launch_fwd_direct(s, dtype, x, w, bias, y, cs));
+    return cuda_status(launch_fwd_direct(s, dtype, x, w, bias, y, fz, cs));
+}
+
+}  // namespace
+}  // namespace dwc
+
+extern "C" {
+
+dwconv_status dwconv_fwd_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                            int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype, const void *x,
+                            const void *w, const void *bias, void *y, dwconv_stream stream) {
+    return fwd_impl(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, dtype, x, w,
+                    bias, y, Fuse{}, stream);
+}
+
+dwconv_status dwconv_fwd_fused_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                                  int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                                  const void *x, const float *in_scale, const float *in_shift,
+                                  dwconv_activation in_act, const void *w, const void *bias,
+                                  const float *out_scale, const float *out_shift, dwconv_activation out_act,
+                                  void *y, dwconv_stream stream) {
+    const Fuse fz{in_scale, in_shift, (int)in_act, out_scale, out_shift, (int)out_act};
+    return fwd_impl(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, dtype, x, w,
+                    bias, y, fz, stream);
+}
+
+dwconv_status dwconv_fwd_fused(int N, int H, int W, int C, int FH, int FW, int stride, int dilation, int pad,
+                               dwconv_dtype dtype, const void *x, const float *in_scale, const float *in_shift,
+                               dwconv_activation in_act, const void *w, const void *bias, const float *out_scale,
+                               const float *out_shift, dwconv_activation out_act, void *y, dwconv_stream stream) {
+    return dwconv_fwd_fused_2d(N, H, W, C, FH, FW, stride, stride, dilation, dilation, pad, pad, dtype, x,
+                               in_scale, in_shift, in_act, w, bias, out_scale, out_shift, out_act, y, stream);
 }
 
 dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride, int dilation, int pad,

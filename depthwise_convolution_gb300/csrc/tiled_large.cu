@@ -82,7 +82,9 @@ __device__ __forceinline__ Unit decode_l(const GeoL &g, int u) {
 // MAXR: registers per thread, sized so the wanted number of 288-thread CTAs
 // fits an SM: each of the 4 sub-partitions holds 16K registers, and two
 // 9-warp CTAs put 5 warps on some sub-partition, so two CTAs need <= 102.
-template <typename T, int TH, int TW, int MAXR, int FWC, bool FLIP>
+// FUSE: the affine+activation epilogue of the fused forward pass (Flash-DWC
+// §5.2) is compiled in (this kernel provides no BN+Act prologue).
+template <typename T, int TH, int TW, int MAXR, int FWC, bool FLIP, bool FUSE = false>
 __global__ void __maxnreg__(MAXR)
     tiled_large_kernel(const __grid_constant__ CUtensorMap row_map, const __grid_constant__ CUtensorMap filt_map,
                        TiledConv p, GeoL g, unsigned *err) {
@@ -239,6 +241,18 @@ __global__ void __maxnreg__(MAXR)
 
         // Unit done: store, and release the filter if the next unit needs another.
         const int n = cur.group * g.NI + img_l;
+        if (FUSE && p.fz.post() && c < p.C) {
+            const Affine a0 = affine_out(p.fz, c), a1 = affine_out(p.fz, c + 1);
+            with_act(p.fz.out_act, [&](auto act) {
+#pragma unroll
+                for (int th = 0; th < TH; ++th)
+#pragma unroll
+                    for (int tw = 0; tw < TW; ++tw) {
+                        acc[th][tw].x = activate(fmaf(a0.s, acc[th][tw].x, a0.t), decltype(act)::value);
+                        acc[th][tw].y = activate(fmaf(a1.s, acc[th][tw].y, a1.t), decltype(act)::value);
+                    }
+            });
+        }
         if (c < p.C && n < p.N) {
             const int i0 = cur.band * tile_rows + rt * TH;
             const int j0 = cur.twi * tile_cols + ct * TW;
@@ -288,7 +302,7 @@ bool plan(const TiledConv &p, GeoL &g, size_t &smem) {
     return smem <= 220 * 1024;
 }
 
-template <typename T, int TH, int TW, int MAXR, int FWC, bool FLIP>
+template <typename T, int TH, int TW, int MAXR, int FWC, bool FLIP, bool FUSE = false>
 cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     GeoL g;
     size_t smem;
@@ -309,7 +323,7 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     if (!encode_tmap_4d(&row_map, dt, base, dims, str, box) ||
         !encode_tmap_4d(&filt_map, dt, p.w, fdims, fstr, fbox))
         return cudaErrorNotSupported;
-    auto kern = tiled_large_kernel<T, TH, TW, MAXR, FWC, FLIP>;
+    auto kern = tiled_large_kernel<T, TH, TW, MAXR, FWC, FLIP, FUSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -330,8 +344,10 @@ template <typename T, int MAXR>
 cudaError_t by_width(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     constexpr int TH = DWCONV_L_TH, TW = DWCONV_L_TW;
 #if DWCONV_L_FW31
-    if (p.FW == 31) return p.flip ? run<T, TH, TW, MAXR, 31, true>(p, dt, st) : run<T, TH, TW, MAXR, 31, false>(p, dt, st);
+    if (p.FW == 31 && !p.fz.pre() && !p.fz.post()) return p.flip ? run<T, TH, TW, MAXR, 31, true>(p, dt, st) : run<T, TH, TW, MAXR, 31, false>(p, dt, st);
 #endif
+    if (p.fz.pre()) return cudaErrorNotSupported;
+    if (p.fz.post()) return p.flip ? cudaErrorNotSupported : run<T, TH, TW, MAXR, 0, false, true>(p, dt, st);
     return p.flip ? run<T, TH, TW, MAXR, 0, true>(p, dt, st) : run<T, TH, TW, MAXR, 0, false>(p, dt, st);
 }
 

@@ -1,362 +1,11 @@
 // Tensor-core forward pass and stride-1 input gradient for 16-bit data and
-// 3x3, 5x5 and 7x7 filters.
-//
-// The GEMV of one channel (Flash-DWC §2.1) is packed into dense MMAs as in
-// Flash-DWC §4.2: 8 consecutive outputs of one output row ("a group") read a
-// window of 16 consecutive inputs, and for one filter row fh
-//
-//   Y[group m][n] += sum_{k<16} A[m][k] * B[k][n],   A[m][k] = X[ih][8j_m + k],
-//                                                    B[k][n] = w[fh][k - n] (0 outside [0, FW)),
-//
-// a 16 x 8 Toeplitz band of the filter row.  One warp-level mma.sync
-// m16n8k16 (bf16/fp16 in, fp32 accumulate) takes 16 groups at once, in two
-// blocks of 8 M rows; a block is G groups of each of 8/G consecutive output
-// rows (G = 8 on maps wider than 32 columns, 4 above 16, 2 above 8).
-// A channel's output block needs FH such MMAs (one per filter row); the
-// accumulator stays in registers across them, so every partial sum is kept in
-// fp32 and the bias is added once, at the start.
-//
-// Work unit: 32 channels x OTW = 8G columns of NI images, 256 threads, each
-// warp 4 channels; contiguous unit ranges per CTA.  With NI = 1 (maps more
-// than 16 columns wide) the unit is OTH = 2 * KNB * 8/G rows of one image and
-// M rows 8-15 cover the rows half a tile below rows 0-7; with NI = 2 (narrow
-// maps, few rows) it is OTH = KNB * 8/G rows of two images and M rows 8-15
-// cover the same rows of the second image.
-//   1. one TMA copy stages the NHWC input halo in shared memory with the
-//      64-byte swizzle (zeros outside the input: padding is generated); with
-//      room for two staging buffers the next two units' loads are in flight;
-//   2. ldmatrix.trans + stmatrix transpose it into a channel-major buffer
-//      T[channel][row][column], in which the 8 windows of an 8-row matrix of
-//      an MMA operand are 8 rows of 16 bytes (one ldmatrix matrix);
-//   3. the A operands of the KNB row sets x FH filter rows overlap: MMA (row
-//      set j, filter row fh) reads rows from x = j*8/G + fh on, so the operand
-//      of x (one ldmatrix.x4) serves every (j, fh) with that x;
-//   4. B (the Toeplitz bands of the warp's 4 channels) stays in registers for
-//      all units of a channel tile;
-//   5. the results, rounded to 16 bits, go to a separate 64B-swizzled NHWC
-//      output tile and leave with one TMA tensor store (clipped at the
-//      tensor edges by the copy engine).
-// Two CTA barriers per unit: "T and the output tile are ready" and "the
-// output tile is complete (and every warp is done with T)".
-#include "mma_common.cuh"
+// 3x3, 5x5 and 7x7 filters: shape rules and the launcher of the plain passes.
+// The kernel (Flash-DWC §4.2 Toeplitz packing on mma.sync) is in
+// tiled_mma_kernel.cuh; the fused forward pass has its own instances in
+// tiled_mma_fused.cu.
+#include "tiled_mma_kernel.cuh"
 
 namespace dwc {
-namespace {
-
-using namespace tiled;
-using namespace mma;
-
-#ifndef DWCONV_MMA_REUSE
-#define DWCONV_MMA_REUSE 4  // G for which half of each A operand is rebuilt from registers (0: none)
-#endif
-
-constexpr int kCh = 32;                 // channels per work unit
-constexpr int kChPerWarp = 4;           // channels per warp
-constexpr int kMThreads = kCh / kChPerWarp * 32;
-constexpr int kPB = 2 * kCh;            // bytes of one staged pixel (= swizzle span)
-
-// Shared-memory address of a byte offset inside a buffer with the TMA's
-// 64-byte swizzle (16-byte chunk bits 4-5 XOR address bits 7-8).
-__device__ __forceinline__ unsigned swz(unsigned a) { return a ^ (((a >> 7) & 3u) << 4); }
-
-// Tile geometry, fixed by the filter height, G, the images per unit NI and
-// the row sets per unit KNB.
-template <int FH, int G, int NI, int KNB>
-struct Cfg {
-    static constexpr int RB = 8 / G;                              // output rows of an 8-row M block
-    static constexpr int OTH = NI == 1 ? 2 * KNB * RB : KNB * RB; // output rows per image
-    static constexpr int OTW = 8 * G;                             // output columns
-    static constexpr int HRI = OTH + FH - 1;                      // staged rows per image
-    static constexpr int DHT = NI == 1 ? KNB * RB : HRI;          // T rows from M rows 0-7 to 8-15
-    static constexpr int OHB = NI == 1 ? KNB * RB : OTH;          // output-tile rows, same
-    static constexpr int TR = NI * HRI, SW = OTW + 8;             // staged rows, columns
-    static constexpr int RS = SW;                                 // T row stride (halves)
-    static constexpr int CS = channel_stride(TR * RS);            // T channel stride (halves)
-    static constexpr int NQ = (KNB - 1) * RB + FH;                // A operands per channel
-    static constexpr unsigned s_bytes = TR * SW * kPB;
-    static constexpr unsigned s_stride = align1k(s_bytes);
-    static constexpr unsigned t_bytes = align1k(kCh * CS * 2);
-    static constexpr unsigned o_bytes = NI * OTH * OTW * kPB;
-    static constexpr int NS = 2 * s_stride + t_bytes + o_bytes + 1024 <= 227 * 1024 ? 2 : 1;  // staging buffers
-    static constexpr unsigned t_off = NS * s_stride;
-    static constexpr unsigned o_off = t_off + t_bytes;
-    static constexpr unsigned smem = o_off + o_bytes;             // + 1 KB alignment slack at launch
-    static constexpr int MINB = smem + 2048 <= 113 * 1024 ? 2 : 1;  // CTAs per SM registers are capped for
-};
-
-template <typename T, int FH, int FW, int G, int NI, int KNB>
-__global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB>::MINB))
-    tiled_mma_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap out_map,
-                     TiledConv p, GeoM g, unsigned *err) {
-    using C = Cfg<FH, G, NI, KNB>;
-    constexpr int RB = C::RB, DHT = C::DHT, NQ = C::NQ, NS = C::NS;
-    extern __shared__ __align__(1024) unsigned char smem_dyn[];
-    __shared__ __align__(8) uint64_t bar[NS];
-    using Op = MmaOp<T>;
-
-    // Swizzled buffers start on 1024-byte boundaries (the launch adds 1 KB of slack).
-    unsigned char *smem_raw = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int gq = lane / 4, t4 = lane % 4;  // mma fragment coordinates
-    unsigned char *S = smem_raw;             // NS staging buffers [NI][HRI][SW][32], s_stride apart
-    const unsigned s_addr = smem_addr(S);
-    const unsigned t_addr = s_addr + C::t_off;  // T [32][CS] halves
-    const unsigned o_addr = s_addr + C::o_off;  // output tile [NI][OTH][OTW][32], swizzled
-    const T *wg = static_cast<const T *>(p.w);
-
-    // Contiguous unit range of this CTA (channel tile slowest: few B reloads).
-    const int u_begin = (int)((long long)g.units * blockIdx.x / gridDim.x);
-    const int u_end = (int)((long long)g.units * (blockIdx.x + 1) / gridDim.x);
-
-    if (tid == 0) {
-        for (int b = 0; b < NS; ++b) mbar_init(&bar[b], 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
-
-    // Unit cursors (row band fastest) for the loads (thread 0) and the compute.
-    Unit ld = decode(g, u_begin), cur = ld;
-    auto issue = [&](int b) {
-        const Unit un = ld;
-        advance(g, g.groups, ld);
-        mbar_arrive_expect_tx(&bar[b], C::s_bytes);
-        tma_load_4d(S + b * C::s_stride, &halo_map, un.ctile * kCh, un.twi * C::OTW - p.pad_w,
-                    un.band * C::OTH - p.pad_h, un.group * NI, &bar[b]);
-    };
-    if (tid == 0)
-        for (int b = 0; b < NS && u_begin + b < u_end; ++b) issue(b);
-
-    // A operand x of a channel = one ldmatrix.x4: matrix j (lanes 8j..8j+7
-    // give its row addresses) holds M rows 8(j%2)..+7 and k 8(j/2)..+7; M row
-    // i of block j%2 is window i % G of T row x + i / G + DHT (j%2).
-    const int mj = lane / 8, mi = lane % 8;
-    const int lane_off = ((mj & 1) * DHT + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj >> 1);
-    // ldmatrix.x2 of T rows x + DHT alone: matrix mj & 1 = k half.
-    const int lane_off2 = (DHT + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj & 1);
-    // Transposition: one ldmatrix.x4 = the 4 16-byte channel chunks of 8
-    // pixels; this lane addresses row tr of matrix tj.
-    const int tr = lane % 8, tj = lane / 8;
-    // Output: lane (gq, t4) writes position (row gq / G (+ OHB for M rows
-    // 8-15), column 8 (gq % G) + 2t4 + e) of each row set; the bits the
-    // swizzle reads (7 and up) do not depend on the row set or on e, so the
-    // lane's swizzled chunk is fixed.
-    const unsigned o_pos = (unsigned)((gq / G) * C::OTW + 8 * (gq % G) + 2 * t4) * kPB;
-    const unsigned o_lane = o_addr + swz(o_pos + (unsigned)warp * 8);
-    const unsigned o_lane0 = o_lane + (gq & 1) * kPB, o_lane1 = o_lane + (1 - (gq & 1)) * kPB;
-
-    int loaded_ctile = -1;
-    float bias_r[kChPerWarp];
-    unsigned bfr[kChPerWarp][FH][2];  // Toeplitz bands, B fragments (k 0-7, k 8-15)
-    for (int u = u_begin, k = 0; u < u_end; ++u, ++k, advance(g, g.groups, cur)) {
-        if (cur.ctile != loaded_ctile) {
-            // B[k][n] = w[fh][k - n]: lane (gq, t4) holds k = 2t4, 2t4+1 (+8), n = gq.
-            // For the input gradient the filter is rotated by 180 degrees.
-            loaded_ctile = cur.ctile;
-#pragma unroll
-            for (int ci = 0; ci < kChPerWarp; ++ci) {
-                const int cc = cur.ctile * kCh + warp * kChPerWarp + ci;
-                const bool live = cc < p.C;
-                bias_r[ci] = (p.bias && live) ? p.bias[cc] : 0.f;
-#pragma unroll
-                for (int fh = 0; fh < FH; ++fh) {
-                    const int sfh = p.flip ? FH - 1 - fh : fh;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        T v[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int fw = 2 * t4 + e + 8 * h - gq;
-                            v[e] = from_f32<T>(0.f);
-                            if (live && fw >= 0 && fw < FW)
-                                v[e] = wg[(sfh * FW + (p.flip ? FW - 1 - fw : fw)) * p.C + cc];
-                        }
-                        bfr[ci][fh][h] = Op::pack_raw(v[0], v[1]);
-                    }
-                }
-            }
-        }
-        if (!mbar_wait(&bar[k % NS], (k / NS) & 1)) {
-            report_timeout(err);
-            return;
-        }
-
-        // Transpose S[row][col][ch] -> T[ch][row][col], 8 columns x 32
-        // channels per step: ldmatrix.trans gives lane (gq, t4) cols 2t4,
-        // 2t4+1 of channel 8 chunk + gq; stmatrix writes them as the 16-byte
-        // row (channel, row, 8 cols).  Every warp finished reading T (previous
-        // unit) before the last barrier.
-        const unsigned s_buf = s_addr + (k % NS) * C::s_stride;
-        for (int b = warp; b < C::TR * (C::SW / 8); b += kMThreads / 32) {
-            const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
-            const unsigned src = s_buf + swz((unsigned)((row * C::SW + col0 + tr) * kPB + 16 * tj));
-            unsigned v0, v1, v2, v3;
-            ldsm_x4_trans(v0, v1, v2, v3, src);
-            stsm_x4(t_addr + 2u * ((8 * tj + tr) * C::CS + row * C::RS + col0), v0, v1, v2, v3);
-        }
-        // The previous unit's TMA store must have read the output tile.
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
-        __syncthreads();  // T ready, output tile free, this staging buffer free
-        if (tid == 0 && u + NS < u_end) issue(k % NS);
-
-        // MMAs.  Stage x loads operand x + 1 (one ahead, also across
-        // channels) and runs the MMAs of operand x, row sets interleaved
-        // (independent accumulators).
-        float d[kChPerWarp][KNB][4];
-        // With kReuse (NI = 1), operand x >= DHT shares its rows-x half with
-        // operand x - DHT (whose rows-(x - DHT + DHT) half it is): that half is
-        // copied from registers and only rows x + DHT are loaded (one
-        // ldmatrix.x2).  Measured: a gain for G = 4; for G = 8 the extra
-        // registers spill.
-        constexpr bool kReuse = DWCONV_MMA_REUSE == G && NI == 1;
-        unsigned A[kReuse ? kChPerWarp : 1][kReuse ? NQ : 2][4];
-        auto load_a = [&](int ci, int x) {
-            const unsigned base = t_addr + 2u * ((warp * kChPerWarp + ci) * C::CS + x * C::RS);
-            if constexpr (kReuse) {
-                if (x < DHT) {
-                    ldsm_x4(A[ci][x][0], A[ci][x][1], A[ci][x][2], A[ci][x][3], base + 2u * lane_off);
-                } else {
-                    A[ci][x][0] = A[ci][x - DHT][1];
-                    A[ci][x][2] = A[ci][x - DHT][3];
-                    ldsm_x2(A[ci][x][1], A[ci][x][3], base + 2u * lane_off2);
-                }
-            } else {
-                const int sl = (ci * NQ + x) & 1;  // stage number (over all channels) mod 2
-                ldsm_x4(A[0][sl][0], A[0][sl][1], A[0][sl][2], A[0][sl][3], base + 2u * lane_off);
-            }
-        };
-        load_a(0, 0);
-#pragma unroll
-        for (int ci = 0; ci < kChPerWarp; ++ci) {
-#pragma unroll
-            for (int j = 0; j < KNB; ++j) d[ci][j][0] = d[ci][j][1] = d[ci][j][2] = d[ci][j][3] = bias_r[ci];
-#pragma unroll
-            for (int x = 0; x < NQ; ++x) {
-                if (x + 1 < NQ)
-                    load_a(ci, x + 1);
-                else if (ci + 1 < kChPerWarp)
-                    load_a(ci + 1, 0);
-                const unsigned *a;
-                if constexpr (kReuse)
-                    a = A[ci][x];
-                else
-                    a = A[0][(ci * NQ + x) & 1];
-#pragma unroll
-                for (int j = 0; j < KNB; ++j) {
-                    const int fh = x - j * RB;
-                    if (fh >= 0 && fh < FH)
-                        Op::run(d[ci][j], a[0], a[1], a[2], a[3], bfr[ci][fh][0], bfr[ci][fh][1]);
-                }
-            }
-        }
-
-        // Output tile, 64B-swizzled for the TMA store: this lane writes 8
-        // bytes (its warp's 4 channels) per output position.  The two columns
-        // 2t4, 2t4+1 go out in the order set by gq's parity, so one store
-        // covers both 64-byte halves of a 128-byte line (4-way instead of
-        // 8-way bank conflicts).
-#pragma unroll
-        for (int j = 0; j < KNB; ++j)
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                unsigned lo[2], hi[2];  // column 2t4 + e: channels (0, 1), (2, 3)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    lo[e] = Op::pack(d[0][j][2 * half + e], d[1][j][2 * half + e]);
-                    hi[e] = Op::pack(d[2][j][2 * half + e], d[3][j][2 * half + e]);
-                }
-                const bool odd = gq & 1;
-                const unsigned row = (j * RB + half * C::OHB) * C::OTW * kPB;
-                asm volatile("st.shared.v2.b32 [%0], {%1, %2};\n" ::"r"(o_lane0 + row), "r"(odd ? lo[1] : lo[0]),
-                             "r"(odd ? hi[1] : hi[0])
-                             : "memory");
-                asm volatile("st.shared.v2.b32 [%0], {%1, %2};\n" ::"r"(o_lane1 + row), "r"(odd ? lo[0] : lo[1]),
-                             "r"(odd ? hi[0] : hi[1])
-                             : "memory");
-            }
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // visible to the TMA store
-        __syncthreads();  // output tile complete; every warp is done with T
-        if (tid == 0) {
-            asm volatile(
-                "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];\n" ::"l"(
-                    reinterpret_cast<uint64_t>(&out_map)),
-                "r"(cur.ctile * kCh), "r"(cur.twi * C::OTW), "r"(cur.band * C::OTH), "r"(cur.group * NI),
-                "r"(o_addr)
-                : "memory");
-            asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
-        }
-    }
-    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
-}
-
-template <typename T, int FH, int FW, int G, int NI, int KNB>
-cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    using C = Cfg<FH, G, NI, KNB>;
-    if (C::smem + 1024 > 227 * 1024) return cudaErrorNotSupported;
-    GeoM g{};
-    g.tiles_h = (p.OHs + C::OTH - 1) / C::OTH;
-    g.tiles_w = (p.OWs + C::OTW - 1) / C::OTW;
-    g.groups = (p.N + NI - 1) / NI;
-    const long long per = (long long)g.groups * g.tiles_w * g.tiles_h;
-    const long long units = per * ((p.C + kCh - 1) / kCh);
-    if (units >= (1LL << 30)) return cudaErrorNotSupported;
-    g.per_ctile = (int)per;
-    g.units = (int)units;
-    // Halo map as for the CUDA-core kernels, NI images per box, 64-byte
-    // swizzle (the inner box row is exactly one 32-channel pixel).  The output
-    // map covers y (or dx) directly; the TMA store clips the tile at the edges.
-    const size_t es = sizeof(T);
-    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off_h * p.Wf + p.in_off_w) * p.C * es;
-    const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.in_step_w * p.C * es, (uint64_t)p.in_step_h * p.Wf * p.C * es,
-                             (uint64_t)p.Hf * p.Wf * p.C * es};
-    const uint32_t box[4] = {(uint32_t)kCh, (uint32_t)C::SW, (uint32_t)C::HRI, (uint32_t)NI};
-    const uint32_t obox[4] = {(uint32_t)kCh, (uint32_t)C::OTW, (uint32_t)C::OTH, (uint32_t)NI};
-    CUtensorMap map, omap;
-    if (!encode_tmap_4d(&map, dt, base, dims, str, box, kPB) ||
-        !make_out_map(&omap, p, dt, es, obox, kPB))
-        return cudaErrorNotSupported;
-    auto kern = tiled_mma_kernel<T, FH, FW, G, NI, KNB>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem + 1024);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMThreads, C::smem + 1024);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorNotSupported;
-    const long long slots = (long long)sm_count() * per_sm;
-    const int grid = (int)std::min<long long>(g.units, slots);
-    kern<<<grid, kMThreads, C::smem + 1024, st>>>(map, omap, p, g, device_error_word());
-    note_launches(1);
-    note_kernel("tiled_mma");
-    return cudaGetLastError();
-}
-
-// Tile shape by map width: one image and 8 groups of 8 columns per M block
-// down to two images and 2 groups of 4 rows.  Maps of at most 8 columns stay
-// on the CUDA-core kernel: with 8-row units of two images (G = 1) a unit has
-// only FH MMAs per channel and the transposition and barriers dominate
-// (measured on GB300, bf16 7x7 on 7x7 maps: 0.033 ms against 0.024 ms).
-template <typename T, int FH, int FW>
-cudaError_t by_width(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    if (p.OWs > 32) return run<T, FH, FW, 8, 1, 4>(p, dt, st);
-    if (p.OWs > 16) return run<T, FH, FW, 4, 1, 4>(p, dt, st);
-    if (p.OWs > 8) return run<T, FH, FW, 2, 2, 4>(p, dt, st);
-    return cudaErrorNotSupported;
-}
-
-template <typename T>
-cudaError_t by_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    if (p.FH == 7 && p.FW == 7) return by_width<T, 7, 7>(p, dt, st);
-    if (p.FH == 5 && p.FW == 5) return by_width<T, 5, 5>(p, dt, st);
-    if (p.FH == 3 && p.FW == 3) return by_width<T, 3, 3>(p, dt, st);
-    return cudaErrorNotSupported;
-}
-
-}  // namespace
-
-#ifndef DWCONV_MMA
-#define DWCONV_MMA 1  // 0: leave every shape to the CUDA-core kernels
-#endif
 
 bool tiled_mma_supports(const TiledConv &p, dwconv_dtype dt) {
     if (!DWCONV_MMA || p.zero_phases || (dt != DWCONV_FP16 && dt != DWCONV_BF16)) return false;
@@ -370,9 +19,10 @@ cudaError_t launch_tiled_mma(const TiledConv &p, dwconv_dtype dt, cudaStream_t s
     // Output positions off the (out_step, out_off) grid are not written: a
     // caller with out_step > 1 zeroes them itself.
     if (!DWCONV_MMA || p.zero_phases) return cudaErrorNotSupported;
+    if (p.fz.pre() || p.fz.post()) return launch_tiled_mma_fused(p, dt, st);
     switch (dt) {
-        case DWCONV_FP16: return by_filter<__half>(p, dt, st);
-        case DWCONV_BF16: return by_filter<__nv_bfloat16>(p, dt, st);
+        case DWCONV_FP16: return by_filter<__half, false>(p, dt, st);
+        case DWCONV_BF16: return by_filter<__nv_bfloat16, false>(p, dt, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -56,7 +56,10 @@ struct CfgL {
     static_assert(SW % 8 == 0, "16-byte T rows");
 };
 
-template <typename T, int FH, int NKB, int G>
+// FUSE: the fused forward pass (Flash-DWC §5.2) compiled in -- the BN+Act
+// prologue during the transposition, the affine+activation epilogue on the
+// fp32 sums; separate instances keep the plain passes' register allocation.
+template <typename T, int FH, int NKB, int G, bool FUSE>
 __global__ void __launch_bounds__(kLThreads, 1)
     tiled_mma_large_kernel(const __grid_constant__ CUtensorMap halo_map,
                            const __grid_constant__ CUtensorMap out_map, TiledConv p, GeoM g, unsigned *err) {
@@ -147,13 +150,41 @@ __global__ void __launch_bounds__(kLThreads, 1)
         // Transpose S[row][col][8 ch] -> T[ch][row][col], four 8-column blocks
         // per step; the last step repeats its final block where the count is
         // not a multiple of 4 (same data to the same place).
-        for (int m0 = warp * 4; m0 < C::HR * C::CB; m0 += kLThreads / 8) {
-            const int m = min(m0 + tj, C::HR * C::CB - 1);
-            const int row = m / C::CB, col0 = (m % C::CB) * 8;
-            unsigned v0, v1, v2, v3;
-            ldsm_x4_trans(v0, v1, v2, v3, s_addr + (unsigned)((row * C::SW + col0 + tr) * 16));
-            stsm_x4(t_addr + 2u * (tr * C::CS + row * C::RS + col0), v0, v1, v2, v3);
-        }
+        // With the BN+Act prologue, lane (gq, t4) holds channel gq of
+        // columns 2t4, 2t4+1 of block m0 + j in register j; positions outside
+        // the input are padding of x' and stay zero.
+        auto transpose = [&](auto pre) {
+            constexpr int PA = decltype(pre)::value;  // activation, or -1: no prologue
+            Affine a{1.f, 0.f};
+            if constexpr (PA >= 0) {
+                const int c = cur.ctile * kLCh + gq;
+                if (c < p.C) a = affine_in(p.fz, c);
+            }
+            for (int m0 = warp * 4; m0 < C::HR * C::CB; m0 += kLThreads / 8) {
+                const int m = min(m0 + tj, C::HR * C::CB - 1);
+                const int row = m / C::CB, col0 = (m % C::CB) * 8;
+                unsigned v[4];
+                ldsm_x4_trans(v[0], v[1], v[2], v[3], s_addr + (unsigned)((row * C::SW + col0 + tr) * 16));
+                if constexpr (PA >= 0) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int mm = min(m0 + j, C::HR * C::CB - 1);
+                        const int ih = cur.band * C::OTH - p.pad_h + mm / C::CB;
+                        const int iw = cur.twi * C::OTW - p.pad_w + (mm % C::CB) * 8 + 2 * t4;
+                        const bool rok = ih >= 0 && ih < p.Hs;
+                        float2 f = unpack2<T>(v[j]);
+                        f.x = rok && iw >= 0 && iw < p.Ws ? activate(fmaf(a.s, f.x, a.t), PA) : 0.f;
+                        f.y = rok && iw + 1 >= 0 && iw + 1 < p.Ws ? activate(fmaf(a.s, f.y, a.t), PA) : 0.f;
+                        v[j] = pack2<T>(f);
+                    }
+                }
+                stsm_x4(t_addr + 2u * (tr * C::CS + row * C::RS + col0), v[0], v[1], v[2], v[3]);
+            }
+        };
+        if (FUSE && p.fz.pre())
+            with_act(p.fz.in_act, transpose);
+        else
+            transpose(std::integral_constant<int, -1>{});
         if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
         __syncthreads();  // T and F ready, S and the output tile free
         if (tid == 0 && u + 1 < u_end) issue();
@@ -186,6 +217,17 @@ __global__ void __launch_bounds__(kLThreads, 1)
             }
         }
 
+        if (FUSE && p.fz.post()) {
+            const int cc = cur.ctile * kLCh + warp;
+            const Affine a = cc < p.C ? affine_out(p.fz, cc) : Affine{1.f, 0.f};
+            with_act(p.fz.out_act, [&](auto act) {
+#pragma unroll
+                for (int j = 0; j < kLNB; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) d[j][e] = activate(fmaf(a.s, d[j][e], a.t), decltype(act)::value);
+            });
+        }
+
         // Output tile [OTH][OTW][8 ch]: this lane's channel, 2 bytes per position.
         const bool odd = gq & 1;
 #pragma unroll
@@ -215,7 +257,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
 }
 
-template <typename T, int FH, int NKB, int G>
+template <typename T, int FH, int NKB, int G, bool FUSE>
 cudaError_t run_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     using C = CfgL<FH, NKB, G>;
     if (C::smem + 1024 > 227 * 1024) return cudaErrorNotSupported;
@@ -238,7 +280,7 @@ cudaError_t run_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     CUtensorMap map, omap;
     if (!encode_tmap_4d(&map, dt, base, dims, str, box) || !make_out_map(&omap, p, dt, es, obox, 0))
         return cudaErrorNotSupported;
-    auto kern = tiled_mma_large_kernel<T, FH, NKB, G>;
+    auto kern = tiled_mma_large_kernel<T, FH, NKB, G, FUSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem + 1024);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -252,20 +294,26 @@ cudaError_t run_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <typename T, int FH, int NKB>
+template <typename T, int FH, int NKB, bool FUSE>
 cudaError_t large_by_width(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    if (p.OWs > 32) return run_large<T, FH, NKB, 8>(p, dt, st);
-    if (p.OWs > 16) return run_large<T, FH, NKB, 4>(p, dt, st);
+    if (p.OWs > 32) return run_large<T, FH, NKB, 8, FUSE>(p, dt, st);
+    if (p.OWs > 16) return run_large<T, FH, NKB, 4, FUSE>(p, dt, st);
     return cudaErrorNotSupported;
 }
 
 // Filter blocks for a width: the band of 8 outputs spans 8 + FW - 1 inputs.
-template <typename T>
+template <typename T, bool FUSE>
 cudaError_t large_by_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     const int nkb = (p.FW + 7 + 15) / 16;
-    if (p.FH == 31 && nkb == 3) return large_by_width<T, 31, 3>(p, dt, st);
-    if (p.FH == 13 && nkb == 2) return large_by_width<T, 13, 2>(p, dt, st);
+    if (p.FH == 31 && nkb == 3) return large_by_width<T, 31, 3, FUSE>(p, dt, st);
+    if (p.FH == 13 && nkb == 2) return large_by_width<T, 13, 2, FUSE>(p, dt, st);
     return cudaErrorNotSupported;
+}
+
+template <typename T>
+cudaError_t large_dispatch(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    if (p.fz.pre() || p.fz.post()) return p.flip ? cudaErrorNotSupported : large_by_filter<T, true>(p, dt, st);
+    return large_by_filter<T, false>(p, dt, st);
 }
 
 }  // namespace
@@ -277,8 +325,8 @@ cudaError_t large_by_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st
 cudaError_t launch_tiled_mma_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     if (!DWCONV_MMA_LARGE || p.zero_phases || p.out_step_h != 1 || p.out_step_w != 1) return cudaErrorNotSupported;
     switch (dt) {
-        case DWCONV_FP16: return large_by_filter<__half>(p, dt, st);
-        case DWCONV_BF16: return large_by_filter<__nv_bfloat16>(p, dt, st);
+        case DWCONV_FP16: return large_dispatch<__half>(p, dt, st);
+        case DWCONV_BF16: return large_dispatch<__nv_bfloat16>(p, dt, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -56,7 +56,10 @@ size_t smem_cap() {
 }
 
 
-template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS>
+// FUSE: the BN+Act prologue and the affine+activation epilogue of the fused
+// forward pass (Flash-DWC §5.2) are compiled in; separate instances, so that
+// the plain passes keep their own register allocation.
+template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS, bool FUSE>
 __global__ void __launch_bounds__(kThreads, MINB)
     tiled_small_kernel(const __grid_constant__ CUtensorMap halo_map, TiledConv p, Geo g, unsigned *err) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -112,6 +115,38 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const Unit cur = decode(g, u);
         const int c = cur.ctile * 32 + 2 * cp;
         const bool cvalid = c < p.C;
+        if (FUSE && p.fz.pre()) {
+            // BN+Act prologue, once per staged value, in place: thread (cp,
+            // t) takes channel pair cp of every 8th halo row.  Positions
+            // outside the input are padding of x' and stay zero; x' is
+            // rounded to T as the unfused layer would store it.
+            T *hb = reinterpret_cast<T *>(smem_raw + (k & 1) * buf_stride);
+            const Affine a0 = cvalid ? affine_in(p.fz, c) : Affine{1.f, 0.f};
+            const Affine a1 = cvalid ? affine_in(p.fz, c + 1) : Affine{1.f, 0.f};
+            with_act(p.fz.in_act, [&](auto act) {
+                constexpr int A = decltype(act)::value;
+                for (int rr = t; rr < g.NI * g.HH; rr += kTiles) {
+                    const int im = rr / g.HH, r = rr - im * g.HH;
+                    const int ih = cur.band * tile_rows - p.pad_h + r;
+                    const bool rok = ih >= 0 && ih < p.Hs && cur.group * g.NI + im < p.N;
+                    T *row = hb + rr * g.HW * 32 + 2 * cp;
+                    for (int col = 0; col < g.HW; ++col) {
+                        const int iw = cur.twi * tile_cols - p.pad_w + col;
+                        float2 v = make_float2(0.f, 0.f);
+                        if (rok && iw >= 0 && iw < p.Ws) {
+                            v = Pair<T>::load(row + col * 32);
+                            v.x = activate(fmaf(a0.s, v.x, a0.t), A);
+                            v.y = activate(fmaf(a1.s, v.y, a1.t), A);
+                        }
+                        Pair<T>::store(row + col * 32, v);
+                    }
+                }
+            });
+            // The generic-proxy writes come before this buffer's next TMA
+            // fill; every thread sees the whole transformed halo.
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            __syncthreads();
+        }
         if (cur.ctile != loaded_ctile) {
             loaded_ctile = cur.ctile;
 #pragma unroll
@@ -152,6 +187,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
 
         const int n = cur.group * g.NI + img_l;
+        if (FUSE && p.fz.post() && cvalid) {
+            // Epilogue: per-channel affine map and activation on the fp32 sums.
+            const Affine a0 = affine_out(p.fz, c), a1 = affine_out(p.fz, c + 1);
+            with_act(p.fz.out_act, [&](auto act) {
+#pragma unroll
+                for (int th = 0; th < TH; ++th)
+#pragma unroll
+                    for (int tw = 0; tw < TW; ++tw) {
+                        acc[th][tw].x = activate(fmaf(a0.s, acc[th][tw].x, a0.t), decltype(act)::value);
+                        acc[th][tw].y = activate(fmaf(a1.s, acc[th][tw].y, a1.t), decltype(act)::value);
+                    }
+            });
+        }
         if (cvalid && n < p.N) {
             const int i0 = cur.band * tile_rows + r0;
             const int jj0 = cur.twi * tile_cols + j0;
@@ -188,9 +236,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
 }
 
-template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS>
+template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS, bool FUSE = false>
 cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    auto kern = tiled_small_kernel<T, FH, FW, TH, TW, MINB, OS>;
+    auto kern = tiled_small_kernel<T, FH, FW, TH, TW, MINB, OS, FUSE>;
     const Geo g = make_geo(p, TH, TW, sizeof(T), false, smem_cap<T>());
     if (g.units == 0) return cudaErrorNotSupported;
     const size_t smem = stage_bytes(g, TH, TW, sizeof(T), false);
@@ -217,6 +265,7 @@ cudaError_t dispatch_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st
     constexpr int TH7 = k16 ? DWCONV_S16_TH : DWCONV_S32_TH, TW7 = k16 ? DWCONV_S16_TW : 7;
     constexpr int MB7 = k16 ? DWCONV_S16_MINB : DWCONV_S32_MINB;
     if (p.zero_phases) {
+        if (p.fz.pre() || p.fz.post()) return cudaErrorNotSupported;
         if (p.out_step_h != 2 || p.out_step_w != 2) return cudaErrorNotSupported;
         if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 2>(p, dt, st);
         if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 2>(p, dt, st);
@@ -224,6 +273,14 @@ cudaError_t dispatch_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st
         return cudaErrorNotSupported;
     }
     if (p.out_step_h != 1 || p.out_step_w != 1) return cudaErrorNotSupported;
+    if (p.fz.pre() || p.fz.post()) {
+        if (p.flip) return cudaErrorNotSupported;
+        if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7, 1, true>(p, dt, st);
+        if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 1, true>(p, dt, st);
+        if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 1, true>(p, dt, st);
+        if (p.FH == 3 && p.FW == 5) return run<T, 3, 5, 4, 7, 3, 1, true>(p, dt, st);
+        return cudaErrorNotSupported;
+    }
     if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7, 1>(p, dt, st);
     if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 1>(p, dt, st);
     if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 1>(p, dt, st);

@@ -91,6 +91,56 @@ def dwconv_fwd(x, w, bias=None, stride=1, dilation=1, pad=0, out=None, stream=No
     return out
 
 
+def _act(a) -> int:
+    if isinstance(a, str):
+        try:
+            return _lib.ACTIVATIONS[a]
+        except KeyError:
+            raise ValueError(f"unknown activation {a!r}; one of {sorted(_lib.ACTIVATIONS)}") from None
+    return int(a)
+
+
+def _vec(v, C, name):
+    if v is None:
+        return None
+    if v.dtype != torch.float32 or tuple(v.shape) != (C,):
+        raise ValueError(f"{name} must be [C] float32")
+    return _dev(v, name, 1)
+
+
+def dwconv_fwd_fused(x, w, bias=None, in_scale=None, in_shift=None, in_act="none", out_scale=None,
+                     out_shift=None, out_act="none", stride=1, dilation=1, pad=0, out=None, stream=None):
+    """Forward pass with a BN+Act prologue and an affine+activation epilogue:
+    x' = act_in(in_scale * x + in_shift) rounded to x's dtype (padding of x'
+    is zero), y = act_out(out_scale * (DWC(x', w) + bias) + out_shift).
+    Scales and shifts: [C] float32 CUDA tensors or None (1 and 0); activations:
+    "none", "relu", "relu6", "silu", "gelu" (or the ABI codes).  A BatchNorm in
+    inference form folds into scale = gamma / sqrt(var + eps) and
+    shift = beta - mean * scale.  Other arguments as dwconv_fwd."""
+    N, H, W, C = x.shape
+    FH, FW = w.shape[0], w.shape[1]
+    dt = _code(x)
+    ia, oa = _act(in_act), _act(out_act)
+    for v, name in ((in_scale, "in_scale"), (in_shift, "in_shift"), (out_scale, "out_scale"),
+                    (out_shift, "out_shift"), (bias, "bias")):
+        if v is not None and (v.dtype != torch.float32 or tuple(v.shape) != (C,)):
+            raise ValueError(f"{name} must be [C] float32")
+    if w.dtype != x.dtype or tuple(w.shape) != (FH, FW, C):
+        raise ValueError("w must be [FH, FW, C] with x's dtype")
+    OH, OW = dwconv_output_size(H, W, FH, FW, stride, dilation, pad)
+    if out is None:
+        out = torch.empty((N, OH, OW, C), dtype=x.dtype, device=x.device)
+    elif out.dtype != x.dtype or tuple(out.shape) != (N, OH, OW, C):
+        raise ValueError("out has the wrong shape or dtype")
+    _lib.check(_lib.load().dwconv_fwd_fused_2d(
+        N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
+        _dev(x, "x", 4), _vec(in_scale, C, "in_scale"), _vec(in_shift, C, "in_shift"), ia,
+        _dev(w, "w", 3), None if bias is None else _dev(bias, "bias", 1),
+        _vec(out_scale, C, "out_scale"), _vec(out_shift, C, "out_shift"), oa,
+        _dev(out, "out", 4), _stream(stream)), "dwconv_fwd_fused")
+    return out
+
+
 def dwconv_bwd_data(dy, w, H, W, stride=1, dilation=1, pad=0, out=None, stream=None):
     """dx [N,H,W,C] from dy [N,OH,OW,C] and w [FH,FW,C]; stride, dilation, pad: int or (h, w)."""
     N, OH, OW, C = dy.shape

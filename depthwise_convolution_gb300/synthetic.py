@@ -26,6 +26,7 @@ _TORCH_DTYPES = {
 
 # Tensor ids within a workload's seed sequence.
 _X, _W, _B, _DY = 0, 1, 2, 3
+_PRE, _POST = 4, 6  # scale at the id, shift at id + 1
 
 
 @dataclasses.dataclass(frozen=True)
@@ -120,6 +121,17 @@ def make_inputs(wl: Workload, dy_hw=None) -> dict:
     out["dy"] = (_cast(normal((wl.N, dy_hw[0], dy_hw[1], wl.C), wl.dy_sigma, wl.seed, _DY), wl.dtype)
                  if needs_dy else None)
     return out
+
+
+def make_affine(C: int, seed: int, stage: str) -> tuple:
+    """Per-channel (scale, shift) float32 CPU vectors for a fused forward pass,
+    stage "pre" (the BN before the convolution) or "post" (after it): scale
+    ~ N(1, 0.5^2) (a folded BN's gamma / sqrt(var + eps), sign changes
+    included), shift ~ N(0, 0.5^2)."""
+    base = {"pre": _PRE, "post": _POST}[stage]
+    scale = normal((C,), 0.5, seed, base) + np.float32(1.0)
+    shift = normal((C,), 0.5, seed, base + 1)
+    return torch.from_numpy(scale.astype(np.float32)), torch.from_numpy(shift.astype(np.float32))
 
 
 # The five workloads: shapes, distributions and seeds.

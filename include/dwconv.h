@@ -64,6 +64,15 @@ typedef enum {
     DWCONV_BF16 = 3
 } dwconv_dtype;
 
+/* Activation functions of the fused forward pass (dwconv_fwd_fused). */
+typedef enum {
+    DWCONV_ACT_NONE = 0,   /* identity */
+    DWCONV_ACT_RELU = 1,   /* max(v, 0) */
+    DWCONV_ACT_RELU6 = 2,  /* min(max(v, 0), 6) */
+    DWCONV_ACT_SILU = 3,   /* v * sigmoid(v) = v / (1 + exp(-v)) */
+    DWCONV_ACT_GELU = 4    /* v * Phi(v) = v/2 * (1 + erf(v / sqrt 2)), the exact (erf) form */
+} dwconv_activation;
+
 /* A CUDA stream (the same handle as cudaStream_t).  NULL = the legacy default stream. */
 typedef struct CUstream_st *dwconv_stream;
 
@@ -212,6 +221,42 @@ dwconv_status dwconv_bwd_filter_2d(int N, int H, int W, int C, int FH, int FW, i
                                    int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
                                    const void *x, const void *dy, float *dw, void *workspace,
                                    size_t workspace_bytes, dwconv_stream stream);
+
+/*
+ * Fused forward pass (Flash-DWC §5.2 "Kernel fusion": depthwise convolutions
+ * usually sit next to a batch normalisation and an activation, BN+Act+DWC;
+ * fusing them into the convolution's kernel saves the memory passes of the
+ * separate layers).  BN in inference form is a per-channel affine map, so
+ * with per-channel scale and shift vectors the pass computes
+ *
+ *   x'[n,ih,iw,c] = round_T(in_act(in_scale[c] * x[n,ih,iw,c] + in_shift[c]))
+ *   z[n,oh,ow,c]  = bias[c] + sum w[fh,fw,c] * x'[n, oh*stride_h-pad_h+fh*dilation_h, ..., c]
+ *   y[n,oh,ow,c]  = round_T(out_act(out_scale[c] * z[n,oh,ow,c] + out_shift[c]))
+ *
+ * with x' outside the input reading as zero (the padding belongs to x', the
+ * tensor the unfused BN+Act layer would have written) and round_T the
+ * rounding to the storage type (none for fp32): x' holds exactly what the
+ * unfused layer would store.  The affine maps are one fp32 fused
+ * multiply-add; the activations are evaluated in fp32.
+ * in_scale, in_shift, out_scale, out_shift: float [C] device vectors, each
+ * nullable (NULL scale = 1, NULL shift = 0); *_act a dwconv_activation.
+ * With every one of them NULL / DWCONV_ACT_NONE the call is dwconv_fwd_2d.
+ * Other arguments, layouts, ownership and errors as dwconv_fwd_2d; the
+ * fused vectors must be 4-byte aligned (else DWCONV_ERR_MISALIGNED), an
+ * activation outside the enum is DWCONV_ERR_INVALID_ARG, and DWCONV_INT8
+ * with any fusion is DWCONV_ERR_UNSUPPORTED.
+ */
+dwconv_status dwconv_fwd_fused_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                                  int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                                  const void *x, const float *in_scale, const float *in_shift,
+                                  dwconv_activation in_act, const void *w, const void *bias,
+                                  const float *out_scale, const float *out_shift, dwconv_activation out_act,
+                                  void *y, dwconv_stream stream);
+/* dwconv_fwd_fused_2d with the same stride, dilation and padding on both axes. */
+dwconv_status dwconv_fwd_fused(int N, int H, int W, int C, int FH, int FW, int stride, int dilation, int pad,
+                               dwconv_dtype dtype, const void *x, const float *in_scale, const float *in_shift,
+                               dwconv_activation in_act, const void *w, const void *bias, const float *out_scale,
+                               const float *out_shift, dwconv_activation out_act, void *y, dwconv_stream stream);
 
 /* A static, human-readable name for a status code. */
 const char *dwconv_status_string(dwconv_status status);

@@ -152,3 +152,63 @@ def check_wgrad(d, dtype, S, D, P, what="wgrad"):
     g.check(what)
     ref, mag = oracle.wgrad(to64(x), to64(dy), FH, FW, S, D, P)
     return compare(to64(dw), ref, mag, dtype, False, what)
+
+
+# Largest slope of each activation (|act'| <= LIP): an error e in the
+# activation's argument moves its value by at most LIP * e.  SiLU' peaks at
+# 1.0998 (v = 2.40), GELU' at 1.1289 (v = 1.41).
+LIP = {"none": 1.0, "relu": 1.0, "relu6": 1.0, "silu": 1.1, "gelu": 1.13}
+
+
+def check_fused(d, dtype, S, D, P, pre=None, post=None, images=None, what="fused"):
+    """Fused forward pass against oracle.fwd_fused.  pre / post: (scale,
+    shift, act) with CPU float32 scale / shift (or None).
+
+    Tolerance: LIP[act_post] * (TOL * mag + |s_post| * E_pre) + 1e-6 * mag,
+    plus half an ulp of 16-bit outputs, where mag is the oracle's magnitude
+    of act_post's argument and E_pre = sum |w| * ulp(x') bounds a one-ulp
+    difference in the rounding of any prologue value x' to the storage type
+    (the kernel evaluates the prologue in fp32, the oracle in float64, so a
+    value within a few fp32 ulps of a rounding boundary may round either way).
+    """
+    x, w, b = d["x"], d["w"], d["bias"]
+    N, H, W, C = x.shape
+    FH, FW = w.shape[:2]
+    OH, OW = out_hw(H, W, FH, FW, S, D, P)
+    cuda = lambda v: None if v is None else v.cuda()
+    kw = {}
+    if pre is not None:
+        kw.update(in_scale=cuda(pre[0]), in_shift=cuda(pre[1]), in_act=pre[2])
+    if post is not None:
+        kw.update(out_scale=cuda(post[0]), out_shift=cuda(post[1]), out_act=post[2])
+    g = Guarded((N, OH, OW, C), TORCH[dtype])
+    y = ops.dwconv_fwd_fused(x.cuda(), w.cuda(), cuda(b), stride=S, dilation=D, pad=P, out=g.t, **kw)
+    ops.dwconv_check_device_errors()
+    g.check(what)
+    kernel = ops.dwconv_last_kernel()
+    imgs = list(range(N)) if images is None else sorted(set(i % N for i in images))
+    f64 = lambda v: None if v is None else to64(v)
+    opre = None if pre is None else (f64(pre[0]), f64(pre[1]), pre[2])
+    opost = None if post is None else (f64(post[0]), f64(post[1]), post[2])
+    fmt = dtype if dtype in ("fp16", "bf16", "fp32") else None
+    ref, mag = oracle.fwd_fused(to64(x[imgs]), to64(w), f64(b), pre=opre, post=opost, fmt=fmt,
+                                stride=S, dilation=D, pad=P)
+    got = to64(y[imgs])
+    lip = LIP[post[2]] if post is not None else 1.0
+    s_post = np.ones(C) if post is None or post[0] is None else np.abs(f64(post[0]))
+    e_pre = 0.0
+    if pre is not None and dtype in ("fp16", "bf16"):
+        xq = oracle.prologue(to64(x[imgs]), opre, fmt)
+        e_pre, _ = oracle.fwd(2 * half_ulp(xq, dtype), np.abs(to64(w)), None, S, D, P)
+    assert got.shape == ref.shape
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bound = lip * (TOL[dtype] * mag + s_post * e_pre) + 1e-6 * mag
+    if dtype in ("fp16", "bf16"):
+        bound = bound + half_ulp(np.maximum(np.abs(ref), np.abs(got)), dtype)
+    over = err > bound
+    if over.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what} [{kernel}]: {int(over.sum())} elements over tolerance; worst at {i}: "
+                             f"gpu={got[i]!r} ref={ref[i]!r} mag={mag[i]!r} bound={bound[i]!r}")
+    return kernel

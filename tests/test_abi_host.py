@@ -128,6 +128,38 @@ def test_backward_validation(lib):
     assert lib.dwconv_bwd_filter(*args, _lib.BF16, A, A, A + 2, A, need, None) == _lib.ERR_MISALIGNED
 
 
+def fused(lib, *, dt=_lib.FP16, x=A, isc=None, ish=None, iact=0, b=None, osc=None, osh=None, oact=0, y=A):
+    return lib.dwconv_fwd_fused_2d(2, 8, 8, 16, 3, 3, 1, 1, 1, 1, 1, 1, dt, x, isc, ish, iact, A, b,
+                                   osc, osh, oact, y, None)
+
+
+def test_fused_validation_before_any_launch(lib):
+    before = lib.dwconv_launch_count()
+    assert fused(lib, iact=5) == _lib.ERR_INVALID_ARG                  # activation outside the enum
+    assert fused(lib, oact=-1) == _lib.ERR_INVALID_ARG
+    assert fused(lib, dt=_lib.INT8, iact=_lib.ACT_RELU) == _lib.ERR_UNSUPPORTED
+    assert fused(lib, dt=_lib.INT8, osh=A) == _lib.ERR_UNSUPPORTED
+    assert fused(lib, isc=A + 2) == _lib.ERR_MISALIGNED                 # float vectors
+    assert fused(lib, osh=A + 1) == _lib.ERR_MISALIGNED
+    assert fused(lib, x=None, iact=_lib.ACT_GELU) == _lib.ERR_INVALID_ARG
+    assert lib.dwconv_launch_count() == before
+    # the symmetric form validates the same way
+    assert lib.dwconv_fwd_fused(2, 8, 8, 16, 3, 3, 1, 1, 1, _lib.FP16, A, None, None, 9, A, None, None, None, 0,
+                                A, None) == _lib.ERR_INVALID_ARG
+
+
+def test_python_fused_binding_checks_arguments():
+    import torch
+    x = torch.zeros(1, 4, 4, 8, dtype=torch.float16)
+    w = torch.zeros(3, 3, 8, dtype=torch.float16)
+    with pytest.raises(ValueError, match="unknown activation"):
+        ops.dwconv_fwd_fused(x, w, in_act="tanh")
+    with pytest.raises(ValueError, match="out_scale"):
+        ops.dwconv_fwd_fused(x, w, out_scale=torch.ones(8, dtype=torch.float16))
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.dwconv_fwd_fused(x, w, in_act="relu")
+
+
 def test_workspace_size_is_a_pure_function_of_the_shape(lib):
     args = (128, 56, 56, 96, 7, 7, 1, 1, 3)
     a = lib.dwconv_bwd_filter_workspace_size(*args, _lib.FP16)
