@@ -200,6 +200,18 @@ class Layer:
             ops.dwconv_bwd_filter(self.x, self.dy, wl.FH, wl.FW, wl.stride, wl.dilation, wl.pad, out=self.dw,
                                   workspace=self.ws, stream=stream)
 
+    def run_fused(self, stream=None):
+        """The forward pass fused with a BN+ReLU before it and a BN+ReLU6 after
+        it (per-channel scale/shift vectors from the seeded generator)."""
+        wl = self.wl
+        if not hasattr(self, "aff"):
+            pre = [t.to(self.x.device) for t in synthetic.make_affine(wl.C, wl.seed, "pre")]
+            post = [t.to(self.x.device) for t in synthetic.make_affine(wl.C, wl.seed, "post")]
+            self.aff = pre + post
+        s0, t0, s1, t1 = self.aff
+        ops.dwconv_fwd_fused(self.x, self.w, self.bias, s0, t0, "relu", s1, t1, "relu6", wl.stride, wl.dilation,
+                             wl.pad, out=self.y, stream=stream)
+
     def twin(self):
         """A second set of device buffers with the same inputs (for pipelining)."""
         t = object.__new__(Layer)
@@ -237,6 +249,30 @@ def time_layer(layer, steps, warmup, flush):
     per_pass = {p: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)] for j, p in enumerate(passes)}
     step_ms = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)]
     return step_ms, per_pass, launches
+
+
+def time_fusion(layer, steps, flush):
+    """Forward pass alone and fused (BN+ReLU before, BN+ReLU6 after), CUDA
+    events per call, L2 flushed before each; plus the HBM floor of the two
+    separate elementwise passes the fusion replaces (read + write x and y
+    once each, at the measured copy bandwidth)."""
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, fn in (("plain", lambda: layer.run_pass("fwd")), ("fused", layer.run_fused)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        kernel = ops.dwconv_last_kernel()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        out[name] = {"ms": round(statistics.mean(a.elapsed_time(b) for a, b in ev), 4), "kernel": kernel}
+    out["fused_over_plain"] = round(out["fused"]["ms"] / out["plain"]["ms"], 3)
+    return out
 
 
 def time_e2e(layer, steps):
@@ -451,6 +487,24 @@ def main():
             except Exception as e:  # report, do not hide
                 sweep[name] = {"error": str(e)[:200]}
 
+    fusion = {}
+    if rank == 0 and ws == 1 and not args.no_sweep:
+        pk_gbs = pk["hbm_gbs"]
+        for name, other in [(wl.name, wl)] + list(synthetic.WORKLOADS.items()):
+            if other.dtype == "int8" or "fwd" not in other.passes or name in fusion:
+                continue
+            try:
+                lay = layer if name == wl.name else Layer(other)
+                f = time_fusion(lay, max(20, args.steps // 10), flush)
+                es = lay.x.element_size()
+                sep = 2 * (lay.x.numel() + lay.y.numel()) * es
+                f["separate_passes_floor_ms"] = round(sep / (pk_gbs * 1e9) * 1e3, 4)
+                fusion[name] = f
+                if lay is not layer:
+                    del lay
+            except Exception as e:  # report, do not hide
+                fusion[name] = {"error": str(e)[:200]}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         v, cores, sample = oracle_sample(wl)
@@ -466,7 +520,7 @@ def main():
                        "l2": "flushed before each timed step (256 MiB write)",
                        "parallelism": f"{ws} independent replica(s)"},
             "passes": passes, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-            "clocks": sampler.summary(t0, t1), "cpu_baseline": cpu, "sweep": sweep}
+            "clocks": sampler.summary(t0, t1), "cpu_baseline": cpu, "sweep": sweep, "fusion": fusion}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -143,12 +143,35 @@ struct Fuse {
     __host__ __device__ bool post() const { return out_scale || out_shift || out_act; }
 };
 
+// Gauss error function for GELU, from Abramowitz & Stegun, "Handbook of
+// Mathematical Functions", formula 7.1.26: for x >= 0,
+//   erfc(x) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2) + e(x),
+//   t = 1 / (1 + p x),  |e(x)| <= 1.5e-7,
+// with p and a1..a5 as printed there.  Evaluated in fp32 with the fast
+// exponential and reciprocal (a few fp32 ulps more).
+__device__ __forceinline__ float erfc_as(float x) {
+    const float t = __fdividef(1.f, fmaf(0.3275911f, x, 1.f));
+    float q = fmaf(1.061405429f, t, -1.453152027f);
+    q = fmaf(q, t, 1.421413741f);
+    q = fmaf(q, t, -0.284496736f);
+    q = fmaf(q, t, 0.254829592f);
+    return q * t * __expf(-x * x);
+}
+
+// v * Phi(v), Phi the standard normal distribution function:
+// Phi(v) = erfc(-v / sqrt 2) / 2, i.e. 1 - erfc(|v| / sqrt 2) / 2 for v >= 0
+// and erfc(|v| / sqrt 2) / 2 for v < 0 (no cancellation in the negative tail).
+__device__ __forceinline__ float gelu_erf(float v) {
+    const float h = 0.5f * erfc_as(fabsf(v) * 0.7071067811865476f);
+    return v * (v >= 0.f ? 1.f - h : h);
+}
+
 __device__ __forceinline__ float activate(float v, int act) {
     switch (act) {
         case DWCONV_ACT_RELU: return fmaxf(v, 0.f);
         case DWCONV_ACT_RELU6: return fminf(fmaxf(v, 0.f), 6.f);
-        case DWCONV_ACT_SILU: return v / (1.f + expf(-v));                        // v * sigmoid(v)
-        case DWCONV_ACT_GELU: return 0.5f * v * (1.f + erff(v * 0.7071067811865476f));  // v * Phi(v)
+        case DWCONV_ACT_SILU: return __fdividef(v, 1.f + __expf(-v));  // v * sigmoid(v)
+        case DWCONV_ACT_GELU: return gelu_erf(v);
         default: return v;
     }
 }
@@ -168,15 +191,24 @@ __device__ __forceinline__ float apply(Affine a, float v, int act) { return acti
 // Calls f(std::integral_constant<int, act>{}) so that loops over many values
 // see the activation as a compile-time constant (one branch per loop, not per
 // value).
-template <typename F>
+// With LIGHT, only the piecewise-linear activations (none, ReLU, ReLU6) are
+// compiled in: for instances the host calls with no other.
+template <bool LIGHT = false, typename F>
 __device__ __forceinline__ void with_act(int act, F &&f) {
     switch (act) {
         case DWCONV_ACT_RELU: f(std::integral_constant<int, DWCONV_ACT_RELU>{}); break;
         case DWCONV_ACT_RELU6: f(std::integral_constant<int, DWCONV_ACT_RELU6>{}); break;
-        case DWCONV_ACT_SILU: f(std::integral_constant<int, DWCONV_ACT_SILU>{}); break;
-        case DWCONV_ACT_GELU: f(std::integral_constant<int, DWCONV_ACT_GELU>{}); break;
+        case DWCONV_ACT_SILU:
+            if constexpr (!LIGHT) f(std::integral_constant<int, DWCONV_ACT_SILU>{});
+            break;
+        case DWCONV_ACT_GELU:
+            if constexpr (!LIGHT) f(std::integral_constant<int, DWCONV_ACT_GELU>{});
+            break;
         default: f(std::integral_constant<int, DWCONV_ACT_NONE>{}); break;
     }
+}
+__host__ __device__ inline bool act_is_light(int act) {
+    return act == DWCONV_ACT_NONE || act == DWCONV_ACT_RELU || act == DWCONV_ACT_RELU6;
 }
 
 // A channel pair of a 16-bit type packed in one 32-bit word <-> float2.
@@ -195,6 +227,44 @@ template <> __device__ __forceinline__ unsigned pack2<__half>(float2 v) {
 template <> __device__ __forceinline__ unsigned pack2<__nv_bfloat16>(float2 v) {
     const __nv_bfloat162 h = __float22bfloat162_rn(v);
     return *reinterpret_cast<const unsigned *>(&h);
+}
+
+// Packed max(v, 0) and min(v, 6) on a pair of 16-bit values.  Rounding is
+// monotonic and 0 and 6 are exact in both formats, so clamping after the
+// rounding gives the rounding of the clamped fp32 value.
+template <typename T> __device__ __forceinline__ unsigned clamp_packed(unsigned v, bool six);
+template <> __device__ __forceinline__ unsigned clamp_packed<__half>(unsigned v, bool six) {
+    __half2 h = __hmax2(*reinterpret_cast<const __half2 *>(&v), __float2half2_rn(0.f));
+    if (six) h = __hmin2(h, __float2half2_rn(6.f));
+    return *reinterpret_cast<const unsigned *>(&h);
+}
+template <> __device__ __forceinline__ unsigned clamp_packed<__nv_bfloat16>(unsigned v, bool six) {
+    __nv_bfloat162 h = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&v), __float2bfloat162_rn(0.f));
+    if (six) h = __hmin2(h, __float2bfloat162_rn(6.f));
+    return *reinterpret_cast<const unsigned *>(&h);
+}
+
+// BN+Act prologue on a packed pair of 16-bit values x: round_T(act(s x + t))
+// per half (s, t per half), the affine map as one packed fp32 FMA.
+template <typename T, int A>
+__device__ __forceinline__ unsigned prologue_packed(unsigned v, float2 s, float2 t) {
+    float2 f = __ffma2_rn(unpack2<T>(v), s, t);
+    if constexpr (A == DWCONV_ACT_SILU || A == DWCONV_ACT_GELU) {
+        f.x = activate(f.x, A);
+        f.y = activate(f.y, A);
+    }
+    unsigned r = pack2<T>(f);
+    if constexpr (A == DWCONV_ACT_RELU || A == DWCONV_ACT_RELU6) r = clamp_packed<T>(r, A == DWCONV_ACT_RELU6);
+    return r;
+}
+
+// The same on an fp32 pair.
+template <int A>
+__device__ __forceinline__ float2 prologue_f32(float2 v, float2 s, float2 t) {
+    float2 f = __ffma2_rn(v, s, t);
+    f.x = activate(f.x, A);
+    f.y = activate(f.y, A);
+    return f;
 }
 
 // ---- launchers (each returns the launch's cudaError_t) -----------------------

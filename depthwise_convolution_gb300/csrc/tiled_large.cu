@@ -347,7 +347,10 @@ cudaError_t by_width(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     if (p.FW == 31 && !p.fz.pre() && !p.fz.post()) return p.flip ? run<T, TH, TW, MAXR, 31, true>(p, dt, st) : run<T, TH, TW, MAXR, 31, false>(p, dt, st);
 #endif
     if (p.fz.pre()) return cudaErrorNotSupported;
-    if (p.fz.post()) return p.flip ? cudaErrorNotSupported : run<T, TH, TW, MAXR, 0, false, true>(p, dt, st);
+    // Nine warps per CTA put three on one SM sub-partition, whose register
+    // file holds 16384: at most 170 registers per thread.
+    constexpr int kMaxR = MAXR < 168 ? MAXR : 168;
+    if (p.fz.post()) return p.flip ? cudaErrorNotSupported : run<T, TH, TW, kMaxR, 0, false, true>(p, dt, st);
     return p.flip ? run<T, TH, TW, MAXR, 0, true>(p, dt, st) : run<T, TH, TW, MAXR, 0, false>(p, dt, st);
 }
 

@@ -202,33 +202,58 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB>::MINB))
         // outside the input are padding of x' and stay zero.
         auto transpose = [&](auto pre) {
             constexpr int PA = decltype(pre)::value;  // activation, or -1: no prologue
-            Affine a[4];
+            float2 s2[4], t2[4];
+            unsigned cmask = 0;  // bit 2i + e: column 8i + 2t4 + e lies inside the input
             if constexpr (PA >= 0) {
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int c = cur.ctile * kCh + 8 * m + gq;
-                    a[m] = c < p.C ? affine_in(p.fz, c) : Affine{1.f, 0.f};
+                    const Affine a = c < p.C ? affine_in(p.fz, c) : Affine{1.f, 0.f};
+                    s2[m] = make_float2(a.s, a.s);
+                    t2[m] = make_float2(a.t, a.t);
                 }
-            }
-            const int ih0 = cur.band * C::OTH - p.pad_h, iw0 = cur.twi * C::OTW - p.pad_w + 2 * t4;
-            for (int b = warp; b < C::TR * (C::SW / 8); b += kMThreads / 32) {
-                const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
-                const unsigned src = s_buf + swz((unsigned)((row * C::SW + col0 + tr) * kPB + 16 * tj));
-                unsigned v[4];
-                ldsm_x4_trans(v[0], v[1], v[2], v[3], src);
-                if constexpr (PA >= 0) {
-                    const int img = row / C::HRI, ih = ih0 + row - img * C::HRI, iw = iw0 + col0;
-                    const bool rok = ih >= 0 && ih < p.Hs && cur.group * NI + img < p.N;
-                    const bool ok0 = rok && iw >= 0 && iw < p.Ws, ok1 = rok && iw + 1 >= 0 && iw + 1 < p.Ws;
+                const int iw0 = cur.twi * C::OTW - p.pad_w + 2 * t4;
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        float2 f = unpack2<T>(v[m]);
-                        f.x = ok0 ? activate(fmaf(a[m].s, f.x, a[m].t), PA) : 0.f;
-                        f.y = ok1 ? activate(fmaf(a[m].s, f.y, a[m].t), PA) : 0.f;
-                        v[m] = pack2<T>(f);
+                for (int i = 0; i < C::SW / 8; ++i)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int iw = iw0 + 8 * i + e;
+                        cmask |= (iw >= 0 && iw < p.Ws ? 1u : 0u) << (2 * i + e);
                     }
+            }
+            const int ih0 = cur.band * C::OTH - p.pad_h;
+            constexpr int kSteps = C::TR * (C::SW / 8), kStride = kMThreads / 32;
+            auto src = [&](int b) {
+                const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
+                return s_buf + swz((unsigned)((row * C::SW + col0 + tr) * kPB + 16 * tj));
+            };
+            auto dst = [&](int b) {
+                const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
+                return t_addr + 2u * ((8 * tj + tr) * C::CS + row * C::RS + col0);
+            };
+            if constexpr (PA < 0) {
+                for (int b = warp; b < kSteps; b += kStride) {
+                    const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
+                    unsigned v[4];
+                    ldsm_x4_trans(v[0], v[1], v[2], v[3],
+                                  s_buf + swz((unsigned)((row * C::SW + col0 + tr) * kPB + 16 * tj)));
+                    stsm_x4(t_addr + 2u * ((8 * tj + tr) * C::CS + row * C::RS + col0), v[0], v[1], v[2], v[3]);
                 }
-                stsm_x4(t_addr + 2u * ((8 * tj + tr) * C::CS + row * C::RS + col0), v[0], v[1], v[2], v[3]);
+            } else {
+                // (Measured on GB300: issuing the next step's load before this
+                // step's arithmetic, or skipping all-padding steps, is slower.)
+                for (int b = warp; b < kSteps; b += kStride) {
+                    unsigned v[4];
+                    ldsm_x4_trans(v[0], v[1], v[2], v[3], src(b));
+                    const int row = b / (C::SW / 8), chunk = b % (C::SW / 8);
+                    const int img = row / C::HRI, ih = ih0 + row - img * C::HRI;
+                    const bool rok = ih >= 0 && ih < p.Hs && cur.group * NI + img < p.N;
+                    const unsigned m2 = rok ? (cmask >> (2 * chunk)) & 3u : 0u;
+                    const unsigned keep = (m2 & 1u ? 0x0000FFFFu : 0u) | (m2 & 2u ? 0xFFFF0000u : 0u);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) v[m] = prologue_packed<T, PA>(v[m], s2[m], t2[m]) & keep;
+                    stsm_x4(dst(b), v[0], v[1], v[2], v[3]);
+                }
             }
         };
         if (FUSE && p.fz.pre())

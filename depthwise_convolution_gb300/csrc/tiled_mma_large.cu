@@ -155,30 +155,58 @@ __global__ void __launch_bounds__(kLThreads, 1)
         // the input are padding of x' and stay zero.
         auto transpose = [&](auto pre) {
             constexpr int PA = decltype(pre)::value;  // activation, or -1: no prologue
-            Affine a{1.f, 0.f};
+            float2 s2 = make_float2(1.f, 1.f), t2 = make_float2(0.f, 0.f);
+            unsigned cmask = 0;  // bit 2i + e: column 8i + 2t4 + e lies inside the input
             if constexpr (PA >= 0) {
                 const int c = cur.ctile * kLCh + gq;
-                if (c < p.C) a = affine_in(p.fz, c);
+                if (c < p.C) {
+                    const Affine a = affine_in(p.fz, c);
+                    s2 = make_float2(a.s, a.s);
+                    t2 = make_float2(a.t, a.t);
+                }
+                static_assert(C::CB <= 16, "column mask of 32 bits");
+                const int iw0 = cur.twi * C::OTW - p.pad_w + 2 * t4;
+#pragma unroll
+                for (int i = 0; i < C::CB; ++i)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int iw = iw0 + 8 * i + e;
+                        cmask |= (iw >= 0 && iw < p.Ws ? 1u : 0u) << (2 * i + e);
+                    }
             }
-            for (int m0 = warp * 4; m0 < C::HR * C::CB; m0 += kLThreads / 8) {
-                const int m = min(m0 + tj, C::HR * C::CB - 1);
-                const int row = m / C::CB, col0 = (m % C::CB) * 8;
-                unsigned v[4];
-                ldsm_x4_trans(v[0], v[1], v[2], v[3], s_addr + (unsigned)((row * C::SW + col0 + tr) * 16));
-                if constexpr (PA >= 0) {
+            constexpr int kBlocks = C::HR * C::CB, kStride = kLThreads / 8;
+            auto src = [&](int m0) {
+                const int m = min(m0 + tj, kBlocks - 1);
+                return s_addr + (unsigned)(((m / C::CB) * C::SW + (m % C::CB) * 8 + tr) * 16);
+            };
+            auto dst = [&](int m0) {
+                const int m = min(m0 + tj, kBlocks - 1);
+                return t_addr + 2u * (tr * C::CS + (m / C::CB) * C::RS + (m % C::CB) * 8);
+            };
+            if constexpr (PA < 0) {
+                for (int m0 = warp * 4; m0 < kBlocks; m0 += kStride) {
+                    const int m = min(m0 + tj, kBlocks - 1);
+                    const int row = m / C::CB, col0 = (m % C::CB) * 8;
+                    unsigned v[4];
+                    ldsm_x4_trans(v[0], v[1], v[2], v[3], s_addr + (unsigned)((row * C::SW + col0 + tr) * 16));
+                    stsm_x4(t_addr + 2u * (tr * C::CS + row * C::RS + col0), v[0], v[1], v[2], v[3]);
+                }
+            } else {
+                for (int m0 = warp * 4; m0 < kBlocks; m0 += kStride) {
+                    unsigned v[4];
+                    ldsm_x4_trans(v[0], v[1], v[2], v[3], src(m0));
+                    // Blocks m0..m0+3 (clamped to the last): row r, column chunk ch.
+                    int r = m0 / C::CB, ch = m0 - r * C::CB;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int mm = min(m0 + j, C::HR * C::CB - 1);
-                        const int ih = cur.band * C::OTH - p.pad_h + mm / C::CB;
-                        const int iw = cur.twi * C::OTW - p.pad_w + (mm % C::CB) * 8 + 2 * t4;
-                        const bool rok = ih >= 0 && ih < p.Hs;
-                        float2 f = unpack2<T>(v[j]);
-                        f.x = rok && iw >= 0 && iw < p.Ws ? activate(fmaf(a.s, f.x, a.t), PA) : 0.f;
-                        f.y = rok && iw + 1 >= 0 && iw + 1 < p.Ws ? activate(fmaf(a.s, f.y, a.t), PA) : 0.f;
-                        v[j] = pack2<T>(f);
+                        if (j > 0 && m0 + j < kBlocks && ++ch == C::CB) ch = 0, ++r;
+                        const int ih = cur.band * C::OTH - p.pad_h + r;
+                        const unsigned m2 = ih >= 0 && ih < p.Hs ? (cmask >> (2 * ch)) & 3u : 0u;
+                        const unsigned keep = (m2 & 1u ? 0x0000FFFFu : 0u) | (m2 & 2u ? 0xFFFF0000u : 0u);
+                        v[j] = prologue_packed<T, PA>(v[j], s2, t2) & keep;
                     }
+                    stsm_x4(dst(m0), v[0], v[1], v[2], v[3]);
                 }
-                stsm_x4(t_addr + 2u * (tr * C::CS + row * C::RS + col0), v[0], v[1], v[2], v[3]);
             }
         };
         if (FUSE && p.fz.pre())

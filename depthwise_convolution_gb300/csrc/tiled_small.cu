@@ -57,9 +57,10 @@ size_t smem_cap() {
 
 
 // FUSE: the BN+Act prologue and the affine+activation epilogue of the fused
-// forward pass (Flash-DWC §5.2) are compiled in; separate instances, so that
-// the plain passes keep their own register allocation.
-template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS, bool FUSE>
+// forward pass (Flash-DWC §5.2) are compiled in -- 1: piecewise-linear
+// activations only, 2: all; separate instances, so that the plain passes
+// keep their own register allocation.
+template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS, int FUSE>
 __global__ void __launch_bounds__(kThreads, MINB)
     tiled_small_kernel(const __grid_constant__ CUtensorMap halo_map, TiledConv p, Geo g, unsigned *err) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -123,23 +124,33 @@ __global__ void __launch_bounds__(kThreads, MINB)
             T *hb = reinterpret_cast<T *>(smem_raw + (k & 1) * buf_stride);
             const Affine a0 = cvalid ? affine_in(p.fz, c) : Affine{1.f, 0.f};
             const Affine a1 = cvalid ? affine_in(p.fz, c + 1) : Affine{1.f, 0.f};
-            with_act(p.fz.in_act, [&](auto act) {
+            const float2 s2 = make_float2(a0.s, a1.s), t2 = make_float2(a0.t, a1.t);
+            // Halo columns [c_lo, c_hi) lie inside the input.
+            const int col_in = cur.twi * tile_cols - p.pad_w;
+            const int c_lo = min(max(-col_in, 0), g.HW), c_hi = max(min(p.Ws - col_in, g.HW), c_lo);
+            with_act<FUSE == 1>(p.fz.in_act, [&](auto act) {
                 constexpr int A = decltype(act)::value;
+#pragma unroll 1
                 for (int rr = t; rr < g.NI * g.HH; rr += kTiles) {
                     const int im = rr / g.HH, r = rr - im * g.HH;
                     const int ih = cur.band * tile_rows - p.pad_h + r;
                     const bool rok = ih >= 0 && ih < p.Hs && cur.group * g.NI + im < p.N;
                     T *row = hb + rr * g.HW * 32 + 2 * cp;
-                    for (int col = 0; col < g.HW; ++col) {
-                        const int iw = cur.twi * tile_cols - p.pad_w + col;
-                        float2 v = make_float2(0.f, 0.f);
-                        if (rok && iw >= 0 && iw < p.Ws) {
-                            v = Pair<T>::load(row + col * 32);
-                            v.x = activate(fmaf(a0.s, v.x, a0.t), A);
-                            v.y = activate(fmaf(a1.s, v.y, a1.t), A);
+                    const int lo = rok ? c_lo : g.HW, hi = rok ? c_hi : g.HW;
+#pragma unroll 1
+                    for (int col = 0; col < lo; ++col) Pair<T>::store(row + col * 32, make_float2(0.f, 0.f));
+#pragma unroll 4
+                    for (int col = lo; col < hi; ++col) {
+                        if constexpr (sizeof(T) == 4) {
+                            float2 *q = reinterpret_cast<float2 *>(row + col * 32);
+                            *q = prologue_f32<A>(*q, s2, t2);
+                        } else {
+                            unsigned *q = reinterpret_cast<unsigned *>(row + col * 32);
+                            *q = prologue_packed<T, A>(*q, s2, t2);
                         }
-                        Pair<T>::store(row + col * 32, v);
                     }
+#pragma unroll 1
+                    for (int col = hi; col < g.HW; ++col) Pair<T>::store(row + col * 32, make_float2(0.f, 0.f));
                 }
             });
             // The generic-proxy writes come before this buffer's next TMA
@@ -190,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (FUSE && p.fz.post() && cvalid) {
             // Epilogue: per-channel affine map and activation on the fp32 sums.
             const Affine a0 = affine_out(p.fz, c), a1 = affine_out(p.fz, c + 1);
-            with_act(p.fz.out_act, [&](auto act) {
+            with_act<FUSE == 1>(p.fz.out_act, [&](auto act) {
 #pragma unroll
                 for (int th = 0; th < TH; ++th)
 #pragma unroll
@@ -236,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
 }
 
-template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS, bool FUSE = false>
+template <typename T, int FH, int FW, int TH, int TW, int MINB, int OS, int FUSE = 0>
 cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     auto kern = tiled_small_kernel<T, FH, FW, TH, TW, MINB, OS, FUSE>;
     const Geo g = make_geo(p, TH, TW, sizeof(T), false, smem_cap<T>());
@@ -275,10 +286,20 @@ cudaError_t dispatch_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st
     if (p.out_step_h != 1 || p.out_step_w != 1) return cudaErrorNotSupported;
     if (p.fz.pre() || p.fz.post()) {
         if (p.flip) return cudaErrorNotSupported;
-        if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7, 1, true>(p, dt, st);
-        if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 1, true>(p, dt, st);
-        if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 1, true>(p, dt, st);
-        if (p.FH == 3 && p.FW == 5) return run<T, 3, 5, 4, 7, 3, 1, true>(p, dt, st);
+        // SiLU and GELU keep several values of their polynomial / exponential
+        // live per output: those instances are sized for one CTA less per SM
+        // (more registers per thread) so that nothing spills.
+        if (!act_is_light(p.fz.in_act) || !act_is_light(p.fz.out_act)) {
+            if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7 - 1, 1, 2>(p, dt, st);
+            if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 1, 1, 2>(p, dt, st);
+            if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 2, 1, 2>(p, dt, st);
+            if (p.FH == 3 && p.FW == 5) return run<T, 3, 5, 4, 7, 2, 1, 2>(p, dt, st);
+            return cudaErrorNotSupported;
+        }
+        if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7, 1, 1>(p, dt, st);
+        if (p.FH == 5 && p.FW == 5) return run<T, 5, 5, 4, 7, 2, 1, 1>(p, dt, st);
+        if (p.FH == 3 && p.FW == 3) return run<T, 3, 3, 4, 7, 3, 1, 1>(p, dt, st);
+        if (p.FH == 3 && p.FW == 5) return run<T, 3, 5, 4, 7, 3, 1, 1>(p, dt, st);
         return cudaErrorNotSupported;
     }
     if (p.FH == 7 && p.FW == 7) return run<T, 7, 7, TH7, TW7, MB7, 1>(p, dt, st);

@@ -237,7 +237,10 @@ dwconv_status dwconv_bwd_filter_2d(int N, int H, int W, int C, int FH, int FW, i
  * tensor the unfused BN+Act layer would have written) and round_T the
  * rounding to the storage type (none for fp32): x' holds exactly what the
  * unfused layer would store.  The affine maps are one fp32 fused
- * multiply-add; the activations are evaluated in fp32.
+ * multiply-add; the activations are evaluated in fp32 (SiLU with the fast
+ * exponential and reciprocal, GELU through the erfc approximation of
+ * Abramowitz & Stegun 7.1.26, |error| <= 1.5e-7: both within 1e-6 |v| + 1e-7
+ * of the exact function).
  * in_scale, in_shift, out_scale, out_shift: float [C] device vectors, each
  * nullable (NULL scale = 1, NULL shift = 0); *_act a dwconv_activation.
  * With every one of them NULL / DWCONV_ACT_NONE the call is dwconv_fwd_2d.

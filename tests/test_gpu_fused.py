@@ -98,3 +98,28 @@ def test_prologue_padding_is_zero_on_device():
         cols = torch.tensor([2.0] + [3.0] * (W - 2) + [2.0])
         expect = (rows[:, None] * cols[None, :])[None, :, :, None].expand(1, H, W, 32)
         assert torch.equal(y.float().cpu(), expect), (dt, ops.dwconv_last_kernel())
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu", "relu", "relu6"])
+@pytest.mark.parametrize("F", [1, 3])
+def test_activation_accuracy_fp32(act, F):
+    """The fp32 activations on their own (a filter that passes x through:
+    1x1 on the direct kernel, the centre tap of a 3x3 on the tiled one), as
+    epilogue and as prologue, against the float64 definitions: within
+    1e-6 |v| + 1e-7 (SiLU with the fast exponential and reciprocal; GELU
+    with Abramowitz & Stegun 7.1.26, |erf error| <= 1.5e-7)."""
+    import numpy as np
+    import oracle
+    from depthwise_convolution_gb300 import ops
+    C, H, W = 32, 48, 64
+    v = torch.linspace(-14.0, 14.0, H * W * C, dtype=torch.float64).reshape(1, H, W, C)
+    x = v.float().cuda()
+    w = torch.zeros(F, F, C, device="cuda")
+    w[F // 2, F // 2] = 1.0
+    ref = oracle.activation(v.float().double().numpy(), act)
+    bound = 1e-6 * np.abs(v.numpy()) + 1e-7
+    for mode in ("post", "pre"):
+        kw = {"out_act": act} if mode == "post" else {"in_act": act}
+        y = ops.dwconv_fwd_fused(x, w, pad=F // 2, **kw)
+        err = np.abs(y.double().cpu().numpy() - ref)
+        assert np.all(err <= bound), (mode, ops.dwconv_last_kernel(), float((err - bound).max()))
