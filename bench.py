@@ -505,6 +505,34 @@ def main():
             except Exception as e:  # report, do not hide
                 fusion[name] = {"error": str(e)[:200]}
 
+    # Opt-in hybrid-accumulation weight gradient (fp16 data): time against
+    # the exact pass on the same buffers.
+    variants = {}
+    if rank == 0 and ws == 1 and not args.no_sweep and wl.dtype == "fp16" and "wgrad" in wl.passes:
+        try:
+            stream = torch.cuda.current_stream()
+            res = {}
+            for name, ha in (("exact", False), ("half_accumulate", True)):
+                fn = lambda: ops.dwconv_bwd_filter(layer.x, layer.dy, wl.FH, wl.FW, wl.stride, wl.dilation,  # noqa
+                                                   wl.pad, out=layer.dw, workspace=layer.ws, half_accumulate=ha)
+                for _ in range(3):
+                    fn()
+                torch.cuda.synchronize()
+                kern = ops.dwconv_last_kernel()
+                n = max(20, args.steps // 10)
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+                for i in range(n):
+                    flush.fill_(i & 0xFF)
+                    ev[i][0].record(stream)
+                    fn()
+                    ev[i][1].record(stream)
+                torch.cuda.synchronize()
+                res[name] = {"ms": round(statistics.mean(a.elapsed_time(b) for a, b in ev), 4), "kernel": kern}
+            res["speedup"] = round(res["exact"]["ms"] / res["half_accumulate"]["ms"], 3)
+            variants["wgrad"] = res
+        except Exception as e:  # report, do not hide
+            variants["wgrad"] = {"error": str(e)[:200]}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         v, cores, sample = oracle_sample(wl)
@@ -520,7 +548,8 @@ def main():
                        "l2": "flushed before each timed step (256 MiB write)",
                        "parallelism": f"{ws} independent replica(s)"},
             "passes": passes, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-            "clocks": sampler.summary(t0, t1), "cpu_baseline": cpu, "sweep": sweep, "fusion": fusion}
+            "clocks": sampler.summary(t0, t1), "cpu_baseline": cpu, "sweep": sweep, "fusion": fusion,
+            "variants": variants}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

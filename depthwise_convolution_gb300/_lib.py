@@ -39,6 +39,8 @@ SIGNATURES = {
     "dwconv_bwd_filter_2d": (_I, [_I] * 12 + [_I, _P, _P, _P, _P, _SZ, _P]),
     "dwconv_fwd_fused": (_I, [_I] * 9 + [_I, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P]),
     "dwconv_fwd_fused_2d": (_I, [_I] * 12 + [_I, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P]),
+    "dwconv_bwd_filter_ha": (_I, [_I] * 9 + [_I, _P, _P, _P, _P, _SZ, _P]),
+    "dwconv_bwd_filter_ha_2d": (_I, [_I] * 12 + [_I, _P, _P, _P, _P, _SZ, _P]),
     "dwconv_launch_count": (ctypes.c_ulonglong, []),
     "dwconv_last_kernel": (ctypes.c_char_p, []),
 }

@@ -310,6 +310,7 @@ struct TiledConv {
     // are written with zeros.
     int OHf, OWf, OHs, OWs, out_step_h, out_step_w, out_off_h, out_off_w, zero_phases;
     Fuse fz;               // forward only; all null / zero: plain convolution
+    int half_accumulate;   // weight gradient, fp16 data: fp16 partial sums per unit (opt-in)
 };
 
 // Returns cudaErrorNotSupported when no tiled instance covers the request.

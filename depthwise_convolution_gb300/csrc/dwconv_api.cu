@@ -358,16 +358,21 @@ size_t dwconv_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int 
                                                dtype);
 }
 
-dwconv_status dwconv_bwd_filter_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
-                                   int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
-                                   const void *x, const void *dy, float *dw, void *workspace,
-                                   size_t workspace_bytes, dwconv_stream stream) {
+}  // extern "C"
+
+namespace dwc {
+namespace {
+
+dwconv_status bwd_filter_impl(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                              int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                              const void *x, const void *dy, float *dw, void *workspace, size_t workspace_bytes,
+                              int half_accumulate, dwconv_stream stream) {
     if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
     Shape s;
     dwconv_status st =
         make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s);
     if (st != DWCONV_OK) return st;
-    if (dtype == DWCONV_INT8) return DWCONV_ERR_UNSUPPORTED;
+    if (dtype == DWCONV_INT8 || (half_accumulate && dtype != DWCONV_FP16)) return DWCONV_ERR_UNSUPPORTED;
     if (!x || !dy || !dw) return DWCONV_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     if (!aligned(x, es) || !aligned(dy, es) || !aligned(dw, 4)) return DWCONV_ERR_MISALIGNED;
@@ -380,13 +385,44 @@ dwconv_status dwconv_bwd_filter_2d(int N, int H, int W, int C, int FH, int FW, i
 
     TiledConv p;
     if (wgrad_tiled_params(s, dtype, x, dy, dw, p) && aligned(x, 16) && aligned(dy, 16)) {
+        p.half_accumulate = half_accumulate;
         cudaError_t e = launch_tiled_wgrad(p, dtype, part, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
+    // Shapes without a tiled instance take the exact fp32 path, also for the
+    // hybrid-accumulation entry point (its bound holds a fortiori).
     const int Z = wgrad_slices(s);
     cudaError_t e = launch_wgrad_direct(s, dtype, x, dy, part, Z, cs);
     if (e != cudaSuccess) return DWCONV_ERR_CUDA;
     return cuda_status(launch_wgrad_reduce(part, Z, (long long)FH * FW * C, dw, cs));
+}
+
+}  // namespace
+}  // namespace dwc
+
+extern "C" {
+
+dwconv_status dwconv_bwd_filter_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                                   int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                                   const void *x, const void *dy, float *dw, void *workspace,
+                                   size_t workspace_bytes, dwconv_stream stream) {
+    return bwd_filter_impl(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, dtype, x,
+                           dy, dw, workspace, workspace_bytes, 0, stream);
+}
+
+dwconv_status dwconv_bwd_filter_ha_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                                      int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                                      const void *x, const void *dy, float *dw, void *workspace,
+                                      size_t workspace_bytes, dwconv_stream stream) {
+    return bwd_filter_impl(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, dtype, x,
+                           dy, dw, workspace, workspace_bytes, 1, stream);
+}
+
+dwconv_status dwconv_bwd_filter_ha(int N, int H, int W, int C, int FH, int FW, int stride, int dilation, int pad,
+                                   dwconv_dtype dtype, const void *x, const void *dy, float *dw, void *workspace,
+                                   size_t workspace_bytes, dwconv_stream stream) {
+    return dwconv_bwd_filter_ha_2d(N, H, W, C, FH, FW, stride, stride, dilation, dilation, pad, pad, dtype, x, dy,
+                                   dw, workspace, workspace_bytes, stream);
 }
 
 dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int stride, int dilation, int pad,

@@ -48,10 +48,20 @@ using namespace tiled;
 #define DWCONV_W_FFMA2_FH 5
 #endif
 
+// CTAs per SM the 7x7 hybrid-accumulation instance is sized for (its fp16
+// partial sums add FH*FW registers to the fp32 accumulators).
+#ifndef DWCONV_WHA_MINB
+#define DWCONV_WHA_MINB 3
+#endif
+
 // Work is split into about this many CTAs (resident CTAs x 152 SMs of a GB300).
 constexpr int kTargetCtas(bool k16) { return 152 * (k16 ? DWCONV_W16_MINB : 2); }
 
-template <typename T, int FH, int FW, int TH, int TW, int MINB>
+// HA (fp16 data only): hybrid accumulation, the opt-in of Flash-DWC §5.1
+// "mixed accumulation" -- each thread's TH x TW products of a unit are summed
+// per tap in fp16 (packed HFMA2, two channels per instruction), and that
+// partial sum is added to the fp32 accumulator once per unit.
+template <typename T, int FH, int FW, int TH, int TW, int MINB, bool HA = false>
 __global__ void __launch_bounds__(kThreads, MINB)
     tiled_wgrad_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap dy_map,
                        TiledConv p, Geo g, float *__restrict__ part, int Zc, unsigned *err) {
@@ -115,28 +125,66 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const T *sx = reinterpret_cast<const T *>(cur) + img_l * halo_elems;
         const T *sy = reinterpret_cast<const T *>(cur + align128(hb)) + img_l * otile_elems;
         const int r0 = rt * TH, j0 = ct * TW;
-        using M = typename std::conditional<sizeof(T) == 2 && FH == DWCONV_W_FFMA2_FH, MacW<T>, Mac<T>>::type;
+        using M = typename std::conditional<!HA && sizeof(T) == 2 && FH == DWCONV_W_FFMA2_FH, MacW<T>,
+                                            Mac<T>>::type;
         typename M::V dyv[TH][TW];
 #pragma unroll
         for (int th = 0; th < TH; ++th)
 #pragma unroll
             for (int tw = 0; tw < TW; ++tw)
                 dyv[th][tw] = M::load(sy + ((r0 + th) * tile_cols + j0 + tw) * 32 + 2 * cp);
+        if constexpr (HA) {
+            static_assert(std::is_same<T, __half>::value, "hybrid accumulation is for fp16 data");
+            __half2 part_h[FH][FW];
 #pragma unroll
-        for (int r = 0; r < TH + FH - 1; ++r) {
-            typename M::V xv[WW];
-            const T *srow = sx + ((r0 + r) * g.HW + j0) * 32 + 2 * cp;
+            for (int fh = 0; fh < FH; ++fh)
 #pragma unroll
-            for (int j = 0; j < WW; ++j) xv[j] = M::load(srow + j * 32);
+                for (int fw = 0; fw < FW; ++fw) part_h[fh][fw] = __float2half2_rn(0.f);
 #pragma unroll
-            for (int th = 0; th < TH; ++th) {
-                const int fh = r - th;
-                if (fh < 0 || fh >= FH) continue;
+            for (int r = 0; r < TH + FH - 1; ++r) {
+                __half2 xv[WW];
+                const T *srow = sx + ((r0 + r) * g.HW + j0) * 32 + 2 * cp;
 #pragma unroll
-                for (int fw = 0; fw < FW; ++fw)
+                for (int j = 0; j < WW; ++j) xv[j] = *reinterpret_cast<const __half2 *>(srow + j * 32);
 #pragma unroll
-                    for (int tw = 0; tw < TW; ++tw)
-                        M::fma(acc[fh][fw], dyv[th][tw], xv[tw + fw]);
+                for (int th = 0; th < TH; ++th) {
+                    const int fh = r - th;
+                    if (fh < 0 || fh >= FH) continue;
+#pragma unroll
+                    for (int fw = 0; fw < FW; ++fw)
+#pragma unroll
+                        for (int tw = 0; tw < TW; ++tw) {
+                            const unsigned d = dyv[th][tw];
+                            part_h[fh][fw] =
+                                __hfma2(*reinterpret_cast<const __half2 *>(&d), xv[tw + fw], part_h[fh][fw]);
+                        }
+                }
+            }
+#pragma unroll
+            for (int fh = 0; fh < FH; ++fh)
+#pragma unroll
+                for (int fw = 0; fw < FW; ++fw) {
+                    const float2 f = __half22float2(part_h[fh][fw]);
+                    acc[fh][fw].x += f.x;
+                    acc[fh][fw].y += f.y;
+                }
+        } else {
+#pragma unroll
+            for (int r = 0; r < TH + FH - 1; ++r) {
+                typename M::V xv[WW];
+                const T *srow = sx + ((r0 + r) * g.HW + j0) * 32 + 2 * cp;
+#pragma unroll
+                for (int j = 0; j < WW; ++j) xv[j] = M::load(srow + j * 32);
+#pragma unroll
+                for (int th = 0; th < TH; ++th) {
+                    const int fh = r - th;
+                    if (fh < 0 || fh >= FH) continue;
+#pragma unroll
+                    for (int fw = 0; fw < FW; ++fw)
+#pragma unroll
+                        for (int tw = 0; tw < TW; ++tw)
+                            M::fma(acc[fh][fw], dyv[th][tw], xv[tw + fw]);
+                }
             }
         }
         __syncthreads();  // this buffer is refilled by the copy issued next iteration
@@ -190,13 +238,13 @@ bool plan_geo(const TiledConv &p, Geo &g, int &Zc, size_t &smem) {
     return true;
 }
 
-template <typename T, int FH, int FW, int TH, int TW, int MINB>
+template <typename T, int FH, int FW, int TH, int TW, int MINB, bool HA = false>
 cudaError_t run(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st) {
     Geo g;
     int Zc;
     size_t smem;
     if (!plan_geo<T, FH, FW, TH, TW>(p, g, Zc, smem)) return cudaErrorNotSupported;
-    auto kern = tiled_wgrad_kernel<T, FH, FW, TH, TW, MINB>;
+    auto kern = tiled_wgrad_kernel<T, FH, FW, TH, TW, MINB, HA>;
     CUtensorMap halo_map, dy_map;
     if (!make_halo_map(&halo_map, p, g, dt, sizeof(T)) ||
         !make_tile_map(&dy_map, p.dy, p, g, TH, TW, dt, sizeof(T)))
@@ -205,7 +253,7 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t s
     if (e != cudaSuccess) return e;
     kern<<<g.ctiles * Zc, kThreads, smem, st>>>(halo_map, dy_map, p, g, part, Zc, device_error_word());
     note_launches(1);
-    note_kernel("tiled_wgrad");
+    note_kernel(HA ? "tiled_wgrad_ha" : "tiled_wgrad");
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_wgrad_reduce(part, Zc, (long long)p.FH * p.FW * p.C, static_cast<float *>(p.out), st);
@@ -227,6 +275,13 @@ cudaError_t dispatch(const TiledConv &p, dwconv_dtype dt, float *part, cudaStrea
     if (Zc_out) {  // planning only
         *Zc_out = Zc;
         return cudaSuccess;
+    }
+    if constexpr (std::is_same<T, __half>::value) {
+        if (p.half_accumulate) {
+            if (p.FH == 7) return run<T, 7, 7, TH7, TW7, DWCONV_WHA_MINB, true>(p, dt, part, st);
+            if (p.FH == 5) return run<T, 5, 5, 4, 7, 2, true>(p, dt, part, st);
+            return run<T, 3, 3, 4, 7, 3, true>(p, dt, part, st);
+        }
     }
     if (p.FH == 7) return run<T, 7, 7, TH7, TW7, MB7>(p, dt, part, st);
     if (p.FH == 5) return run<T, 5, 5, 4, 7, 2>(p, dt, part, st);

@@ -168,8 +168,10 @@ def dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation, pad, 
 
 
 def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, workspace=None,
-                      stream=None):
-    """dw [FH,FW,C] fp32 from x [N,H,W,C] and dy [N,OH,OW,C]."""
+                      stream=None, half_accumulate=False):
+    """dw [FH,FW,C] fp32 from x [N,H,W,C] and dy [N,OH,OW,C].  half_accumulate
+    (fp16 data only) calls dwconv_bwd_filter_ha: fp16 partial sums over short
+    sub-units, merged in fp32 (an opt-in with a looser error bound)."""
     N, H, W, C = x.shape
     dt = _code(x)
     if dy.dtype != x.dtype:
@@ -185,10 +187,12 @@ def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, work
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _lib.check(_lib.load().dwconv_bwd_filter_2d(
+    fn = _lib.load().dwconv_bwd_filter_ha_2d if half_accumulate else _lib.load().dwconv_bwd_filter_2d
+    _lib.check(fn(
         N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
         _dev(x, "x", 4), _dev(dy, "dy", 4), _dev(out, "out", 3),
-        workspace.data_ptr(), ws_bytes, _stream(stream)), "dwconv_bwd_filter")
+        workspace.data_ptr(), ws_bytes, _stream(stream)),
+        "dwconv_bwd_filter_ha" if half_accumulate else "dwconv_bwd_filter")
     return out
 
 

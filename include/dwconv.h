@@ -261,6 +261,32 @@ dwconv_status dwconv_fwd_fused(int N, int H, int W, int C, int FH, int FW, int s
                                dwconv_activation in_act, const void *w, const void *bias, const float *out_scale,
                                const float *out_shift, dwconv_activation out_act, void *y, dwconv_stream stream);
 
+/*
+ * Weight gradient with hybrid accumulation (Flash-DWC §5.1 "mixed
+ * accumulation", an opt-in): the long accumulation over N*OH*OW is split into
+ * short sub-units, each summed in fp16, and the sub-unit sums are merged in
+ * fp32.  Here a sub-unit is the products of one thread's output tile of one
+ * work unit (14 positions per tap for 7x7 filters, 28 for 3x3 and 5x5),
+ * accumulated with packed fp16 fused multiply-adds (two channels per
+ * instruction).  Error bound per dw element: gamma_L * sum |dy * x| with
+ * L <= 28 and fp16's unit roundoff u = 2^-11 (gamma_L = L u / (1 - L u),
+ * 1.39e-2 for L = 28), plus the fp32 merge; every fp16 partial sum must stay
+ * below 65504 in magnitude.
+ * Arguments, workspace (dwconv_bwd_filter_workspace_size_2d), layouts and
+ * errors as dwconv_bwd_filter_2d; DWCONV_FP16 only (other dtypes:
+ * DWCONV_ERR_UNSUPPORTED).  Shapes the tiled weight-gradient kernel does not
+ * cover run the exact fp32 path instead (dwconv_last_kernel says which ran:
+ * "tiled_wgrad_ha" for the hybrid kernel).
+ */
+dwconv_status dwconv_bwd_filter_ha_2d(int N, int H, int W, int C, int FH, int FW, int stride_h, int stride_w,
+                                      int dilation_h, int dilation_w, int pad_h, int pad_w, dwconv_dtype dtype,
+                                      const void *x, const void *dy, float *dw, void *workspace,
+                                      size_t workspace_bytes, dwconv_stream stream);
+/* dwconv_bwd_filter_ha_2d with the same stride, dilation and padding on both axes. */
+dwconv_status dwconv_bwd_filter_ha(int N, int H, int W, int C, int FH, int FW, int stride, int dilation, int pad,
+                                   dwconv_dtype dtype, const void *x, const void *dy, float *dw, void *workspace,
+                                   size_t workspace_bytes, dwconv_stream stream);
+
 /* A static, human-readable name for a status code. */
 const char *dwconv_status_string(dwconv_status status);
 
@@ -275,7 +301,7 @@ unsigned long long dwconv_launch_count(void);
  * string: "tiled_mma" (tensor-core Toeplitz, 16-bit 3x3/5x5/7x7),
  * "tiled_mma_large" (tensor-core Toeplitz, large 16-bit filters),
  * "tiled_small" / "tiled_large" (register-tiled FMA kernels), "tiled_wgrad"
- * (tiled weight gradient), "direct_fwd" / "direct_dgrad" / "direct_wgrad"
+ * (tiled weight gradient), "tiled_wgrad_ha" (its hybrid-accumulation form), "direct_fwd" / "direct_dgrad" / "direct_wgrad"
  * (one output per thread), or "none" before the first launch.  The host-side
  * dispatch sets it when it launches; it says nothing about completion.  For
  * reporting which kernel ran (e.g. against which roofline to measure it).

@@ -160,6 +160,19 @@ def test_python_fused_binding_checks_arguments():
         ops.dwconv_fwd_fused(x, w, in_act="relu")
 
 
+def test_half_accumulate_wgrad_validation(lib):
+    args = (2, 8, 8, 16, 3, 3, 1, 1, 1)
+    need = lib.dwconv_bwd_filter_workspace_size(*args, _lib.FP16)
+    before = lib.dwconv_launch_count()
+    for dt in (_lib.BF16, _lib.FP32, _lib.INT8):     # fp16 data only
+        assert lib.dwconv_bwd_filter_ha(*args, dt, A, A, A, A, need, None) == _lib.ERR_UNSUPPORTED
+    assert lib.dwconv_bwd_filter_ha(*args, _lib.FP16, A, A, A, A, need - 4, None) == _lib.ERR_INVALID_ARG
+    assert lib.dwconv_bwd_filter_ha(*args, _lib.FP16, None, A, A, A, need, None) == _lib.ERR_INVALID_ARG
+    assert lib.dwconv_bwd_filter_ha_2d(2, 8, 8, 16, 3, 3, 1, 1, 1, 1, 1, 1, _lib.FP16, A, A, A + 2, A, need,
+                                       None) == _lib.ERR_MISALIGNED
+    assert lib.dwconv_launch_count() == before
+
+
 def test_workspace_size_is_a_pure_function_of_the_shape(lib):
     args = (128, 56, 56, 96, 7, 7, 1, 1, 3)
     a = lib.dwconv_bwd_filter_workspace_size(*args, _lib.FP16)

@@ -1,0 +1,61 @@
+"""Hybrid-accumulation weight gradient (Flash-DWC §5.1 "mixed accumulation",
+opt-in, fp16 data) against the oracle.
+
+Bound per dw element, derived from the arithmetic: each fp16 sub-unit sum of
+L <= 28 products (one thread's output tile of a work unit) is computed with
+L fused multiply-adds rounding to fp16, so its error is at most
+gamma_L * sum |p| with gamma_L = L u / (1 - L u), u = 2^-11 (1.39e-2 for
+L = 28); the fp32 merge of the sub-unit sums stays within the fp32-accumulation
+bound of the exact path (2e-3 * mag).  Total: (gamma_28 + 2e-3) * mag.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from depthwise_convolution_gb300 import ops
+from parity import Guarded, random_inputs, to64
+
+pytestmark = pytest.mark.gpu
+
+U16 = 2.0 ** -11
+GAMMA_28 = 28 * U16 / (1 - 28 * U16)
+BOUND = GAMMA_28 + 2e-3
+
+CASES = [
+    (2, 20, 44, 32, 7, 7, 1, 1, 3),
+    (3, 17, 23, 40, 5, 5, 1, 1, 2),   # channel tail, ragged tiles
+    (2, 16, 16, 64, 3, 3, 1, 1, 1),
+    (2, 24, 24, 32, 3, 3, 2, 2, 2),   # stride 2 dilation 2: even sub-grid
+    (1, 9, 11, 8, 3, 3, 2, 1, 1),     # stride 2: exact fp32 path
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
+def test_half_accumulate_within_derived_bound(case):
+    N, H, W, C, FH, FW, S, D, P = case
+    d = random_inputs("fp16", N, H, W, C, FH, FW, S, D, P, seed=53)
+    x, dy = d["x"], d["dy"]
+    g = Guarded((FH, FW, C), torch.float32)
+    dw = ops.dwconv_bwd_filter(x.cuda(), dy.cuda(), FH, FW, S, D, P, out=g.t, half_accumulate=True)
+    ops.dwconv_check_device_errors()
+    g.check("wgrad_ha")
+    kernel = ops.dwconv_last_kernel()
+    ref, mag = oracle.wgrad(to64(x), to64(dy), FH, FW, S, D, P)
+    err = np.abs(to64(dw) - ref)
+    assert np.all(err <= BOUND * mag), (kernel, float((err / np.maximum(mag, 1e-30)).max()))
+    expect = "direct_wgrad" if S == 2 and D == 1 else "tiled_wgrad_ha"
+    assert kernel == expect
+
+
+def test_half_accumulate_is_deterministic_and_differs_from_exact():
+    N, H, W, C, FH, FW, S, D, P = 4, 28, 28, 64, 7, 7, 1, 1, 3
+    d = random_inputs("fp16", N, H, W, C, FH, FW, S, D, P, seed=59)
+    x, dy = d["x"].cuda(), d["dy"].cuda()
+    a = ops.dwconv_bwd_filter(x, dy, FH, FW, S, D, P, half_accumulate=True)
+    b = ops.dwconv_bwd_filter(x, dy, FH, FW, S, D, P, half_accumulate=True)
+    e = ops.dwconv_bwd_filter(x, dy, FH, FW, S, D, P)
+    assert torch.equal(a, b)
+    assert not torch.equal(a, e)   # fp16 partial sums really are in use
