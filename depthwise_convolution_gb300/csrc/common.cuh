@@ -311,7 +311,23 @@ struct TiledConv {
     int OHf, OWf, OHs, OWs, out_step_h, out_step_w, out_off_h, out_off_w, zero_phases;
     Fuse fz;               // forward only; all null / zero: plain convolution
     int half_accumulate;   // weight gradient, fp16 data: fp16 partial sums per unit (opt-in)
+    // Transposed view (strip filters taller than wide): the kernel's rows are
+    // the tensors' columns.  Hs, Ws, pad_h, pad_w, FH, FW, OHs, OWs are then
+    // given in the kernel's orientation (swapped); Hf, Wf, in_step_*, in_off_*,
+    // OHf, OWf, out_step_*, out_off_* keep describing memory, and w stays
+    // [FH_mem][FW_mem][C] = [FW][FH][C] of the kernel.  Only the large-filter
+    // kernels (tiled_large.cu, tiled_mma_large.cu) accept it.
+    int transpose;
 };
+
+// Byte strides of the taps' input sub-grid along the kernel's columns, rows and
+// images (the memory rows and columns exchange roles under p.transpose).
+inline void in_strides(const TiledConv &p, size_t es, uint64_t str[3]) {
+    const uint64_t col = (uint64_t)p.in_step_w * p.C * es, row = (uint64_t)p.in_step_h * p.Wf * p.C * es;
+    str[0] = p.transpose ? row : col;
+    str[1] = p.transpose ? col : row;
+    str[2] = (uint64_t)p.Hf * p.Wf * p.C * es;
+}
 
 // Returns cudaErrorNotSupported when no tiled instance covers the request.
 cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);

@@ -5,6 +5,8 @@
 #include <atomic>
 #include <climits>
 
+#include <utility>
+
 #include "common.cuh"
 #include "tma.cuh"
 
@@ -112,6 +114,24 @@ bool unit_subgrid(const Shape &s, TiledConv &p) {
     p.Hs = (s.H - rh + gh - 1) / gh; p.Ws = (s.W - rw + gw - 1) / gw;
     p.pad_h = (s.PH + rh) / gh; p.pad_w = (s.PW + rw) / gw;
     return true;
+}
+
+// Strip filters taller than wide (FW < 8 <= FH, e.g. 51 x 5 or 31 x 1): the
+// large-filter kernels walk filter rows and tile filter columns, so they take
+// the problem transposed -- rows and columns exchange roles in the kernel's
+// view (TiledConv::transpose) while the tensors stay where they are.
+cudaError_t launch_tall_strip(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    if (!(p.FW < 8 && p.FH >= 8) || p.zero_phases || p.out_step_h != 1 || p.out_step_w != 1)
+        return cudaErrorNotSupported;
+    TiledConv q = p;
+    q.transpose = 1;
+    std::swap(q.Hs, q.Ws);
+    std::swap(q.pad_h, q.pad_w);
+    std::swap(q.FH, q.FW);
+    std::swap(q.OHs, q.OWs);
+    cudaError_t e = launch_tiled_mma_large(q, dt, st);
+    if (e == cudaErrorNotSupported) e = launch_tiled_large(q, dt, st);
+    return e;
 }
 
 // wgrad split: slices of the N*OH*OW axis.  A pure function of the shape so
@@ -224,7 +244,8 @@ dwconv_status fwd_impl(int N, int H, int W, int C, int FH, int FW, int stride_h,
         p.OHf = s.OH; p.OWf = s.OW; p.OHs = s.OH; p.OWs = s.OW;
         p.out_step_h = p.out_step_w = 1; p.out_off_h = p.out_off_w = 0; p.zero_phases = 0;
         p.fz = fz;
-        cudaError_t e = launch_tiled_mma(p, dtype, cs);
+        cudaError_t e = launch_tall_strip(p, dtype, cs);
+        if (e == cudaErrorNotSupported) e = launch_tiled_mma(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma_large(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_small(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);
@@ -320,7 +341,8 @@ dwconv_status dwconv_bwd_data_2d(int N, int H, int W, int C, int FH, int FW, int
                 if (e != cudaErrorNotSupported) return cuda_status(e);
             }
         }
-        cudaError_t e = launch_tiled_mma(p, dtype, cs);
+        cudaError_t e = launch_tall_strip(p, dtype, cs);
+        if (e == cudaErrorNotSupported) e = launch_tiled_mma(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma_large(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_small(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);

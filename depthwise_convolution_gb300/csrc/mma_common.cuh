@@ -118,8 +118,8 @@ inline bool make_out_map(CUtensorMap *m, const TiledConv &p, dwconv_dtype dt, si
                          int swizzle) {
     const char *base = static_cast<const char *>(p.out) + ((size_t)p.out_off_h * p.OWf + p.out_off_w) * p.C * es;
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.OWs, (uint64_t)p.OHs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.out_step_w * p.C * es, (uint64_t)p.out_step_h * p.OWf * p.C * es,
-                             (uint64_t)p.OHf * p.OWf * p.C * es};
+    const uint64_t col = (uint64_t)p.out_step_w * p.C * es, row = (uint64_t)p.out_step_h * p.OWf * p.C * es;
+    const uint64_t str[3] = {p.transpose ? row : col, p.transpose ? col : row, (uint64_t)p.OHf * p.OWf * p.C * es};
     return encode_tmap_4d(m, dt, base, dims, str, box, swizzle);
 }
 

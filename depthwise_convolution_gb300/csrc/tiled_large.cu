@@ -265,7 +265,8 @@ __global__ void __maxnreg__(MAXR)
                 for (int tw = 0; tw < TW; ++tw) {
                     const int j = j0 + tw;
                     if (j >= p.OWs) break;
-                    Pair<T>::store(img + ((long long)i * p.OWf + j) * p.C, acc[th][tw]);
+                    const long long px = p.transpose ? (long long)j * p.OWf + i : (long long)i * p.OWf + j;
+                    Pair<T>::store(img + px * p.C, acc[th][tw]);
                 }
             }
         }
@@ -311,13 +312,16 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     const size_t es = sizeof(T);
     const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off_h * p.Wf + p.in_off_w) * p.C * es;
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.in_step_w * p.C * es, (uint64_t)p.in_step_h * p.Wf * p.C * es,
-                             (uint64_t)p.Hf * p.Wf * p.C * es};
+    uint64_t str[3];
+    in_strides(p, es, str);
     const uint32_t box[4] = {32, (uint32_t)g.HW, 1, (uint32_t)g.NI};
     // Filter [FH][FW][C] as a 4-D tensor with a unit outer dimension; one box =
     // the whole filter of a 32-channel slab.
     const uint64_t fdims[4] = {(uint64_t)p.C, (uint64_t)p.FW, (uint64_t)p.FH, 1};
-    const uint64_t fstr[3] = {(uint64_t)p.C * es, (uint64_t)p.FW * p.C * es, (uint64_t)p.FH * p.FW * p.C * es};
+    // Transposed view: the kernel's filter column fw is memory row fw, whose
+    // stride is FH (the memory width) * C elements.
+    const uint64_t fstr[3] = {(uint64_t)(p.transpose ? p.FH : 1) * p.C * es,
+                              (uint64_t)(p.transpose ? 1 : p.FW) * p.C * es, (uint64_t)p.FH * p.FW * p.C * es};
     const uint32_t fbox[4] = {32, (uint32_t)p.FW, (uint32_t)p.FH, 1};
     CUtensorMap row_map, filt_map;
     if (!encode_tmap_4d(&row_map, dt, base, dims, str, box) ||

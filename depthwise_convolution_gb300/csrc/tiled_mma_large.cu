@@ -1,6 +1,7 @@
 // Tensor-core forward pass and stride-1 input gradient for 16-bit data and
-// large filters (compiled filter heights 13 and 31, widths 8 to 41 columns),
-// maps at least 17 columns wide.
+// large filters (compiled: 13 and 31 rows, 8 to 41 columns; 5 rows, 42 to 57
+// columns, the strips of factorised large kernels, also taken transposed for
+// 42-57 x 5), maps at least 17 columns wide.
 //
 // The packing is the one of the small-filter kernel (Flash-DWC §4.2): for a
 // filter row fh, 8 consecutive outputs of one output row read a window of
@@ -134,7 +135,9 @@ __global__ void __launch_bounds__(kLThreads, 1)
                 const int c = i % kLCh, t = i / kLCh, fw = t % p.FW, fh = t / p.FW;
                 const int cc = cur.ctile * kLCh + c;
                 if (cc >= p.C) continue;
-                const T v = __ldg(wg + (size_t)t * p.C + cc);
+                // Transposed view: kernel tap (fh, fw) is memory tap (fw, fh).
+                const int mt = p.transpose ? fw * FH + fh : t;
+                const T v = __ldg(wg + (size_t)mt * p.C + cc);
                 const int dfh = p.flip ? FH - 1 - fh : fh, dfw = p.flip ? p.FW - 1 - fw : fw;
                 T *row = F + (c * FH + dfh) * 2 * C::FP;
                 row[dfw + 8] = v;            // copy 0
@@ -301,8 +304,8 @@ cudaError_t run_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     const size_t es = sizeof(T);
     const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off_h * p.Wf + p.in_off_w) * p.C * es;
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.in_step_w * p.C * es, (uint64_t)p.in_step_h * p.Wf * p.C * es,
-                             (uint64_t)p.Hf * p.Wf * p.C * es};
+    uint64_t str[3];
+    in_strides(p, es, str);
     const uint32_t box[4] = {(uint32_t)kLCh, (uint32_t)C::SW, (uint32_t)C::HR, 1};
     const uint32_t obox[4] = {(uint32_t)kLCh, (uint32_t)C::OTW, (uint32_t)C::OTH, 1};
     CUtensorMap map, omap;
@@ -335,6 +338,7 @@ cudaError_t large_by_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st
     const int nkb = (p.FW + 7 + 15) / 16;
     if (p.FH == 31 && nkb == 3) return large_by_width<T, 31, 3, FUSE>(p, dt, st);
     if (p.FH == 13 && nkb == 2) return large_by_width<T, 13, 2, FUSE>(p, dt, st);
+    if (p.FH == 5 && nkb == 4) return large_by_width<T, 5, 4, FUSE>(p, dt, st);  // 5 x 51 strips (either way)
     return cudaErrorNotSupported;
 }
 
