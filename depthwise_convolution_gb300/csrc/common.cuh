@@ -352,5 +352,9 @@ cudaError_t launch_tiled_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t
 // into p.out).
 int tiled_wgrad_slices(const TiledConv &p, dwconv_dtype dt);
 cudaError_t launch_tiled_wgrad(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st);
+// Weight gradient for the filters tiled_wgrad does not compile (large and
+// strip filters; p.transpose accepted), tiled_wgrad_large.cu: same contract.
+int tiled_wgrad_large_slices(const TiledConv &p, dwconv_dtype dt);
+cudaError_t launch_tiled_wgrad_large(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st);
 
 }  // namespace dwc

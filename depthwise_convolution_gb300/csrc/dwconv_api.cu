@@ -161,7 +161,27 @@ bool wgrad_tiled_params(const Shape &s, dwconv_dtype dt, const void *x, const vo
     p.N = s.N; p.C = s.C; p.FH = s.FH; p.FW = s.FW; p.flip = 0;
     p.OHf = s.OH; p.OWf = s.OW; p.OHs = s.OH; p.OWs = s.OW;
     p.out_step_h = p.out_step_w = 1; p.out_off_h = p.out_off_w = 0; p.zero_phases = 0;
-    return tiled_wgrad_slices(p, dt) > 0;
+    return true;
+}
+
+// The large-filter weight gradient walks filter columns in register windows:
+// a filter taller than wide is taken transposed (TiledConv::transpose).
+TiledConv wgrad_large_view(const TiledConv &p) {
+    TiledConv q = p;
+    if (p.FW < 8 && p.FH > p.FW) {
+        q.transpose = 1;
+        std::swap(q.Hs, q.Ws);
+        std::swap(q.pad_h, q.pad_w);
+        std::swap(q.FH, q.FW);
+        std::swap(q.OHs, q.OWs);
+    }
+    return q;
+}
+
+// Slices (workspace) of the tiled weight-gradient path for this shape, 0 if none.
+int wgrad_tiled_plan(const TiledConv &p, dwconv_dtype dt) {
+    const int z = tiled_wgrad_slices(p, dt);
+    return z > 0 ? z : tiled_wgrad_large_slices(wgrad_large_view(p), dt);
 }
 
 }  // namespace
@@ -368,7 +388,7 @@ size_t dwconv_bwd_filter_workspace_size_2d(int N, int H, int W, int C, int FH, i
     size_t need = (size_t)wgrad_slices(s) * per_slice;
     TiledConv p;
     if (wgrad_tiled_params(s, dtype, nullptr, nullptr, nullptr, p)) {
-        const size_t tiled = (size_t)tiled_wgrad_slices(p, dtype) * per_slice;
+        const size_t tiled = (size_t)wgrad_tiled_plan(p, dtype) * per_slice;
         if (tiled > need) need = tiled;
     }
     return need;
@@ -409,6 +429,7 @@ dwconv_status bwd_filter_impl(int N, int H, int W, int C, int FH, int FW, int st
     if (wgrad_tiled_params(s, dtype, x, dy, dw, p) && aligned(x, 16) && aligned(dy, 16)) {
         p.half_accumulate = half_accumulate;
         cudaError_t e = launch_tiled_wgrad(p, dtype, part, cs);
+        if (e == cudaErrorNotSupported) e = launch_tiled_wgrad_large(wgrad_large_view(p), dtype, part, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
     // Shapes without a tiled instance take the exact fp32 path, also for the
