@@ -232,12 +232,21 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB>::MINB))
                 return t_addr + 2u * ((8 * tj + tr) * C::CS + row * C::RS + col0);
             };
             if constexpr (PA < 0) {
-                for (int b = warp; b < kSteps; b += kStride) {
-                    const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
+                // Two steps per iteration: both loads are in flight before the
+                // stores (measured on GB300: 4 % faster fwd/dgrad at 7x7).
+                int b = warp;
+                for (; b + kStride < kSteps; b += 2 * kStride) {
+                    unsigned v[2][4];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        ldsm_x4_trans(v[u][0], v[u][1], v[u][2], v[u][3], src(b + u * kStride));
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) stsm_x4(dst(b + u * kStride), v[u][0], v[u][1], v[u][2], v[u][3]);
+                }
+                for (; b < kSteps; b += kStride) {
                     unsigned v[4];
-                    ldsm_x4_trans(v[0], v[1], v[2], v[3],
-                                  s_buf + swz((unsigned)((row * C::SW + col0 + tr) * kPB + 16 * tj)));
-                    stsm_x4(t_addr + 2u * ((8 * tj + tr) * C::CS + row * C::RS + col0), v[0], v[1], v[2], v[3]);
+                    ldsm_x4_trans(v[0], v[1], v[2], v[3], src(b));
+                    stsm_x4(dst(b), v[0], v[1], v[2], v[3]);
                 }
             } else {
                 // (Measured on GB300: issuing the next step's load before this

@@ -187,12 +187,20 @@ __global__ void __launch_bounds__(kLThreads, 1)
                 return t_addr + 2u * (tr * C::CS + (m / C::CB) * C::RS + (m % C::CB) * 8);
             };
             if constexpr (PA < 0) {
-                for (int m0 = warp * 4; m0 < kBlocks; m0 += kStride) {
-                    const int m = min(m0 + tj, kBlocks - 1);
-                    const int row = m / C::CB, col0 = (m % C::CB) * 8;
+                // Two steps per iteration: both loads are in flight before the stores.
+                int m0 = warp * 4;
+                for (; m0 + kStride < kBlocks; m0 += 2 * kStride) {
+                    unsigned v[2][4];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        ldsm_x4_trans(v[u][0], v[u][1], v[u][2], v[u][3], src(m0 + u * kStride));
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) stsm_x4(dst(m0 + u * kStride), v[u][0], v[u][1], v[u][2], v[u][3]);
+                }
+                for (; m0 < kBlocks; m0 += kStride) {
                     unsigned v[4];
-                    ldsm_x4_trans(v[0], v[1], v[2], v[3], s_addr + (unsigned)((row * C::SW + col0 + tr) * 16));
-                    stsm_x4(t_addr + 2u * (tr * C::CS + row * C::RS + col0), v[0], v[1], v[2], v[3]);
+                    ldsm_x4_trans(v[0], v[1], v[2], v[3], src(m0));
+                    stsm_x4(dst(m0), v[0], v[1], v[2], v[3]);
                 }
             } else {
                 for (int m0 = warp * 4; m0 < kBlocks; m0 += kStride) {
