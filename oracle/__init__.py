@@ -12,6 +12,8 @@ Contents
     and int64 for integer data, threaded over channel ranges.  Each returns the
     result and the per-element magnitude ``mag`` (sum of |products| plus |bias|)
     that the parity tolerance scales with.
+``decode_e4m3``
+    FP8 E4M3 codes to float64, from the format's bit definition.
 ``dbias``
     The adjoint of the bias term (sum of dy over n, oh, ow), in numpy.
 ``fwd_fused`` / ``prologue`` / ``activation`` / ``round_to``
@@ -280,6 +282,20 @@ def fwd_fused(x, w, bias=None, pre=None, post=None, fmt=None, stride=1, dilation
     return activation(s * z + t, post[2]), np.abs(s) * mag + np.abs(t)
 
 
+def decode_e4m3(bits):
+    """Values of FP8 E4M3 codes (uint8), float64, from the format's definition
+    (OCP 8-bit floating point, E4M3): sign bit, 4 exponent bits with bias 7,
+    3 mantissa bits; exponent field 0 holds the subnormals m * 2^-9; the code
+    S.1111.111 is NaN and there are no infinities (largest value 448)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    val = np.where((b & 0x7F) == 0x7F, np.nan, val)
+    return sign * val
+
+
 def dbias(dy):
     """Bias gradient.  dy [N,OH,OW,C] -> (db [C], mag [C]).
 
@@ -298,5 +314,5 @@ def dbias(dy):
 
 from . import forms, pages  # noqa: E402  (pure-Python helpers, no C needed)
 
-__all__ = ["build", "fwd", "fwd_fused", "prologue", "affine_act", "activation", "ACTIVATIONS", "round_to", "FORMATS", "dgrad", "wgrad", "dbias", "out_extent",
+__all__ = ["build", "fwd", "fwd_fused", "decode_e4m3", "prologue", "affine_act", "activation", "ACTIVATIONS", "round_to", "FORMATS", "dgrad", "wgrad", "dbias", "out_extent",
            "default_threads", "forms", "pages"]

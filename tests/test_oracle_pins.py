@@ -483,3 +483,23 @@ def test_prologue_rounds_to_storage_format():
     pre = (None, np.array([2.0 ** -9]), "none")
     assert np.all(oracle.fwd_fused(x, w, pre=pre, fmt="bf16")[0] == 1.0)
     assert np.all(oracle.fwd_fused(x, w, pre=pre, fmt="fp16")[0] == 1 + 2.0 ** -9)
+
+
+# ---------------------------------------------------------------- FP8 E4M3
+
+def test_e4m3_decode_known_codes():
+    v = oracle.decode_e4m3(np.array([0x00, 0x38, 0xB8, 0x7E, 0x01, 0x08, 0x07, 0x40, 0x3C], dtype=np.uint8))
+    assert v.tolist() == [0.0, 1.0, -1.0, 448.0, 2.0 ** -9, 2.0 ** -6, 7 * 2.0 ** -9, 2.0, 1.5]
+    assert np.isnan(oracle.decode_e4m3(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.decode_e4m3(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    # monotone over the positive codes 0x00..0x7E
+    pos = got[:0x7F]
+    assert np.all(np.diff(pos) > 0)
