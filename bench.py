@@ -180,7 +180,7 @@ class Layer:
         self.bias = None if d["bias"] is None else d["bias"].to(device)
         self.dy = None if d["dy"] is None else d["dy"].to(device)
         N, H, W, C = wl.N, wl.H, wl.W, wl.C
-        ydt = torch.int32 if wl.dtype == "int8" else self.x.dtype
+        ydt = torch.int32 if wl.dtype == "int8" else torch.bfloat16 if wl.dtype == "fp8" else self.x.dtype
         self.y = torch.empty((N, self.OH, self.OW, C), dtype=ydt, device=device)
         self.dx = torch.empty((N, H, W, C), dtype=self.x.dtype, device=device) if "dgrad" in wl.passes else None
         self.dw = torch.empty((wl.FH, wl.FW, C), dtype=torch.float32, device=device) if "wgrad" in wl.passes else None
@@ -532,6 +532,24 @@ def main():
             variants["wgrad"] = res
         except Exception as e:  # report, do not hide
             variants["wgrad"] = {"error": str(e)[:200]}
+
+    # FP8 E4M3 inputs (bf16 output) on the fp32 7x7 layer's shape: forward pass.
+    if rank == 0 and ws == 1 and not args.no_sweep and hasattr(torch, "float8_e4m3fn"):
+        try:
+            base = synthetic.WORKLOADS["fp32-fwd-7x7-64x56x56x128"]
+            f8 = dataclasses.replace(base, name="fp8-fwd-7x7-64x56x56x128", dtype="fp8")
+            lay = Layer(f8)
+            s_ms, pp, _ = time_layer(lay, max(20, args.steps // 10), 3, flush)
+            t_ms = statistics.mean(pp["fwd"])
+            ub = lay.unique("fwd")
+            rf = pass_roofline(lay.kernel["fwd"], lay.valid, ub, t_ms, pk, fma_peak_tflops)
+            variants["fp8_fwd"] = {"workload": f8.name, "ms": round(t_ms, 4), "kernel": lay.kernel["fwd"],
+                                   "gflops_nominal": round(lay.nominal / t_ms / 1e6, 1),
+                                   "gbs_unique": round(ub / t_ms / 1e6, 1), "bound": rf["bound"],
+                                   "roofline_frac": rf["frac"]}
+            del lay
+        except Exception as e:  # report, do not hide
+            variants["fp8_fwd"] = {"error": str(e)[:200]}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:

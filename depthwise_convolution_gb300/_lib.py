@@ -15,7 +15,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT = range(6)
-INT8, FP32, FP16, BF16 = range(4)
+INT8, FP32, FP16, BF16, FP8_E4M3 = range(5)
 ACT_NONE, ACT_RELU, ACT_RELU6, ACT_SILU, ACT_GELU = range(5)
 ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "relu6": ACT_RELU6, "silu": ACT_SILU, "gelu": ACT_GELU}
 

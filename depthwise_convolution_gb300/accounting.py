@@ -11,7 +11,7 @@ transfers a kernel actually makes:
 """
 from __future__ import annotations
 
-ELEM = {"int8": 1, "fp32": 4, "fp16": 2, "bf16": 2}
+ELEM = {"int8": 1, "fp32": 4, "fp16": 2, "bf16": 2, "fp8": 1}
 
 
 def out_extent(X, F, S, D, P):
@@ -42,7 +42,7 @@ def unique_bytes(pass_name, dtype, N, H, W, C, FH, FW, S, D, P, bias=False):
     touched = N * _axis_touched(H, FH, S, D, P) * _axis_touched(W, FW, S, D, P) * C
     w = FH * FW * C * e
     if pass_name == "fwd":
-        ybytes = N * OH * OW * C * (4 if dtype == "int8" else e)
+        ybytes = N * OH * OW * C * (4 if dtype == "int8" else 2 if dtype == "fp8" else e)  # int32 / bf16 y
         return touched * e + w + (C * 4 if bias else 0) + ybytes
     if pass_name == "dgrad":
         return N * OH * OW * C * e + w + N * H * W * C * e

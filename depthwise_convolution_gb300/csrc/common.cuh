@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -61,6 +62,26 @@ template <> struct Pair<__nv_bfloat16> {
     }
 };
 
+// FP8 E4M3 (inputs of the forward pass only): a pair widens exactly to two
+// floats (through f16, which holds every E4M3 value); the store rounds to
+// nearest even with saturation at +-448 (used only by code paths the host
+// never selects for FP8, kept so that the templates compile).
+template <> struct Pair<__nv_fp8_e4m3> {
+    static __device__ __forceinline__ float2 load(const __nv_fp8_e4m3 *p) {
+        const __half2_raw h =
+            __nv_cvt_fp8x2_to_halfraw2(*reinterpret_cast<const __nv_fp8x2_storage_t *>(p), __NV_E4M3);
+        return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    }
+    static __device__ __forceinline__ void store(__nv_fp8_e4m3 *p, float2 v) {
+        *reinterpret_cast<__nv_fp8x2_storage_t *>(p) = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+    }
+};
+
+// Output element type of the forward pass per input type: FP8 inputs give
+// bf16 outputs, every other type its own.
+template <typename T> struct OutOf { using type = T; };
+template <> struct OutOf<__nv_fp8_e4m3> { using type = __nv_bfloat16; };
+
 // Multiply-accumulate on a channel pair, per storage type.  A pair is held in
 // registers as it is stored: fp32 data as float2, 16-bit data as one packed
 // 32-bit word.  fp32 uses the packed fma.rn.f32x2; 16-bit data uses the
@@ -103,6 +124,19 @@ template <> struct Mac<__nv_bfloat16> {
     }
 };
 
+// FP8: a pair converts exactly to a packed f16 pair on load (one cvt), then
+// the mixed-precision FMAs of the f16 path.
+template <> struct Mac<__nv_fp8_e4m3> {
+    using V = unsigned;
+    static __device__ __forceinline__ V load(const __nv_fp8_e4m3 *p) {
+        const __half2_raw h =
+            __nv_cvt_fp8x2_to_halfraw2(*reinterpret_cast<const __nv_fp8x2_storage_t *>(p), __NV_E4M3);
+        return *reinterpret_cast<const unsigned *>(&h);
+    }
+    static __device__ __forceinline__ V zero() { return 0u; }
+    static __device__ __forceinline__ void fma(float2 &acc, V a, V b) { Mac<__half>::fma(acc, a, b); }
+};
+
 // Widening variant: a channel pair is widened to float2 when loaded and every
 // multiply-add is one packed fma.rn.f32x2 (the same products and roundings as
 // Mac<T>; fewer FMA instructions per value, at the cost of the conversions
@@ -118,6 +152,7 @@ template <typename T> struct MacW {
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(__nv_fp8_e4m3 v) { return float(v); }
 
 template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
@@ -125,6 +160,7 @@ template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
     return __float2bfloat16_rn(v);
 }
+template <> __device__ __forceinline__ __nv_fp8_e4m3 from_f32<__nv_fp8_e4m3>(float v) { return __nv_fp8_e4m3(v); }
 
 // ---- fused BN+Act prologue / affine+activation epilogue ---------------------
 

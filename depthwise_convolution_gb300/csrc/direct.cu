@@ -25,7 +25,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) fwd_direct_fp(Shape s, const T *__restrict__ x,
                                                           const T *__restrict__ w,
                                                           const float *__restrict__ bias,
-                                                          T *__restrict__ y, long long total, Fuse fz) {
+                                                          typename OutOf<T>::type *__restrict__ y, long long total,
+                                                          Fuse fz) {
     const bool pre = fz.pre(), post = fz.post();
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
@@ -51,7 +52,7 @@ __global__ void __launch_bounds__(kThreads) fwd_direct_fp(Shape s, const T *__re
             }
         }
         if (post) acc = apply(affine_out(fz, c), acc, fz.out_act);
-        y[idx] = from_f32<T>(acc);
+        y[idx] = from_f32<typename OutOf<T>::type>(acc);
     }
 }
 
@@ -253,6 +254,11 @@ cudaError_t launch_fwd_direct(const Shape &s, dwconv_dtype dt, const void *x, co
             fwd_direct_fp<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
                 s, (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w, (const float *)bias,
                 (__nv_bfloat16 *)y, total, fz);
+            break;
+        case DWCONV_FP8_E4M3:  // e4m3 x and w, bf16 y
+            fwd_direct_fp<__nv_fp8_e4m3><<<grid, kThreads, 0, st>>>(
+                s, (const __nv_fp8_e4m3 *)x, (const __nv_fp8_e4m3 *)w, (const float *)bias, (__nv_bfloat16 *)y,
+                total, fz);
             break;
         default:
             return cudaErrorInvalidValue;

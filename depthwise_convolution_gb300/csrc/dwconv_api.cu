@@ -75,14 +75,20 @@ dwconv_status make_shape(int N, int H, int W, int C, int FH, int FW, int SH, int
     return DWCONV_OK;
 }
 
-bool valid_dtype(dwconv_dtype dt) { return dt >= DWCONV_INT8 && dt <= DWCONV_BF16; }
+bool valid_dtype(dwconv_dtype dt) { return dt >= DWCONV_INT8 && dt <= DWCONV_FP8_E4M3; }
 
 size_t elem_size(dwconv_dtype dt) {
     switch (dt) {
         case DWCONV_INT8: return 1;
+        case DWCONV_FP8_E4M3: return 1;
         case DWCONV_FP32: return 4;
         default: return 2;
     }
+}
+
+// Element size of the forward output: int32 for int8 data, bf16 for FP8.
+size_t out_elem_size(dwconv_dtype dt) {
+    return dt == DWCONV_INT8 ? 4 : dt == DWCONV_FP8_E4M3 ? 2 : elem_size(dt);
 }
 
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
@@ -95,7 +101,7 @@ bool tiled_layout_ok(const Shape &s, dwconv_dtype dt, const void *in, const void
     if (dt == DWCONV_INT8) return false;
     const size_t es = elem_size(dt);
     if ((s.C * es) % 16 != 0) return false;
-    return aligned(in, 16) && aligned(out, 2 * es) && aligned(w, 2 * es);
+    return aligned(in, 16) && aligned(out, 2 * out_elem_size(dt)) && aligned(w, 2 * es);
 }
 
 // Taps read the input rows oh*SH - PH + fh*DH.  With g = gcd(SH, DH) they all
@@ -245,9 +251,10 @@ dwconv_status fwd_impl(int N, int H, int W, int C, int FH, int FW, int stride_h,
     auto act_ok = [](int a) { return a >= DWCONV_ACT_NONE && a <= DWCONV_ACT_GELU; };
     if (!act_ok(fz.in_act) || !act_ok(fz.out_act)) return DWCONV_ERR_INVALID_ARG;
     if (dtype == DWCONV_INT8 && (fz.pre() || fz.post())) return DWCONV_ERR_UNSUPPORTED;
+    if (dtype == DWCONV_FP8_E4M3 && fz.pre()) return DWCONV_ERR_UNSUPPORTED;
     const size_t es = elem_size(dtype);
     const size_t bs = 4;  // int32 (int8 data) or float bias
-    const size_t ys = dtype == DWCONV_INT8 ? 4 : es;
+    const size_t ys = out_elem_size(dtype);
     if (!aligned(x, es) || !aligned(w, es) || !aligned(y, ys) || (bias && !aligned(bias, bs)))
         return DWCONV_ERR_MISALIGNED;
     for (const float *v : {fz.in_scale, fz.in_shift, fz.out_scale, fz.out_shift})
@@ -320,7 +327,7 @@ dwconv_status dwconv_bwd_data_2d(int N, int H, int W, int C, int FH, int FW, int
     dwconv_status st =
         make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s);
     if (st != DWCONV_OK) return st;
-    if (dtype == DWCONV_INT8) return DWCONV_ERR_UNSUPPORTED;
+    if (dtype == DWCONV_INT8 || dtype == DWCONV_FP8_E4M3) return DWCONV_ERR_UNSUPPORTED;
     if (!dy || !w || !dx) return DWCONV_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     if (!aligned(dy, es) || !aligned(w, es) || !aligned(dx, es)) return DWCONV_ERR_MISALIGNED;
@@ -381,7 +388,7 @@ size_t dwconv_bwd_filter_workspace_size_2d(int N, int H, int W, int C, int FH, i
                                            int stride_w, int dilation_h, int dilation_w, int pad_h, int pad_w,
                                            dwconv_dtype dtype) {
     Shape s;
-    if (!valid_dtype(dtype) || dtype == DWCONV_INT8) return 0;
+    if (!valid_dtype(dtype) || dtype == DWCONV_INT8 || dtype == DWCONV_FP8_E4M3) return 0;
     if (make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s) != DWCONV_OK)
         return 0;
     const size_t per_slice = (size_t)FH * FW * C * sizeof(float);
@@ -414,7 +421,8 @@ dwconv_status bwd_filter_impl(int N, int H, int W, int C, int FH, int FW, int st
     dwconv_status st =
         make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s);
     if (st != DWCONV_OK) return st;
-    if (dtype == DWCONV_INT8 || (half_accumulate && dtype != DWCONV_FP16)) return DWCONV_ERR_UNSUPPORTED;
+    if (dtype == DWCONV_INT8 || dtype == DWCONV_FP8_E4M3 || (half_accumulate && dtype != DWCONV_FP16))
+        return DWCONV_ERR_UNSUPPORTED;
     if (!x || !dy || !dw) return DWCONV_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     if (!aligned(x, es) || !aligned(dy, es) || !aligned(dw, 4)) return DWCONV_ERR_MISALIGNED;
@@ -487,7 +495,7 @@ dwconv_status dwconv_bwd_bias(int N, int OH, int OW, int C, dwconv_dtype dtype, 
     if (!valid_dtype(dtype)) return DWCONV_ERR_INVALID_ARG;
     const size_t need = dwconv_bwd_bias_workspace_size(N, OH, OW, C);
     if (need == 0) return DWCONV_ERR_INVALID_ARG;
-    if (dtype == DWCONV_INT8) return DWCONV_ERR_UNSUPPORTED;
+    if (dtype == DWCONV_INT8 || dtype == DWCONV_FP8_E4M3) return DWCONV_ERR_UNSUPPORTED;
     if (!dy || !db || !workspace || workspace_bytes < need) return DWCONV_ERR_INVALID_ARG;
     if (!aligned(dy, elem_size(dtype)) || !aligned(db, 4) || !aligned(workspace, 16)) return DWCONV_ERR_MISALIGNED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -50,9 +50,13 @@ using namespace tiled;
 #define DWCONV_S32_TH 2
 #endif
 
+// The register class decides the tile choice: packed 16-bit pairs, or pairs
+// held as float2 (fp32 data, and FP8 data widened on load).
+template <typename T> constexpr bool packed16() { return sizeof(typename Mac<T>::V) == 4; }
+
 template <typename T>
 size_t smem_cap() {
-    return sizeof(T) == 4 ? DWCONV_S32_SMEM_KB * 1024 : DWCONV_S16_SMEM_KB * 1024;
+    return packed16<T>() ? DWCONV_S16_SMEM_KB * 1024 : DWCONV_S32_SMEM_KB * 1024;
 }
 
 
@@ -78,7 +82,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int halo_elems = g.HH * g.HW * 32;
     const unsigned buf_stride = align128(box_bytes);  // byte offset of stage buffer 1
     const T *wgt = static_cast<const T *>(p.w);
-    T *out = static_cast<T *>(p.out);
+    using TO = typename OutOf<T>::type;
+    TO *out = static_cast<TO *>(p.out);
     const int tile_rows = g.RT * TH, tile_cols = g.CT * TW;
 
     if (tid == 0) {
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         if constexpr (sizeof(T) == 4) {
                             float2 *q = reinterpret_cast<float2 *>(row + col * 32);
                             *q = prologue_f32<A>(*q, s2, t2);
-                        } else {
+                        } else if constexpr (sizeof(T) == 2) {
                             unsigned *q = reinterpret_cast<unsigned *>(row + col * 32);
                             *q = prologue_packed<T, A>(*q, s2, t2);
                         }
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (cvalid && n < p.N) {
             const int i0 = cur.band * tile_rows + r0;
             const int jj0 = cur.twi * tile_cols + j0;
-            T *img = out + (long long)n * p.OHf * p.OWf * p.C + c;
+            TO *img = out + (long long)n * p.OHf * p.OWf * p.C + c;
 #pragma unroll
             for (int th = 0; th < TH; ++th) {
                 const int i = i0 + th;
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     const int j = jj0 + tw;
                     if (j >= p.OWs) break;
                     if (OS == 1) {
-                        Pair<T>::store(img + ((long long)i * p.OWf + j) * p.C, acc[th][tw]);
+                        Pair<TO>::store(img + ((long long)i * p.OWf + j) * p.C, acc[th][tw]);
                     } else {
                         // Every position of the OS x OS block: the computed phase
                         // gets the sum, the others get zero.
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                                 const int orow = OS * i + a, ocol = OS * j + b;
                                 if (orow < p.OHf && ocol < p.OWf) {
                                     const bool hit = a == p.out_off_h && b == p.out_off_w;
-                                    Pair<T>::store(img + ((long long)orow * p.OWf + ocol) * p.C,
+                                    Pair<TO>::store(img + ((long long)orow * p.OWf + ocol) * p.C,
                                                    hit ? acc[th][tw] : make_float2(0.f, 0.f));
                                 }
                             }
@@ -272,7 +277,7 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
 
 template <typename T>
 cudaError_t dispatch_filter(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    constexpr bool k16 = sizeof(T) == 2;
+    constexpr bool k16 = packed16<T>();
     constexpr int TH7 = k16 ? DWCONV_S16_TH : DWCONV_S32_TH, TW7 = k16 ? DWCONV_S16_TW : 7;
     constexpr int MB7 = k16 ? DWCONV_S16_MINB : DWCONV_S32_MINB;
     if (p.zero_phases) {
@@ -316,6 +321,8 @@ cudaError_t launch_tiled_small(const TiledConv &p, dwconv_dtype dt, cudaStream_t
         case DWCONV_FP32: return dispatch_filter<float>(p, dt, st);
         case DWCONV_FP16: return dispatch_filter<__half>(p, dt, st);
         case DWCONV_BF16: return dispatch_filter<__nv_bfloat16>(p, dt, st);
+        case DWCONV_FP8_E4M3: return p.flip || p.fz.pre() ? cudaErrorNotSupported
+                                                         : dispatch_filter<__nv_fp8_e4m3>(p, dt, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -75,6 +75,7 @@ bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const u
         case DWCONV_FP32: t = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
         case DWCONV_FP16: t = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
         case DWCONV_BF16: t = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
+        case DWCONV_FP8_E4M3: t = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;  // bytes, moved as they are
         default: return false;
     }
     for (int i = 0; i < 3; ++i)
@@ -92,7 +93,8 @@ bool encode_tmap_4d(CUtensorMap *map, dwconv_dtype dt, const void *base, const u
         case 64: swz = CU_TENSOR_MAP_SWIZZLE_64B; break;
         default: return false;
     }
-    if (swizzle && box[0] * (dt == DWCONV_FP32 ? 4u : 2u) != (unsigned)swizzle) return false;
+    const unsigned esz = dt == DWCONV_FP32 ? 4u : dt == DWCONV_FP8_E4M3 ? 1u : 2u;
+    if (swizzle && box[0] * esz != (unsigned)swizzle) return false;
     CUtensorMapL2promotion promo;
     switch (l2_promotion) {
         case 0: promo = CU_TENSOR_MAP_L2_PROMOTION_NONE; break;

@@ -15,6 +15,17 @@ from . import _lib
 
 _DTYPE = {torch.int8: _lib.INT8, torch.float32: _lib.FP32, torch.float16: _lib.FP16,
           torch.bfloat16: _lib.BF16}
+if hasattr(torch, "float8_e4m3fn"):
+    _DTYPE[torch.float8_e4m3fn] = _lib.FP8_E4M3
+
+
+def _y_dtype(x: torch.Tensor, dt: int):
+    """Forward output dtype: int32 for int8 data, bf16 for FP8, else x's."""
+    if dt == _lib.INT8:
+        return torch.int32
+    if dt == _lib.FP8_E4M3:
+        return torch.bfloat16
+    return x.dtype
 
 
 def _code(t: torch.Tensor) -> int:
@@ -79,7 +90,7 @@ def dwconv_fwd(x, w, bias=None, stride=1, dilation=1, pad=0, out=None, stream=No
     if bias is not None and (bias.dtype != bias_dtype or tuple(bias.shape) != (C,)):
         raise ValueError(f"bias must be [C] {bias_dtype}")
     OH, OW = dwconv_output_size(H, W, FH, FW, stride, dilation, pad)
-    y_dtype = torch.int32 if dt == _lib.INT8 else x.dtype
+    y_dtype = _y_dtype(x, dt)
     if out is None:
         out = torch.empty((N, OH, OW, C), dtype=y_dtype, device=x.device)
     elif out.dtype != y_dtype or tuple(out.shape) != (N, OH, OW, C):
@@ -128,9 +139,10 @@ def dwconv_fwd_fused(x, w, bias=None, in_scale=None, in_shift=None, in_act="none
     if w.dtype != x.dtype or tuple(w.shape) != (FH, FW, C):
         raise ValueError("w must be [FH, FW, C] with x's dtype")
     OH, OW = dwconv_output_size(H, W, FH, FW, stride, dilation, pad)
+    y_dtype = _y_dtype(x, dt)
     if out is None:
-        out = torch.empty((N, OH, OW, C), dtype=x.dtype, device=x.device)
-    elif out.dtype != x.dtype or tuple(out.shape) != (N, OH, OW, C):
+        out = torch.empty((N, OH, OW, C), dtype=y_dtype, device=x.device)
+    elif out.dtype != y_dtype or tuple(out.shape) != (N, OH, OW, C):
         raise ValueError("out has the wrong shape or dtype")
     _lib.check(_lib.load().dwconv_fwd_fused_2d(
         N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,

@@ -7,7 +7,8 @@ the same quantised values.
 
 Recipe (per tensor): numpy PCG64 seeded with (workload seed, tensor id), drawn
 as float32 N(0, sigma^2) or as uniform integers over an inclusive range, then
-cast once to the workload's dtype (round-to-nearest-even for 16-bit floats).
+cast once to the workload's dtype (round-to-nearest-even for 16-bit floats
+and for FP8 E4M3, whose inputs stay far below its largest value, 448).
 """
 from __future__ import annotations
 
@@ -22,6 +23,7 @@ _TORCH_DTYPES = {
     "fp32": torch.float32,
     "fp16": torch.float16,
     "bf16": torch.bfloat16,
+    "fp8": getattr(torch, "float8_e4m3fn", None),  # E4M3 inputs of the forward pass
 }
 
 # Tensor ids within a workload's seed sequence.

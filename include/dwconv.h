@@ -24,6 +24,16 @@
  *   DWCONV_FP32  x, w, bias, y, dy, dx, dw: float.
  *   DWCONV_FP16  x, w, y, dy, dx: IEEE half; bias, dw: float.
  *   DWCONV_BF16  x, w, y, dy, dx: bfloat16;  bias, dw: float.
+ *   DWCONV_FP8_E4M3  x, w: OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7,
+ *                3 mantissa bits, no infinities, NaN = S.1111.111, largest
+ *                448); bias float; y bfloat16.  Forward pass only
+ *                (dwconv_fwd*, the fused form with an epilogue but no
+ *                prologue); every other entry point returns
+ *                DWCONV_ERR_UNSUPPORTED.  Operands widen exactly to fp32; a
+ *                per-tensor or per-channel dequantisation scale folds into
+ *                the fused epilogue's out_scale.  (The pages name low-bit
+ *                types such as FP8 as an extension: stored and multiplied in
+ *                low precision, accumulated in fp32.)
  *   Floating-point accumulation is fp32 in every case (Flash-DWC §4.1 shows
  *   16-bit accumulation loses too much accuracy); 16-bit outputs are rounded
  *   to nearest even once, at the end.
@@ -61,7 +71,8 @@ typedef enum {
     DWCONV_INT8 = 0,
     DWCONV_FP32 = 1,
     DWCONV_FP16 = 2,
-    DWCONV_BF16 = 3
+    DWCONV_BF16 = 3,
+    DWCONV_FP8_E4M3 = 4
 } dwconv_dtype;
 
 /* Activation functions of the fused forward pass (dwconv_fwd_fused). */

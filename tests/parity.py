@@ -19,10 +19,12 @@ import torch
 import oracle
 from depthwise_convolution_gb300 import ops
 
-TOL = {"fp32": 1e-5, "fp16": 2e-3, "bf16": 2e-3}
+TOL = {"fp32": 1e-5, "fp16": 2e-3, "bf16": 2e-3, "fp8": 2e-3}
 SIG_BITS = {"fp16": 11, "bf16": 8}      # significand bits including the hidden one
 MIN_EXP = {"fp16": -14, "bf16": -126}   # exponent of the smallest normal number
-TORCH = {"int8": torch.int8, "fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16}
+TORCH = {"int8": torch.int8, "fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16,
+         "fp8": getattr(torch, "float8_e4m3fn", None)}
+OUT16 = {"fp16": "fp16", "bf16": "bf16", "fp8": "bf16"}  # 16-bit output format per input dtype
 GUARD = 256                              # guard elements on each side of an output
 
 
@@ -37,6 +39,8 @@ def to64(t: torch.Tensor) -> np.ndarray:
     t = t.detach().cpu()
     if t.dtype in (torch.int8, torch.int32):
         return t.to(torch.int64).numpy()
+    if TORCH["fp8"] is not None and t.dtype == TORCH["fp8"]:
+        return oracle.decode_e4m3(t.view(torch.uint8).numpy())  # from the format's bits
     return t.to(torch.float64).numpy()
 
 
@@ -52,7 +56,7 @@ def compare(got: np.ndarray, ref: np.ndarray, mag: np.ndarray, dtype: str, out16
     err = np.abs(got - ref)
     bound = TOL[dtype] * mag
     if out16:
-        bound = bound + half_ulp(np.maximum(np.abs(ref), np.abs(got)), dtype)
+        bound = bound + half_ulp(np.maximum(np.abs(ref), np.abs(got)), OUT16[dtype])
     over = err > bound
     if over.any():
         i = np.unravel_index(np.argmax(err - bound), err.shape)
@@ -110,14 +114,14 @@ def check_fwd(d, dtype, S, D, P, images=None, what="fwd"):
     N, H, W, C = x.shape
     FH, FW = w.shape[:2]
     OH, OW = out_hw(H, W, FH, FW, S, D, P)
-    out_dtype = torch.int32 if dtype == "int8" else TORCH[dtype]
+    out_dtype = torch.int32 if dtype == "int8" else torch.bfloat16 if dtype == "fp8" else TORCH[dtype]
     g = Guarded((N, OH, OW, C), out_dtype)
     y = ops.dwconv_fwd(x.cuda(), w.cuda(), None if b is None else b.cuda(), S, D, P, out=g.t)
     ops.dwconv_check_device_errors()
     g.check(what)
     imgs = list(range(N)) if images is None else sorted(set(i % N for i in images))
-    ref, mag = oracle.fwd(to64(x[imgs]), to64(w), None if b is None else to64(b), S, D, P)
-    return compare(to64(y[imgs]), ref, mag, dtype, dtype in ("fp16", "bf16"), what)
+    ref, mag = oracle.fwd(to64(x)[imgs], to64(w), None if b is None else to64(b), S, D, P)
+    return compare(to64(y[imgs]), ref, mag, dtype, dtype in ("fp16", "bf16", "fp8"), what)
 
 
 def check_dgrad(d, dtype, S, D, P, images=None, what="dgrad"):
@@ -181,7 +185,7 @@ def check_fused(d, dtype, S, D, P, pre=None, post=None, images=None, what="fused
         kw.update(in_scale=cuda(pre[0]), in_shift=cuda(pre[1]), in_act=pre[2])
     if post is not None:
         kw.update(out_scale=cuda(post[0]), out_shift=cuda(post[1]), out_act=post[2])
-    g = Guarded((N, OH, OW, C), TORCH[dtype])
+    g = Guarded((N, OH, OW, C), torch.bfloat16 if dtype == "fp8" else TORCH[dtype])
     y = ops.dwconv_fwd_fused(x.cuda(), w.cuda(), cuda(b), stride=S, dilation=D, pad=P, out=g.t, **kw)
     ops.dwconv_check_device_errors()
     g.check(what)
@@ -191,21 +195,21 @@ def check_fused(d, dtype, S, D, P, pre=None, post=None, images=None, what="fused
     opre = None if pre is None else (f64(pre[0]), f64(pre[1]), pre[2])
     opost = None if post is None else (f64(post[0]), f64(post[1]), post[2])
     fmt = dtype if dtype in ("fp16", "bf16", "fp32") else None
-    ref, mag = oracle.fwd_fused(to64(x[imgs]), to64(w), f64(b), pre=opre, post=opost, fmt=fmt,
+    ref, mag = oracle.fwd_fused(to64(x)[imgs], to64(w), f64(b), pre=opre, post=opost, fmt=fmt,
                                 stride=S, dilation=D, pad=P)
     got = to64(y[imgs])
     lip = LIP[post[2]] if post is not None else 1.0
     s_post = np.ones(C) if post is None or post[0] is None else np.abs(f64(post[0]))
     e_pre = 0.0
     if pre is not None and dtype in ("fp16", "bf16"):
-        xq = oracle.prologue(to64(x[imgs]), opre, fmt)
+        xq = oracle.prologue(to64(x)[imgs], opre, fmt)
         e_pre, _ = oracle.fwd(2 * half_ulp(xq, dtype), np.abs(to64(w)), None, S, D, P)
     assert got.shape == ref.shape
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
     bound = lip * (TOL[dtype] * mag + s_post * e_pre) + 1e-6 * mag
-    if dtype in ("fp16", "bf16"):
-        bound = bound + half_ulp(np.maximum(np.abs(ref), np.abs(got)), dtype)
+    if dtype in OUT16:
+        bound = bound + half_ulp(np.maximum(np.abs(ref), np.abs(got)), OUT16[dtype])
     over = err > bound
     if over.any():
         i = np.unravel_index(np.argmax(err - bound), err.shape)

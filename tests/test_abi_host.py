@@ -173,6 +173,21 @@ def test_half_accumulate_wgrad_validation(lib):
     assert lib.dwconv_launch_count() == before
 
 
+def test_fp8_is_forward_only(lib):
+    args = (2, 8, 8, 16, 3, 3, 1, 1, 1)
+    before = lib.dwconv_launch_count()
+    F8 = _lib.FP8_E4M3
+    assert lib.dwconv_bwd_data(*args, F8, A, A, A, None) == _lib.ERR_UNSUPPORTED
+    assert lib.dwconv_bwd_filter_workspace_size(*args, F8) == 0
+    assert lib.dwconv_bwd_filter(*args, F8, A, A, A, A, 1 << 20, None) == _lib.ERR_UNSUPPORTED
+    assert lib.dwconv_bwd_filter_ha(*args, F8, A, A, A, A, 1 << 20, None) == _lib.ERR_UNSUPPORTED
+    assert lib.dwconv_bwd_bias(2, 8, 8, 16, F8, A, A, A, 1 << 20, None) == _lib.ERR_UNSUPPORTED
+    assert fused(lib, dt=F8, iact=_lib.ACT_RELU) == _lib.ERR_UNSUPPORTED   # no prologue for FP8
+    assert fused(lib, dt=F8, y=A + 1) == _lib.ERR_MISALIGNED                 # bf16 output
+    assert lib.dwconv_fwd(2, 8, 8, 16, 3, 3, 1, 1, 1, 5, A, A, None, A, None) == _lib.ERR_INVALID_ARG
+    assert lib.dwconv_launch_count() == before
+
+
 def test_workspace_size_is_a_pure_function_of_the_shape(lib):
     args = (128, 56, 56, 96, 7, 7, 1, 1, 3)
     a = lib.dwconv_bwd_filter_workspace_size(*args, _lib.FP16)
