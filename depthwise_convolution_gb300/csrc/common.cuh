@@ -392,5 +392,9 @@ cudaError_t launch_tiled_wgrad(const TiledConv &p, dwconv_dtype dt, float *part,
 // strip filters; p.transpose accepted), tiled_wgrad_large.cu: same contract.
 int tiled_wgrad_large_slices(const TiledConv &p, dwconv_dtype dt);
 cudaError_t launch_tiled_wgrad_large(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st);
+// Tensor-core weight gradient for large 16-bit filters (tiled_mma_wgrad.cu):
+// same contract, taken before the CUDA-core kernel when an instance covers it.
+int tiled_mma_wgrad_slices(const TiledConv &p, dwconv_dtype dt);
+cudaError_t launch_tiled_mma_wgrad(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st);
 
 }  // namespace dwc

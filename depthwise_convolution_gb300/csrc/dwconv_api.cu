@@ -2,6 +2,7 @@
 //
 // Every entry point validates all arguments on the host before it touches
 // the CUDA runtime, so a rejected call enqueues nothing (and needs no GPU).
+#include <algorithm>
 #include <atomic>
 #include <climits>
 
@@ -187,7 +188,9 @@ TiledConv wgrad_large_view(const TiledConv &p) {
 // Slices (workspace) of the tiled weight-gradient path for this shape, 0 if none.
 int wgrad_tiled_plan(const TiledConv &p, dwconv_dtype dt) {
     const int z = tiled_wgrad_slices(p, dt);
-    return z > 0 ? z : tiled_wgrad_large_slices(wgrad_large_view(p), dt);
+    if (z > 0) return z;
+    const TiledConv q = wgrad_large_view(p);
+    return std::max(tiled_mma_wgrad_slices(q, dt), tiled_wgrad_large_slices(q, dt));
 }
 
 }  // namespace
@@ -437,6 +440,7 @@ dwconv_status bwd_filter_impl(int N, int H, int W, int C, int FH, int FW, int st
     if (wgrad_tiled_params(s, dtype, x, dy, dw, p) && aligned(x, 16) && aligned(dy, 16)) {
         p.half_accumulate = half_accumulate;
         cudaError_t e = launch_tiled_wgrad(p, dtype, part, cs);
+        if (e == cudaErrorNotSupported) e = launch_tiled_mma_wgrad(wgrad_large_view(p), dtype, part, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_wgrad_large(wgrad_large_view(p), dtype, part, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }

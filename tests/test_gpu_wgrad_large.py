@@ -1,5 +1,6 @@
-"""Weight gradient of large and strip filters on the tiled tap-group kernel
-(tiled_wgrad_large.cu) against the oracle, element by element within the
+"""Weight gradient of large and strip filters -- 16-bit data on the
+tensor-core kernel (tiled_mma_wgrad.cu), fp32 on the tiled tap-group kernel
+(tiled_wgrad_large.cu) -- against the oracle, element by element within the
 stated fp32-accumulation bounds, and bit-identical from call to call.
 """
 from __future__ import annotations
@@ -23,6 +24,8 @@ CASES = [
     ("bf16", (1, 9, 33, 16, 1, 31, 1, 1, (0, 15))),    # 1 x K
     ("fp16", (2, 24, 24, 16, 9, 9, 2, 2, 8)),          # stride 2 dilation 2: even sub-grid
     ("fp32", (2, 12, 13, 12, 5, 3, 1, 1, (2, 1))),     # small non-square: no tiled_wgrad instance
+    ("bf16", (2, 40, 70, 16, 13, 13, 1, 1, 6)),        # several dy tiles per row
+    ("fp16", (2, 21, 19, 8, 17, 29, 1, 1, (8, 14))),   # 2 x 4 blocks, ragged both ways
     ("bf16", (1, 5, 6, 8, 11, 11, 1, 1, 5)),           # map smaller than the filter
 ]
 
@@ -37,7 +40,7 @@ def test_large_filter_wgrad(case):
     dt, (N, H, W, C, FH, FW, S, D, P) = case
     d = random_inputs(dt, N, H, W, C, FH, FW, S, D, P, seed=73)
     check_wgrad(d, dt, S, D, P, what="wgrad-large")
-    assert ops.dwconv_last_kernel() == "tiled_wgrad_large"
+    assert ops.dwconv_last_kernel() == ("tiled_wgrad_large" if dt == "fp32" else "tiled_mma_wgrad")
 
 
 def test_large_filter_wgrad_is_deterministic():
@@ -46,5 +49,5 @@ def test_large_filter_wgrad_is_deterministic():
     x, dy = d["x"].cuda(), d["dy"].cuda()
     a = ops.dwconv_bwd_filter(x, dy, FH, FW, S, D, P)
     b = ops.dwconv_bwd_filter(x, dy, FH, FW, S, D, P)
-    assert ops.dwconv_last_kernel() == "tiled_wgrad_large"
+    assert ops.dwconv_last_kernel() == "tiled_mma_wgrad"
     assert torch.equal(a, b)
