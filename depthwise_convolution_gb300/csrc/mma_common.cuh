@@ -48,14 +48,6 @@ template <> struct MmaOp<__nv_bfloat16> {
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     }
-    // m16n8k8: A rows gq / gq+8 (k 2t4, 2t4+1) in a0 / a1, B (k 2t4, 2t4+1; n gq) in b0.
-    static __device__ __forceinline__ void run_k8(float (&d)[4], unsigned a0, unsigned a1, unsigned b0) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
-            "{%0,%1,%2,%3};\n"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(a1), "r"(b0));
-    }
     static __device__ __forceinline__ unsigned pack(float lo, float hi) {
         __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<unsigned *>(&v);
@@ -75,14 +67,6 @@ template <> struct MmaOp<__half> {
             "{%0,%1,%2,%3};\n"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-    // m16n8k8: A rows gq / gq+8 (k 2t4, 2t4+1) in a0 / a1, B (k 2t4, 2t4+1; n gq) in b0.
-    static __device__ __forceinline__ void run_k8(float (&d)[4], unsigned a0, unsigned a1, unsigned b0) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
-            "{%0,%1,%2,%3};\n"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(a1), "r"(b0));
     }
     static __device__ __forceinline__ unsigned pack(float lo, float hi) {
         __half2 v = __floats2half2_rn(lo, hi);

@@ -7,9 +7,9 @@
 // correlation; over a tile it becomes a GEMM whose A operand is a Toeplitz
 // band of dy (the Flash-DWC §4.2 packing with dy in the filter's place):
 //
-//   D[m][n] += sum_{k<8} A[m][k] B[k][n],  A[m][k] = dy[i][J0 + k - fw(m)],  B[k][n] = x[i + fh(n)][J0 + k],
+//   D[m][n] += sum_{k<16} A[m][k] B[k][n],  A[m][k] = dy[i][J0 + k - fw(m)],  B[k][n] = x[i + fh(n)][J0 + k],
 //
-// an mma.sync m16n8k8 (16-bit in, fp32 accumulate) per 8 x columns J0, 16
+// an mma.sync m16n8k16 (16-bit in, fp32 accumulate) per 16 x columns J0, 16
 // filter columns fw(m) = 16 fb + m and 8 filter rows fh(n) = 8 hb + n.  Every
 // x column meets every dy column exactly once, so no band is masked: dy
 // outside the tile is zero in the staged copy.
@@ -40,14 +40,14 @@ struct CfgW {
     static constexpr int FWMAX = 16 * NFB, FHMAX = 8 * NHB;
     // x halo: rows OTH + FH - 1 staged, OTH + 8 NHB - 1 allocated (the last
     // block's surplus rows only reach unused accumulator columns); columns
-    // OTW + FW - 1 rounded up to whole 8-column groups, NG of them at most.
-    static constexpr int NG = (kWOTW + FWMAX - 1 + 7) / 8;
-    static constexpr int SWX = 8 * NG;
+    // OTW + FW - 1 rounded up to whole 16-column groups, NG of them at most.
+    static constexpr int NG = (kWOTW + FWMAX - 1 + 15) / 16;
+    static constexpr int SWX = 16 * NG;
     static constexpr int TXR = kWOTH + FHMAX - 1;
     // T_x row stride: 8 rows of a B load fall in distinct bank quads.
     static constexpr int RSX = SWX % 16 == 8 ? SWX : SWX + ((8 - SWX % 16 + 16) % 16);
     static constexpr int CSX = TXR * RSX;
-    // T_dy: dy column e sits at LM + e; A reads e from -(16 NFB - 1) to 8 NG.
+    // T_dy: dy column e sits at LM + e; A reads e from -(16 NFB - 1) to 16 NG.
     static constexpr int LM = 16 * NFB;
     static constexpr int DW = LM + SWX + 8;
     static constexpr int CSD = 2 * kWOTH * DW + 16;  // two copies; +16 halves: copies apart in banks
@@ -137,10 +137,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
         // 8-pixel blocks per step (lane (tr, tj) addresses pixel tr of block
         // tj); blocks past the last repeat it (same data to the same place).
         {
-            const int nb = g.HR * NG;
+            constexpr int CB = C::SWX / 8;  // 8-pixel blocks per row
+            const int nb = g.HR * CB;
             for (int m0 = warp * 4; m0 < nb; m0 += kWThreads / 8) {
                 const int m = min(m0 + tj, nb - 1);
-                const int row = m / NG, col0 = (m % NG) * 8;
+                const int row = m / CB, col0 = (m % CB) * 8;
                 unsigned v0, v1, v2, v3;
                 ldsm_x4_trans(v0, v1, v2, v3, sx + (unsigned)((row * C::SWX + col0 + tr) * 16));
                 stsm_x4(tx_addr + 2u * (unsigned)(tr * C::CSX + row * C::RSX + col0), v0, v1, v2, v3);
@@ -168,29 +169,33 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
         __syncthreads();  // T_x, T_dy ready; this staging buffer is free
 
-        // MMAs of this warp's channel.  Blocks (grp, fb) whose x columns meet
-        // no dy column of the tile are skipped at compile time.
+        // MMAs of this warp's channel, 16 x columns each (m16n8k16).  A of
+        // block fb, group grp holds dy columns e0 = 16 grp + 2t4 - 16 fb - gq
+        // (a0), e0 - 8 (a1, M rows 8-15), e0 + 8 (a2, k 8-15) and e0 again
+        // (a3: rows 8-15 and k 8-15 cancel).  Blocks (grp, fb) whose x columns
+        // meet no dy column of the tile are skipped at compile time.
 #pragma unroll 1
         for (int i = 0; i < kWOTH; ++i) {
 #pragma unroll
             for (int grp = 0; grp < NG; ++grp) {
-                unsigned b[NHB];
+                unsigned b[NHB][2];
 #pragma unroll
-                for (int hb = 0; hb < NHB; ++hb)
-                    asm volatile("ld.shared.b32 %0, [%1];\n"
-                                 : "=r"(b[hb])
-                                 : "r"(b_lane + 2u * (unsigned)((i + 8 * hb) * C::RSX + 8 * grp)));
+                for (int hb = 0; hb < NHB; ++hb) {
+                    const unsigned ba = b_lane + 2u * (unsigned)((i + 8 * hb) * C::RSX + 16 * grp);
+                    asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(b[hb][0]) : "r"(ba));
+                    asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(b[hb][1]) : "r"(ba + 16u));
+                }
 #pragma unroll
                 for (int fb = 0; fb < NFB; ++fb) {
-                    // x columns 8 grp .. +7 against filter columns 16 fb .. +15:
-                    // dy columns 8 grp - 16 fb - 15 .. 8 grp - 16 fb + 7.
-                    if (8 * grp - 16 * fb + 7 < 0 || 8 * grp - 16 * fb - 15 >= kWOTW) continue;
-                    const unsigned a = a_lane + 2u * (unsigned)(i * C::DW + 8 * grp - 16 * fb);
-                    unsigned a0, a1;
+                    // dy columns 16 grp - 16 fb - 15 .. 16 grp - 16 fb + 15.
+                    if (16 * grp - 16 * fb + 15 < 0 || 16 * grp - 16 * fb - 15 >= kWOTW) continue;
+                    const unsigned a = a_lane + 2u * (unsigned)(i * C::DW + 16 * grp - 16 * fb);
+                    unsigned a0, a1, a2;
                     asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(a0) : "r"(a));
                     asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(a1) : "r"(a - 16u));  // 8 columns left
+                    asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(a2) : "r"(a + 16u));  // 8 columns right
 #pragma unroll
-                    for (int hb = 0; hb < NHB; ++hb) MmaOp<T>::run_k8(acc[fb][hb], a0, a1, b[hb]);
+                    for (int hb = 0; hb < NHB; ++hb) MmaOp<T>::run(acc[fb][hb], a0, a1, a2, a0, b[hb][0], b[hb][1]);
                 }
             }
         }
