@@ -210,7 +210,6 @@ __global__ void __maxnreg__(MAXR)
                 for (int k = 0; k < TW; ++k) xw[k] = M::load(xrow + k * 32);
                 // Filter columns in blocks of TW so the window slot of each input
                 // value is a compile-time index.
-#pragma unroll(FWC ? 1 : 0)
                 for (int fb = 0; fb < FW; fb += TW) {
 #pragma unroll
                     for (int k = 0; k < TW; ++k) {

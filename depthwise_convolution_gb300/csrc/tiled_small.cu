@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             const int col_in = cur.twi * tile_cols - p.pad_w;
             const int c_lo = min(max(-col_in, 0), g.HW), c_hi = max(min(p.Ws - col_in, g.HW), c_lo);
             with_act<FUSE == 1>(p.fz.in_act, [&](auto act) {
-                constexpr int A = decltype(act)::value;
+                [[maybe_unused]] constexpr int A = decltype(act)::value;
 #pragma unroll 1
                 for (int rr = t; rr < g.NI * g.HH; rr += kTiles) {
                     const int im = rr / g.HH, r = rr - im * g.HH;
