@@ -47,7 +47,7 @@ DEFAULT_WORKLOAD = "fp16-train-7x7-128x56x56x96"
 METRIC = "DWC fwd/dgrad/wgrad GFLOP/s and HBM GB/s as % of roofline on 1xGB300"
 L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2, written between timed steps
 FMA_LANES_PER_SM = 128              # fp32 FMA units per SM on Blackwell
-TENSOR_KERNELS = {"tiled_mma", "tiled_mma_large"}   # kernel families on the tensor pipe
+TENSOR_KERNELS = {"tiled_mma", "tiled_mma_large", "tiled_mma_wgrad"}   # kernel families on the tensor pipe
 
 
 # ----------------------------------------------------------------- helpers
@@ -532,6 +532,27 @@ def main():
             variants["wgrad"] = res
         except Exception as e:  # report, do not hide
             variants["wgrad"] = {"error": str(e)[:200]}
+
+    # The 31x31 layer as a training step (its configuration times the forward
+    # pass only): forward, input gradient and weight gradient.
+    if rank == 0 and ws == 1 and not args.no_sweep:
+        try:
+            base = synthetic.WORKLOADS["bf16-fwd-31x31-32x56x56x128"]
+            tw = dataclasses.replace(base, name="bf16-train-31x31-32x56x56x128", bias=False,
+                                     passes=("fwd", "dgrad", "wgrad"))
+            lay = Layer(tw)
+            s_ms, pp, _ = time_layer(lay, max(20, args.steps // 10), 3, flush)
+            entry = {"workload": tw.name, "ms_per_step": round(statistics.mean(s_ms), 4)}
+            for pn in tw.passes:
+                t_ms = statistics.mean(pp[pn])
+                ub = lay.unique(pn)
+                rf = pass_roofline(lay.kernel[pn], lay.valid, ub, t_ms, pk, fma_peak_tflops)
+                entry[pn] = {"ms": round(t_ms, 4), "kernel": lay.kernel[pn], "bound": rf["bound"],
+                             "roofline_frac": rf["frac"]}
+            variants["large_filter_train"] = entry
+            del lay
+        except Exception as e:  # report, do not hide
+            variants["large_filter_train"] = {"error": str(e)[:200]}
 
     # FP8 E4M3 inputs (bf16 output) on the fp32 7x7 layer's shape: forward pass.
     if rank == 0 and ws == 1 and not args.no_sweep and hasattr(torch, "float8_e4m3fn"):
