@@ -59,6 +59,21 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value, ws, device):
+    """The largest of the ranks' values (the slowest rank bounds a step); every
+    rank gets it.  One process: the value itself."""
+    if ws == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(ws, flops_per_rank, ms):
+    """GFLOP/s of the whole job: every rank's work over the slowest rank's time."""
+    return ws * flops_per_rank / (ms * 1e-3) / 1e9
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     out = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "source": "fallback"}
@@ -464,13 +479,9 @@ def main():
         torch.distributed.barrier()
     sampler.stop()
 
-    ms = statistics.mean(step_ms)
-    if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), ws, "cuda")
     step_flops = layer.nominal * len(wl.passes)
-    value = ws * step_flops / (ms * 1e-3) / 1e9
+    value = whole_job_rate(ws, step_flops, ms)
 
     passes = {}
     for p in wl.passes:
@@ -494,11 +505,8 @@ def main():
                     unique_bytes_per_launch=layer.unique(dom))
 
     e2e_ms, h2d, d2h = time_e2e(layer, max(10, args.steps // 10))
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": round(ws * step_flops / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GFLOP/s",
+    e2e_ms = max_over_ranks(e2e_ms, ws, "cuda")
+    e2e = {"value": round(whole_job_rate(ws, step_flops, e2e_ms), 1), "unit": "GFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
     sweep = {}
