@@ -81,6 +81,9 @@ template <> struct Pair<__nv_fp8_e4m3> {
 // bf16 outputs, every other type its own.
 template <typename T> struct OutOf { using type = T; };
 template <> struct OutOf<__nv_fp8_e4m3> { using type = __nv_bfloat16; };
+// Tensor-core operand type per input type: FP8 E4M3 converts exactly to f16.
+template <typename T> struct MmaIn { using type = T; };
+template <> struct MmaIn<__nv_fp8_e4m3> { using type = __half; };
 
 // Multiply-accumulate on a channel pair, per storage type.  A pair is held in
 // registers as it is stored: fp32 data as float2, 16-bit data as one packed

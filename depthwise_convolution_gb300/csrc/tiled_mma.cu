@@ -23,6 +23,7 @@ cudaError_t launch_tiled_mma(const TiledConv &p, dwconv_dtype dt, cudaStream_t s
     switch (dt) {
         case DWCONV_FP16: return by_filter<__half, false>(p, dt, st);
         case DWCONV_BF16: return by_filter<__nv_bfloat16, false>(p, dt, st);
+        case DWCONV_FP8_E4M3: return p.flip ? cudaErrorNotSupported : by_filter<__nv_fp8_e4m3, false>(p, dt, st);
         default: return cudaErrorNotSupported;
     }
 }

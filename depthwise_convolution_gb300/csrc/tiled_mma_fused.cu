@@ -12,6 +12,7 @@ cudaError_t launch_tiled_mma_fused(const TiledConv &p, dwconv_dtype dt, cudaStre
     switch (dt) {
         case DWCONV_FP16: return by_filter<__half, true>(p, dt, st);
         case DWCONV_BF16: return by_filter<__nv_bfloat16, true>(p, dt, st);
+        case DWCONV_FP8_E4M3: return p.flip ? cudaErrorNotSupported : by_filter<__nv_fp8_e4m3, true>(p, dt, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -66,8 +66,9 @@ constexpr int kPB = 2 * kCh;            // bytes of one staged pixel (= swizzle 
 __device__ __forceinline__ unsigned swz(unsigned a) { return a ^ (((a >> 7) & 3u) << 4); }
 
 // Tile geometry, fixed by the filter height, G, the images per unit NI and
-// the row sets per unit KNB.
-template <int FH, int G, int NI, int KNB>
+// the row sets per unit KNB; ES = bytes of a staged input element (2, or 1
+// for FP8 inputs, whose halo is converted to f16 during the transposition).
+template <int FH, int G, int NI, int KNB, int ES = 2>
 struct Cfg {
     static constexpr int RB = 8 / G;                              // output rows of an 8-row M block
     static constexpr int OTH = NI == 1 ? 2 * KNB * RB : KNB * RB; // output rows per image
@@ -79,7 +80,7 @@ struct Cfg {
     static constexpr int RS = SW;                                 // T row stride (halves)
     static constexpr int CS = channel_stride(TR * RS);            // T channel stride (halves)
     static constexpr int NQ = (KNB - 1) * RB + FH;                // A operands per channel
-    static constexpr unsigned s_bytes = TR * SW * kPB;
+    static constexpr unsigned s_bytes = TR * SW * kCh * ES;
     static constexpr unsigned s_stride = align1k(s_bytes);
     static constexpr unsigned t_bytes = align1k(kCh * CS * 2);
     static constexpr unsigned o_bytes = NI * OTH * OTW * kPB;
@@ -93,15 +94,28 @@ struct Cfg {
 // FUSE: the BN+Act prologue and affine+activation epilogue of the fused
 // forward pass are compiled in (a separate instance, so that the plain
 // passes keep their own register allocation).
+template <typename T> __host__ __device__ constexpr int in_es() { return sizeof(T) == 1 ? 1 : 2; }
+
+// Input element to tensor-core operand type (exact for every supported pair).
+template <typename TM, typename T>
+__device__ __forceinline__ TM to_operand(T v) {
+    if constexpr (std::is_same<T, TM>::value)
+        return v;
+    else
+        return from_f32<TM>(to_f32(v));
+}
+
 template <typename T, int FH, int FW, int G, int NI, int KNB, bool FUSE>
-__global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB>::MINB))
+__global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::MINB))
     tiled_mma_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap out_map,
                      TiledConv p, GeoM g, unsigned *err) {
-    using C = Cfg<FH, G, NI, KNB>;
+    using C = Cfg<FH, G, NI, KNB, in_es<T>()>;
     constexpr int RB = C::RB, DHT = C::DHT, NQ = C::NQ, NS = C::NS;
     extern __shared__ __align__(1024) unsigned char smem_dyn[];
     __shared__ __align__(8) uint64_t bar[NS];
-    using Op = MmaOp<T>;
+    using TM = typename MmaIn<T>::type;   // MMA operand type
+    using TO = typename OutOf<T>::type;   // output type
+    using Op = MmaOp<TM>;
 
     // Swizzled buffers start on 1024-byte boundaries (the launch adds 1 KB of slack).
     unsigned char *smem_raw = reinterpret_cast<unsigned char *>(
@@ -172,13 +186,13 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB>::MINB))
                     const int sfh = p.flip ? FH - 1 - fh : fh;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        T v[2];
+                        TM v[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int fw = 2 * t4 + e + 8 * h - gq;
-                            v[e] = from_f32<T>(0.f);
+                            v[e] = from_f32<TM>(0.f);
                             if (live && fw >= 0 && fw < FW)
-                                v[e] = wg[(sfh * FW + (p.flip ? FW - 1 - fw : fw)) * p.C + cc];
+                                v[e] = to_operand<TM>(wg[(sfh * FW + (p.flip ? FW - 1 - fw : fw)) * p.C + cc]);
                         }
                         bfr[ci][fh][h] = Op::pack_raw(v[0], v[1]);
                     }
@@ -231,7 +245,26 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB>::MINB))
                 const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
                 return t_addr + 2u * ((8 * tj + tr) * C::CS + row * C::RS + col0);
             };
-            if constexpr (PA < 0) {
+            if constexpr (sizeof(T) == 1) {
+                // FP8: the staged pixel is 32 bytes, unswizzled.  Lane (gq, t4)
+                // gathers channel 8m + gq of columns col0 + 2t4, +1 -- the
+                // layout ldmatrix.trans gives for 16-bit data -- and converts
+                // each pair exactly to f16.
+                const unsigned char *s8 = smem_raw + (k % NS) * C::s_stride;
+                for (int b = warp; b < kSteps; b += kStride) {
+                    const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
+                    const unsigned char *px = s8 + (row * C::SW + col0 + 2 * t4) * kCh + gq;
+                    unsigned v[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const __nv_fp8x2_storage_t pr =
+                            (__nv_fp8x2_storage_t)(px[8 * m] | ((unsigned)px[kCh + 8 * m] << 8));
+                        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+                        v[m] = *reinterpret_cast<const unsigned *>(&h);
+                    }
+                    stsm_x4(dst(b), v[0], v[1], v[2], v[3]);
+                }
+            } else if constexpr (PA < 0) {
                 // Two steps per iteration: both loads are in flight before the
                 // stores (measured on GB300: 4 % faster fwd/dgrad at 7x7).
                 int b = warp;
@@ -353,8 +386,8 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB>::MINB))
                 unsigned lo[2], hi[2];  // column 2t4 + e: channels (0, 1), (2, 3)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    lo[e] = Op::pack(d[0][j][2 * half + e], d[1][j][2 * half + e]);
-                    hi[e] = Op::pack(d[2][j][2 * half + e], d[3][j][2 * half + e]);
+                    lo[e] = MmaOp<TO>::pack(d[0][j][2 * half + e], d[1][j][2 * half + e]);
+                    hi[e] = MmaOp<TO>::pack(d[2][j][2 * half + e], d[3][j][2 * half + e]);
                 }
                 const bool odd = gq & 1;
                 const unsigned row = (j * RB + half * C::OHB) * C::OTW * kPB;
@@ -382,7 +415,7 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB>::MINB))
 
 template <typename T, int FH, int FW, int G, int NI, int KNB, bool FUSE>
 cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    using C = Cfg<FH, G, NI, KNB>;
+    using C = Cfg<FH, G, NI, KNB, in_es<T>()>;
     if (C::smem + 1024 > 227 * 1024) return cudaErrorNotSupported;
     GeoM g{};
     g.tiles_h = (p.OHs + C::OTH - 1) / C::OTH;
@@ -404,8 +437,11 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     const uint32_t box[4] = {(uint32_t)kCh, (uint32_t)C::SW, (uint32_t)C::HRI, (uint32_t)NI};
     const uint32_t obox[4] = {(uint32_t)kCh, (uint32_t)C::OTW, (uint32_t)C::OTH, (uint32_t)NI};
     CUtensorMap map, omap;
-    if (!encode_tmap_4d(&map, dt, base, dims, str, box, kPB) ||
-        !make_out_map(&omap, p, dt, es, obox, kPB))
+    // FP8: the halo is staged unswizzled (32-byte pixels) and gathered bytewise;
+    // the output is bf16.
+    const dwconv_dtype out_dt = dt == DWCONV_FP8_E4M3 ? DWCONV_BF16 : dt;
+    if (!encode_tmap_4d(&map, dt, base, dims, str, box, sizeof(T) == 1 ? 0 : kPB) ||
+        !make_out_map(&omap, p, out_dt, sizeof(typename OutOf<T>::type), obox, kPB))
         return cudaErrorNotSupported;
     auto kern = tiled_mma_kernel<T, FH, FW, G, NI, KNB, FUSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem + 1024);
