@@ -113,8 +113,8 @@ dwconv_status dwconv_fwd(int N, int H, int W, int C, int FH, int FW, int stride,
  * For S = 1 this is the forward pass over dy with the filter rotated by 180
  * degrees and padding D(FH-1)-P, as §5.1 states; for S > 1 positions that no
  * tap reaches receive 0.  dy [N][OH][OW][C] (OH, OW of an H x W input),
- * w [FH][FW][C], dx [N][H][W][C] (every element written).  Floating dtypes only;
- * DWCONV_INT8 returns DWCONV_ERR_UNSUPPORTED.
+ * w [FH][FW][C], dx [N][H][W][C] (every element written).  fp32, fp16 and bf16;
+ * DWCONV_INT8 and DWCONV_FP8_E4M3 return DWCONV_ERR_UNSUPPORTED.
  */
 dwconv_status dwconv_bwd_data(int N, int H, int W, int C, int FH, int FW, int stride,
                               int dilation, int pad, dwconv_dtype dtype, const void *dy,
@@ -137,7 +137,8 @@ size_t dwconv_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int 
  * repeated calls give bit-identical dw.  x [N][H][W][C], dy [N][OH][OW][C],
  * dw [FH][FW][C] float (fully overwritten).  `workspace` is caller-owned
  * device memory of at least dwconv_bwd_filter_workspace_size() bytes, 256-byte
- * aligned; it may be NULL only if that size is 0.  Floating dtypes only.
+ * aligned; it may be NULL only if that size is 0.  fp32, fp16 and bf16 only
+ * (DWCONV_INT8 and DWCONV_FP8_E4M3: DWCONV_ERR_UNSUPPORTED, workspace size 0).
  */
 dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int stride,
                                 int dilation, int pad, dwconv_dtype dtype, const void *x,
@@ -152,13 +153,15 @@ size_t dwconv_bwd_bias_workspace_size(int N, int OH, int OW, int C);
 
 /*
  * Bias gradient: db[c] = sum over (n,oh,ow) of dy[n,oh,ow,c], the adjoint of
- * adding bias[c] once to every output (the survey's NEXT list; the paper's
- * training passes stop at the input and weight gradients).  dy [N][OH][OW][C]
+ * adding bias[c] once to every output (Flash-DWC §5.1's training passes stop
+ * at the input and weight gradients; a layer with a bias needs this one too).
+ * dy [N][OH][OW][C]
  * in the pass's dtype, db [C] float (fully overwritten).  The N*OH*OW axis is
  * split into slices summed in parallel, then added in a fixed order, so
  * repeated calls give bit-identical db.  `workspace`: caller-owned device
  * memory of at least dwconv_bwd_bias_workspace_size() bytes, 16-byte aligned.
- * Floating dtypes only; DWCONV_INT8 returns DWCONV_ERR_UNSUPPORTED.
+ * fp32, fp16 and bf16 only; DWCONV_INT8 and DWCONV_FP8_E4M3 return
+ * DWCONV_ERR_UNSUPPORTED.
  */
 dwconv_status dwconv_bwd_bias(int N, int OH, int OW, int C, dwconv_dtype dtype, const void *dy,
                               float *db, void *workspace, size_t workspace_bytes, dwconv_stream stream);
