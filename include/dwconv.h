@@ -315,7 +315,9 @@ unsigned long long dwconv_launch_count(void);
  * string: "tiled_mma" (tensor-core Toeplitz, 16-bit 3x3/5x5/7x7),
  * "tiled_mma_large" (tensor-core Toeplitz, large 16-bit filters),
  * "tiled_small" / "tiled_large" (register-tiled FMA kernels), "tiled_wgrad"
- * (tiled weight gradient), "tiled_wgrad_ha" (its hybrid-accumulation form), "direct_fwd" / "direct_dgrad" / "direct_wgrad"
+ * (tiled weight gradient), "tiled_wgrad_ha" (its hybrid-accumulation form),
+ * "tiled_mma_wgrad" (tensor-core weight gradient, large 16-bit filters),
+ * "tiled_wgrad_large" (tap-group weight gradient, other large filters), "direct_fwd" / "direct_dgrad" / "direct_wgrad"
  * (one output per thread), or "none" before the first launch.  The host-side
  * dispatch sets it when it launches; it says nothing about completion.  For
  * reporting which kernel ran (e.g. against which roofline to measure it).
