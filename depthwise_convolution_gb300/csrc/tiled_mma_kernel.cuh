@@ -282,16 +282,36 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
                     stsm_x4(dst(b), v[0], v[1], v[2], v[3]);
                 }
             } else {
-                // (Measured on GB300: issuing the next step's load before this
-                // step's arithmetic, or skipping all-padding steps, is slower.)
-                for (int b = warp; b < kSteps; b += kStride) {
-                    unsigned v[4];
-                    ldsm_x4_trans(v[0], v[1], v[2], v[3], src(b));
+                // Two steps per iteration as in the plain transposition (measured
+                // on GB300: 5 % faster with a ReLU prologue; issuing the next
+                // step's load before this step's arithmetic, or skipping
+                // all-padding steps, was slower).
+                auto keep_of = [&](int b) {
                     const int row = b / (C::SW / 8), chunk = b % (C::SW / 8);
                     const int img = row / C::HRI, ih = ih0 + row - img * C::HRI;
                     const bool rok = ih >= 0 && ih < p.Hs && cur.group * NI + img < p.N;
                     const unsigned m2 = rok ? (cmask >> (2 * chunk)) & 3u : 0u;
-                    const unsigned keep = (m2 & 1u ? 0x0000FFFFu : 0u) | (m2 & 2u ? 0xFFFF0000u : 0u);
+                    return (m2 & 1u ? 0x0000FFFFu : 0u) | (m2 & 2u ? 0xFFFF0000u : 0u);
+                };
+                int b = warp;
+                for (; b + kStride < kSteps; b += 2 * kStride) {
+                    unsigned v[2][4];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        ldsm_x4_trans(v[u][0], v[u][1], v[u][2], v[u][3], src(b + u * kStride));
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const unsigned keep = keep_of(b + u * kStride);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) v[u][m] = prologue_packed<T, PA>(v[u][m], s2[m], t2[m]) & keep;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) stsm_x4(dst(b + u * kStride), v[u][0], v[u][1], v[u][2], v[u][3]);
+                }
+                for (; b < kSteps; b += kStride) {
+                    unsigned v[4];
+                    ldsm_x4_trans(v[0], v[1], v[2], v[3], src(b));
+                    const unsigned keep = keep_of(b);
 #pragma unroll
                     for (int m = 0; m < 4; ++m) v[m] = prologue_packed<T, PA>(v[m], s2[m], t2[m]) & keep;
                     stsm_x4(dst(b), v[0], v[1], v[2], v[3]);
