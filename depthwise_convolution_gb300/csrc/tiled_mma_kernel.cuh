@@ -251,10 +251,9 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
                 // layout ldmatrix.trans gives for 16-bit data -- and converts
                 // each pair exactly to f16.
                 const unsigned char *s8 = smem_raw + (k % NS) * C::s_stride;
-                for (int b = warp; b < kSteps; b += kStride) {
+                auto gather = [&](int b, unsigned (&v)[4]) {
                     const int row = b / (C::SW / 8), col0 = (b % (C::SW / 8)) * 8;
                     const unsigned char *px = s8 + (row * C::SW + col0 + 2 * t4) * kCh + gq;
-                    unsigned v[4];
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         const __nv_fp8x2_storage_t pr =
@@ -262,6 +261,19 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
                         const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
                         v[m] = *reinterpret_cast<const unsigned *>(&h);
                     }
+                };
+                // Two steps per iteration: both gathers before the stores.
+                int b = warp;
+                for (; b + kStride < kSteps; b += 2 * kStride) {
+                    unsigned v[2][4];
+                    gather(b, v[0]);
+                    gather(b + kStride, v[1]);
+                    stsm_x4(dst(b), v[0][0], v[0][1], v[0][2], v[0][3]);
+                    stsm_x4(dst(b + kStride), v[1][0], v[1][1], v[1][2], v[1][3]);
+                }
+                for (; b < kSteps; b += kStride) {
+                    unsigned v[4];
+                    gather(b, v);
                     stsm_x4(dst(b), v[0], v[1], v[2], v[3]);
                 }
             } else if constexpr (PA < 0) {
