@@ -76,7 +76,7 @@ struct GeoWM {
 };
 
 template <typename T, int NFB, int NHB>
-__global__ void __launch_bounds__(kWThreads, 1)
+__global__ void __launch_bounds__(kWThreads, 2)
     tiled_mma_wgrad_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap dy_map,
                            TiledConv p, GeoWM g, float *__restrict__ part, int Zc, unsigned *err) {
     using C = CfgW<NFB, NHB>;
@@ -240,8 +240,8 @@ cudaError_t with_shape(int FH, int FW, F &&f) {
     return cudaErrorNotSupported;
 }
 
-// Shape-only plan: geometry and slices (about one CTA per SM of a 152-SM
-// GB300 over all channel tiles).
+// Shape-only plan: geometry and slices (about one wave of resident CTAs on a
+// 152-SM GB300 over all channel tiles).
 bool plan_wm(const TiledConv &p, dwconv_dtype dt, GeoWM &g, int &Zc) {
     if ((dt != DWCONV_FP16 && dt != DWCONV_BF16) || p.FW < 8) return false;
     g = GeoWM{};
@@ -253,14 +253,16 @@ bool plan_wm(const TiledConv &p, dwconv_dtype dt, GeoWM &g, int &Zc) {
     g.per_ctile = (int)per;
     g.HR = kWOTH + p.FH - 1;
     bool ok = false;
+    int resident = 1;  // CTAs per SM: two by the register bound, fewer if shared memory holds fewer
     with_shape(p.FH, p.FW, [&](auto nfb, auto nhb) {
         using C = CfgW<decltype(nfb)::value, decltype(nhb)::value>;
         g.x_bytes = (unsigned)g.HR * C::SWX * 16;
         ok = C::smem + 1024 <= 227 * 1024 && g.HR <= 256 && C::SWX <= 256;
+        resident = std::max(1, std::min(2, (int)(228 * 1024 / (C::smem + 2048))));
         return cudaSuccess;
     });
     if (!ok) return false;
-    long long z = 152 / g.ctiles;
+    long long z = 152LL * resident / g.ctiles;
     if (z > g.per_ctile) z = g.per_ctile;
     if (z < 1) z = 1;
     Zc = (int)z;
