@@ -55,3 +55,33 @@ def test_module_trains_one_step():
     loss1 = ((layer(x).float() - target) ** 2).mean()
     assert torch.isfinite(loss1) and loss1.item() < loss0.item()
     assert "kernel_size=(7, 7)" in repr(layer)
+
+
+def test_module_same_padding_per_axis():
+    layer = DepthwiseConv2d(16, (5, 51), dtype=torch.float32, device="cpu")
+    assert layer.padding == (2, 25)
+    assert DepthwiseConv2d(16, 7, dilation=2, dtype=torch.float32, device="cpu").padding == (6, 6)
+    assert DepthwiseConv2d(16, 3, padding=0, dtype=torch.float32, device="cpu").padding == 0
+
+
+@pytest.mark.gpu
+def test_strip_layer_keeps_the_map_and_half_accumulate_flows_through():
+    layer = DepthwiseConv2d(32, (51, 5), dtype=torch.float16)
+    x = torch.randn(2, 30, 26, 32, device="cuda").to(torch.float16).requires_grad_()
+    y = layer(x)
+    assert y.shape == x.shape
+    y.float().sum().backward()
+    assert layer.weight.grad is not None and torch.isfinite(layer.weight.grad.float()).all()
+    # the opt-in hybrid accumulation reaches the weight-gradient entry point (7x7 has the HA kernel)
+    # (the backward pass runs on autograd's own thread: compare results, not the
+    # thread-local kernel record)
+    l7 = DepthwiseConv2d(32, 7, bias=False, dtype=torch.float16, half_accumulate=True)
+    x7 = torch.randn(2, 20, 20, 32, device="cuda").to(torch.float16)
+    y7 = l7(x7)
+    dy7 = torch.randn_like(y7)
+    y7.backward(dy7)
+    w = l7.weight.detach()
+    ha = ops.dwconv_bwd_filter(x7, dy7, 7, 7, 1, 1, 3, half_accumulate=True).to(w.dtype)
+    exact = ops.dwconv_bwd_filter(x7, dy7, 7, 7, 1, 1, 3).to(w.dtype)
+    assert torch.equal(l7.weight.grad, ha)
+    assert not torch.equal(ha, exact)
