@@ -52,8 +52,8 @@ using namespace mma;
 #define DWCONV_MMA 1  // 0: leave every shape to the CUDA-core kernels
 #endif
 
-#ifndef DWCONV_MMA_REUSE
-#define DWCONV_MMA_REUSE 4  // G for which half of each A operand is rebuilt from registers (0: none)
+#ifndef DWCONV_MMA_CHAIN_G
+#define DWCONV_MMA_CHAIN_G 4  // largest G whose operands are loaded in chains (half of each from registers)
 #endif
 
 constexpr int kCh = 32;                 // channels per work unit
@@ -339,55 +339,60 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
         __syncthreads();  // T ready, output tile free, this staging buffer free
         if (tid == 0 && u + NS < u_end) issue(k % NS);
 
-        // MMAs.  Stage x loads operand x + 1 (one ahead, also across
-        // channels) and runs the MMAs of operand x, row sets interleaved
-        // (independent accumulators).
+        // MMAs.  Each step loads the next operand (also across channels)
+        // and runs the MMAs of the current one, row sets interleaved
+        // (independent accumulators).  With one image per unit the upper half
+        // of operand x (T rows x + DHT) is the lower half of operand x + DHT,
+        // so the operands of a channel are taken in chains x = r, r + DHT,
+        // r + 2 DHT, ...: a chain's first operand is one ldmatrix.x4, every
+        // later one copies its lower half from registers and loads only its
+        // upper half (one ldmatrix.x2).  Measured on GB300 (bf16 7x7
+        // training layers): a gain at G = 4 (28x28 maps, forward 0.039
+        // against 0.042 ms), a loss at G = 8 (56x56, 0.050 against 0.049 ms),
+        // so chains are used for G <= DWCONV_MMA_CHAIN_G.  The order of the
+        // MMAs on an accumulator is fixed at compile time, so results do not
+        // vary from call to call.
         float d[kChPerWarp][KNB][4];
-        // With kReuse (NI = 1), operand x >= DHT shares its rows-x half with
-        // operand x - DHT (whose rows-(x - DHT + DHT) half it is): that half is
-        // copied from registers and only rows x + DHT are loaded (one
-        // ldmatrix.x2).  Measured: a gain for G = 4; for G = 8 the extra
-        // registers spill.
-        constexpr bool kReuse = DWCONV_MMA_REUSE == G && NI == 1;
-        unsigned A[kReuse ? kChPerWarp : 1][kReuse ? NQ : 2][4];
-        auto load_a = [&](int ci, int x) {
-            const unsigned base = t_addr + 2u * ((warp * kChPerWarp + ci) * C::CS + x * C::RS);
-            if constexpr (kReuse) {
-                if (x < DHT) {
-                    ldsm_x4(A[ci][x][0], A[ci][x][1], A[ci][x][2], A[ci][x][3], base + 2u * lane_off);
-                } else {
-                    A[ci][x][0] = A[ci][x - DHT][1];
-                    A[ci][x][2] = A[ci][x - DHT][3];
-                    ldsm_x2(A[ci][x][1], A[ci][x][3], base + 2u * lane_off2);
-                }
-            } else {
-                const int sl = (ci * NQ + x) & 1;  // stage number (over all channels) mod 2
-                ldsm_x4(A[0][sl][0], A[0][sl][1], A[0][sl][2], A[0][sl][3], base + 2u * lane_off);
-            }
-        };
-        load_a(0, 0);
+        constexpr bool kChain = NI == 1 && G <= DWCONV_MMA_CHAIN_G;
+        constexpr int NR = kChain ? (DHT < NQ ? DHT : NQ) : 1;  // chains per channel
+        constexpr int XS = kChain ? DHT : 1;                      // operand step within a chain
+        auto op_addr = [&](int ci, int x) { return t_addr + 2u * ((warp * kChPerWarp + ci) * C::CS + x * C::RS); };
+        unsigned a[4], an[4];
+        ldsm_x4(a[0], a[1], a[2], a[3], op_addr(0, 0) + 2u * lane_off);
 #pragma unroll
         for (int ci = 0; ci < kChPerWarp; ++ci) {
 #pragma unroll
             for (int j = 0; j < KNB; ++j) d[ci][j][0] = d[ci][j][1] = d[ci][j][2] = d[ci][j][3] = bias_r[ci];
 #pragma unroll
-            for (int x = 0; x < NQ; ++x) {
-                if (x + 1 < NQ)
-                    load_a(ci, x + 1);
-                else if (ci + 1 < kChPerWarp)
-                    load_a(ci + 1, 0);
-                const unsigned *a;
-                if constexpr (kReuse)
-                    a = A[ci][x];
-                else
-                    a = A[0][(ci * NQ + x) & 1];
+            for (int r = 0; r < NR; ++r)
 #pragma unroll
-                for (int j = 0; j < KNB; ++j) {
-                    const int fh = x - j * RB;
-                    if (fh >= 0 && fh < FH)
-                        Op::run(d[ci][j], a[0], a[1], a[2], a[3], bfr[ci][fh][0], bfr[ci][fh][1]);
+                for (int x = r; x < NQ; x += XS) {
+                    bool next = true;
+                    if (x + XS < NQ) {
+                        if constexpr (kChain) {
+                            an[0] = a[1];
+                            an[2] = a[3];
+                            ldsm_x2(an[1], an[3], op_addr(ci, x + XS) + 2u * lane_off2);
+                        } else {
+                            ldsm_x4(an[0], an[1], an[2], an[3], op_addr(ci, x + 1) + 2u * lane_off);
+                        }
+                    } else if (r + 1 < NR) {
+                        ldsm_x4(an[0], an[1], an[2], an[3], op_addr(ci, r + 1) + 2u * lane_off);
+                    } else if (ci + 1 < kChPerWarp) {
+                        ldsm_x4(an[0], an[1], an[2], an[3], op_addr(ci + 1, 0) + 2u * lane_off);
+                    } else {
+                        next = false;
+                    }
+#pragma unroll
+                    for (int j = 0; j < KNB; ++j) {
+                        const int fh = x - j * RB;
+                        if (fh >= 0 && fh < FH)
+                            Op::run(d[ci][j], a[0], a[1], a[2], a[3], bfr[ci][fh][0], bfr[ci][fh][1]);
+                    }
+                    if (next)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) a[e] = an[e];
                 }
-            }
         }
 
         // Epilogue of the fused forward pass: per-channel affine map and
