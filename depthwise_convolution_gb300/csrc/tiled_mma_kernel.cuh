@@ -200,7 +200,13 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
             }
         }
         if (!mbar_wait(&bar[k % NS], (k / NS) & 1)) {
+            // Give up on this unit; thread 0 lets its copies in flight end
+            // (again with bounded waits) before the CTA leaves.
             report_timeout(err);
+            if (tid == 0) {
+                for (int j = k; j < k + NS && u_begin + j < u_end; ++j) mbar_wait(&bar[j % NS], (j / NS) & 1);
+                asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+            }
             return;
         }
 

@@ -147,7 +147,12 @@ __global__ void __launch_bounds__(kLThreads, 1)
             bias_c = (p.bias && cc < p.C) ? p.bias[cc] : 0.f;
         }
         if (!mbar_wait(&bar, k & 1)) {
+            // Thread 0 lets the copies in flight end (bounded) before leaving.
             report_timeout(err);
+            if (tid == 0) {
+                mbar_wait(&bar, k & 1);
+                asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+            }
             return;
         }
         // Transpose S[row][col][8 ch] -> T[ch][row][col], four 8-column blocks
