@@ -29,6 +29,7 @@ SIGNATURES = {
     "dwconv_bwd_filter": (_I, [_I] * 9 + [_I, _P, _P, _P, _P, _SZ, _P]),
     "dwconv_bwd_filter_static": (_I, [_I] * 9 + [_I, _P, _P, _P, _P]),
     "dwconv_check_device_errors": (_I, [_P]),
+    "dwconv_selftest_timeout": (_I, [_P]),
     "dwconv_status_string": (ctypes.c_char_p, [_I]),
     "dwconv_bwd_bias_workspace_size": (ctypes.c_size_t, [_I] * 4),
     "dwconv_bwd_bias": (_I, [_I] * 4 + [_I, _P, _P, _P, ctypes.c_size_t, _P]),

@@ -257,6 +257,13 @@ def dwconv_check_device_errors(stream=None) -> None:
     _lib.check(_lib.load().dwconv_check_device_errors(_stream(stream)), "dwconv_check_device_errors")
 
 
+def dwconv_selftest_timeout(stream=None) -> None:
+    """Enqueue the library's failure-detection self-test: a bounded wait that
+    runs out (no fault, no hang); the next dwconv_check_device_errors raises
+    DwconvError with DWCONV_ERR_TIMEOUT."""
+    _lib.check(_lib.load().dwconv_selftest_timeout(_stream(stream)), "dwconv_selftest_timeout")
+
+
 def dwconv_launch_count() -> int:
     """Kernels libdwconv has launched in this process."""
     return int(_lib.load().dwconv_launch_count())

@@ -210,6 +210,17 @@ dwconv_status dwconv_bwd_filter_static(int N, int H, int W, int C, int FH, int F
 dwconv_status dwconv_check_device_errors(dwconv_stream stream);
 
 /*
+ * Self-test of that failure detection: enqueues on `stream` one thread that
+ * waits, with a short bound (milliseconds), on a shared-memory barrier that
+ * nothing completes -- the kind of wait the tiled kernels make for their
+ * copies -- gives up and records the timeout as they would.  No fault, no
+ * hang; caller memory is not touched.  The next dwconv_check_device_errors
+ * returns DWCONV_ERR_TIMEOUT (and clears the record).  Returns DWCONV_OK once
+ * enqueued, DWCONV_ERR_CUDA if the launch fails.
+ */
+dwconv_status dwconv_selftest_timeout(dwconv_stream stream);
+
+/*
  * Per-axis forms.  Each _2d entry point is the operation of the entry point of
  * the same name with the stride, dilation and padding given separately for
  * the H and W axes: taps read x[n, oh*stride_h - pad_h + fh*dilation_h,
