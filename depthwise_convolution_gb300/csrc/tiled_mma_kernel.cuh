@@ -10,8 +10,10 @@
 //
 // a 16 x 8 Toeplitz band of the filter row.  One warp-level mma.sync
 // m16n8k16 (bf16/fp16 in, fp32 accumulate) takes 16 groups at once, in two
-// blocks of 8 M rows; a block is G groups of each of 8/G consecutive output
-// rows (G = 8 on maps wider than 32 columns, 4 above 16, 2 above 8).
+// blocks of 8 M rows; a block is G groups of each of 8/G output rows spaced G
+// apart (G = 8 on maps wider than 32 columns, 4 above 16, 2 above 8): with
+// that spacing the 8 row addresses of every operand matrix fall in distinct
+// shared-memory banks (adjacent rows put two of them in one bank for G < 8).
 // A channel's output block needs FH such MMAs (one per filter row); the
 // accumulator stays in registers across them, so every partial sum is kept in
 // fp32 and the bias is added once, at the start.
@@ -29,8 +31,8 @@
 //      T[channel][row][column], in which the 8 windows of an 8-row matrix of
 //      an MMA operand are 8 rows of 16 bytes (one ldmatrix matrix);
 //   3. the A operands of the KNB row sets x FH filter rows overlap: MMA (row
-//      set j, filter row fh) reads rows from x = j*8/G + fh on, so the operand
-//      of x (one ldmatrix.x4) serves every (j, fh) with that x;
+//      set j, filter row fh) reads rows from x = base(j) + fh on, so the
+//      operand of x (one ldmatrix.x4) serves every (j, fh) with that x;
 //   4. B (the Toeplitz bands of the warp's 4 channels) stays in registers for
 //      all units of a channel tile;
 //   5. the results, rounded to 16 bits, go to a separate 64B-swizzled NHWC
@@ -79,7 +81,11 @@ struct Cfg {
     static constexpr int TR = NI * HRI, SW = OTW + 8;             // staged rows, columns
     static constexpr int RS = SW;                                 // T row stride (halves)
     static constexpr int CS = channel_stride(TR * RS);            // T channel stride (halves)
-    static constexpr int NQ = (KNB - 1) * RB + FH;                // A operands per channel
+    // Row set j covers output rows base(j) + G i, i < RB (and the same rows
+    // OHB lower for M rows 8-15); the KNB sets tile the rows exactly when KNB
+    // is a multiple of G (or G = 8, one row per block).
+    __host__ __device__ static constexpr int base(int j) { return j % G + 8 * (j / G); }
+    static constexpr int NQ = base(KNB - 1) + FH;                 // A operands per channel
     static constexpr unsigned s_bytes = TR * SW * kCh * ES;
     static constexpr unsigned s_stride = align1k(s_bytes);
     static constexpr unsigned t_bytes = align1k(kCh * CS * 2);
@@ -110,7 +116,8 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
     tiled_mma_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap out_map,
                      TiledConv p, GeoM g, unsigned *err) {
     using C = Cfg<FH, G, NI, KNB, in_es<T>()>;
-    constexpr int RB = C::RB, DHT = C::DHT, NQ = C::NQ, NS = C::NS;
+    constexpr int DHT = C::DHT, NQ = C::NQ, NS = C::NS;
+    static_assert(G == 8 || KNB % G == 0, "row sets must tile the unit's rows");
     extern __shared__ __align__(1024) unsigned char smem_dyn[];
     __shared__ __align__(8) uint64_t bar[NS];
     using TM = typename MmaIn<T>::type;   // MMA operand type
@@ -152,19 +159,19 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
 
     // A operand x of a channel = one ldmatrix.x4: matrix j (lanes 8j..8j+7
     // give its row addresses) holds M rows 8(j%2)..+7 and k 8(j/2)..+7; M row
-    // i of block j%2 is window i % G of T row x + i / G + DHT (j%2).
+    // i of block j%2 is window i % G of T row x + G (i / G) + DHT (j%2).
     const int mj = lane / 8, mi = lane % 8;
-    const int lane_off = ((mj & 1) * DHT + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj >> 1);
+    const int lane_off = ((mj & 1) * DHT + (mi / G) * G) * C::RS + 8 * (mi % G) + 8 * (mj >> 1);
     // ldmatrix.x2 of T rows x + DHT alone: matrix mj & 1 = k half.
-    const int lane_off2 = (DHT + mi / G) * C::RS + 8 * (mi % G) + 8 * (mj & 1);
+    const int lane_off2 = (DHT + (mi / G) * G) * C::RS + 8 * (mi % G) + 8 * (mj & 1);
     // Transposition: one ldmatrix.x4 = the 4 16-byte channel chunks of 8
     // pixels; this lane addresses row tr of matrix tj.
     const int tr = lane % 8, tj = lane / 8;
-    // Output: lane (gq, t4) writes position (row gq / G (+ OHB for M rows
+    // Output: lane (gq, t4) writes position (row G (gq / G) (+ OHB for M rows
     // 8-15), column 8 (gq % G) + 2t4 + e) of each row set; the bits the
     // swizzle reads (7 and up) do not depend on the row set or on e, so the
     // lane's swizzled chunk is fixed.
-    const unsigned o_pos = (unsigned)((gq / G) * C::OTW + 8 * (gq % G) + 2 * t4) * kPB;
+    const unsigned o_pos = (unsigned)((gq / G) * G * C::OTW + 8 * (gq % G) + 2 * t4) * kPB;
     const unsigned o_lane = o_addr + swz(o_pos + (unsigned)warp * 8);
     const unsigned o_lane0 = o_lane + (gq & 1) * kPB, o_lane1 = o_lane + (1 - (gq & 1)) * kPB;
 
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
                     }
 #pragma unroll
                     for (int j = 0; j < KNB; ++j) {
-                        const int fh = x - j * RB;
+                        const int fh = x - C::base(j);
                         if (fh >= 0 && fh < FH)
                             Op::run(d[ci][j], a[0], a[1], a[2], a[3], bfr[ci][fh][0], bfr[ci][fh][1]);
                     }
@@ -433,7 +440,7 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
                     hi[e] = MmaOp<TO>::pack(d[2][j][2 * half + e], d[3][j][2 * half + e]);
                 }
                 const bool odd = gq & 1;
-                const unsigned row = (j * RB + half * C::OHB) * C::OTW * kPB;
+                const unsigned row = (C::base(j) + half * C::OHB) * C::OTW * kPB;
                 asm volatile("st.shared.v2.b32 [%0], {%1, %2};\n" ::"r"(o_lane0 + row), "r"(odd ? lo[1] : lo[0]),
                              "r"(odd ? hi[1] : hi[0])
                              : "memory");
