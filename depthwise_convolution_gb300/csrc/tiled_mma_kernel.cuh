@@ -360,9 +360,9 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
         // r + 2 DHT, ...: a chain's first operand is one ldmatrix.x4, every
         // later one copies its lower half from registers and loads only its
         // upper half (one ldmatrix.x2).  Measured on GB300 (bf16 7x7
-        // training layers): a gain at G = 4 (28x28 maps, forward 0.039
-        // against 0.042 ms), a loss at G = 8 (56x56, 0.050 against 0.049 ms),
-        // so chains are used for G <= DWCONV_MMA_CHAIN_G.  The order of the
+        // training layers): a small gain at G = 4 (28x28 maps, forward + dgrad
+        // 0.068 against 0.069 ms), a loss at G = 8 (56x56, forward 0.050
+        // against 0.049 ms), so chains are used for G <= DWCONV_MMA_CHAIN_G.  The order of the
         // MMAs on an accumulator is fixed at compile time, so results do not
         // vary from call to call.
         float d[kChPerWarp][KNB][4];
