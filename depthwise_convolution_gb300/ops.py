@@ -35,16 +35,26 @@ def _code(t: torch.Tensor) -> int:
         raise TypeError(f"unsupported dtype {t.dtype}") from None
 
 
-def _dev(t: torch.Tensor, name: str, ndim: int) -> int:
+def _dev(t: torch.Tensor, name: str, ndim: int, ref: torch.Tensor = None) -> int:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if ref is not None and t.device != ref.device:
+        raise ValueError(f"{name} must be on {ref.device}, like the input")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dimensions, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous (channels-last dense layout)")
     return t.data_ptr()
+
+
+def _on(t: torch.Tensor):
+    """The library works on the current device: make t's device current for the call
+    (the default stream is then that device's current stream)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("inputs must be CUDA tensors")
+    return torch.cuda.device(t.device)
 
 
 def _stream(stream) -> int:
@@ -95,10 +105,11 @@ def dwconv_fwd(x, w, bias=None, stride=1, dilation=1, pad=0, out=None, stream=No
         out = torch.empty((N, OH, OW, C), dtype=y_dtype, device=x.device)
     elif out.dtype != y_dtype or tuple(out.shape) != (N, OH, OW, C):
         raise ValueError("out has the wrong shape or dtype")
-    _lib.check(_lib.load().dwconv_fwd_2d(
-        N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
-        _dev(x, "x", 4), _dev(w, "w", 3), None if bias is None else _dev(bias, "bias", 1),
-        _dev(out, "out", 4), _stream(stream)), "dwconv_fwd")
+    with _on(x):
+        _lib.check(_lib.load().dwconv_fwd_2d(
+            N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
+            _dev(x, "x", 4), _dev(w, "w", 3, x), None if bias is None else _dev(bias, "bias", 1, x),
+            _dev(out, "out", 4, x), _stream(stream)), "dwconv_fwd")
     return out
 
 
@@ -111,12 +122,12 @@ def _act(a) -> int:
     return int(a)
 
 
-def _vec(v, C, name):
+def _vec(v, C, name, ref):
     if v is None:
         return None
     if v.dtype != torch.float32 or tuple(v.shape) != (C,):
         raise ValueError(f"{name} must be [C] float32")
-    return _dev(v, name, 1)
+    return _dev(v, name, 1, ref)
 
 
 def dwconv_fwd_fused(x, w, bias=None, in_scale=None, in_shift=None, in_act="none", out_scale=None,
@@ -144,12 +155,13 @@ def dwconv_fwd_fused(x, w, bias=None, in_scale=None, in_shift=None, in_act="none
         out = torch.empty((N, OH, OW, C), dtype=y_dtype, device=x.device)
     elif out.dtype != y_dtype or tuple(out.shape) != (N, OH, OW, C):
         raise ValueError("out has the wrong shape or dtype")
-    _lib.check(_lib.load().dwconv_fwd_fused_2d(
-        N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
-        _dev(x, "x", 4), _vec(in_scale, C, "in_scale"), _vec(in_shift, C, "in_shift"), ia,
-        _dev(w, "w", 3), None if bias is None else _dev(bias, "bias", 1),
-        _vec(out_scale, C, "out_scale"), _vec(out_shift, C, "out_shift"), oa,
-        _dev(out, "out", 4), _stream(stream)), "dwconv_fwd_fused")
+    with _on(x):
+        _lib.check(_lib.load().dwconv_fwd_fused_2d(
+            N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
+            _dev(x, "x", 4), _vec(in_scale, C, "in_scale", x), _vec(in_shift, C, "in_shift", x), ia,
+            _dev(w, "w", 3, x), None if bias is None else _dev(bias, "bias", 1, x),
+            _vec(out_scale, C, "out_scale", x), _vec(out_shift, C, "out_shift", x), oa,
+            _dev(out, "out", 4, x), _stream(stream)), "dwconv_fwd_fused")
     return out
 
 
@@ -166,9 +178,11 @@ def dwconv_bwd_data(dy, w, H, W, stride=1, dilation=1, pad=0, out=None, stream=N
         out = torch.empty((N, H, W, C), dtype=dy.dtype, device=dy.device)
     elif out.dtype != dy.dtype or tuple(out.shape) != (N, H, W, C):
         raise ValueError("out has the wrong shape or dtype")
-    _lib.check(_lib.load().dwconv_bwd_data_2d(
-        N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
-        _dev(dy, "dy", 4), _dev(w, "w", 3), _dev(out, "out", 4), _stream(stream)), "dwconv_bwd_data")
+    with _on(dy):
+        _lib.check(_lib.load().dwconv_bwd_data_2d(
+            N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
+            _dev(dy, "dy", 4), _dev(w, "w", 3, dy), _dev(out, "out", 4, dy), _stream(stream)),
+            "dwconv_bwd_data")
     return out
 
 
@@ -200,11 +214,12 @@ def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, work
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     fn = _lib.load().dwconv_bwd_filter_ha_2d if half_accumulate else _lib.load().dwconv_bwd_filter_2d
-    _lib.check(fn(
-        N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
-        _dev(x, "x", 4), _dev(dy, "dy", 4), _dev(out, "out", 3),
-        workspace.data_ptr(), ws_bytes, _stream(stream)),
-        "dwconv_bwd_filter_ha" if half_accumulate else "dwconv_bwd_filter")
+    with _on(x):
+        _lib.check(fn(
+            N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
+            _dev(x, "x", 4), _dev(dy, "dy", 4, x), _dev(out, "out", 3, x),
+            _dev(workspace, "workspace", workspace.dim(), x), ws_bytes, _stream(stream)),
+            "dwconv_bwd_filter_ha" if half_accumulate else "dwconv_bwd_filter")
     return out
 
 
@@ -224,9 +239,10 @@ def dwconv_bwd_bias(dy, out=None, workspace=None, stream=None):
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dy.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _lib.check(_lib.load().dwconv_bwd_bias(
-        N, OH, OW, C, dt, _dev(dy, "dy", 4), _dev(out, "out", 1), workspace.data_ptr(), ws_bytes,
-        _stream(stream)), "dwconv_bwd_bias")
+    with _on(dy):
+        _lib.check(_lib.load().dwconv_bwd_bias(
+            N, OH, OW, C, dt, _dev(dy, "dy", 4), _dev(out, "out", 1, dy),
+            _dev(workspace, "workspace", workspace.dim(), dy), ws_bytes, _stream(stream)), "dwconv_bwd_bias")
     return out
 
 
@@ -245,10 +261,11 @@ def dwconv_bwd_filter_static(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=Non
         out = torch.empty((FH, FW, C), dtype=torch.float32, device=x.device)
     elif out.dtype != torch.float32 or tuple(out.shape) != (FH, FW, C):
         raise ValueError("out must be [FH, FW, C] float32")
-    _lib.check(_lib.load().dwconv_bwd_filter_static(
-        N, H, W, C, FH, FW, stride, dilation, pad, dt,
-        _dev(x, "x", 4), _dev(dy, "dy", 4), _dev(out, "out", 3), _stream(stream)),
-        "dwconv_bwd_filter_static")
+    with _on(x):
+        _lib.check(_lib.load().dwconv_bwd_filter_static(
+            N, H, W, C, FH, FW, stride, dilation, pad, dt,
+            _dev(x, "x", 4), _dev(dy, "dy", 4, x), _dev(out, "out", 3, x), _stream(stream)),
+            "dwconv_bwd_filter_static")
     return out
 
 
