@@ -205,3 +205,12 @@ def test_python_binding_rejects_cpu_tensors():
     w = torch.zeros(3, 3, 8, dtype=torch.float16)
     with pytest.raises(ValueError):
         ops.dwconv_fwd(x, w, pad=1)
+
+
+def test_device_entry_points_report_a_missing_gpu_as_a_cuda_error(lib):
+    # Without a GPU the failure-detection entry points return a status (nothing is launched).
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the GPU tests cover these calls")
+    assert lib.dwconv_selftest_timeout(None) == _lib.ERR_CUDA
+    assert lib.dwconv_check_device_errors(None) == _lib.ERR_CUDA
