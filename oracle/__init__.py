@@ -31,9 +31,12 @@ Contents
     The arithmetic the pages print: halo extents, storage budgets, the GEMM
     traffic model, and the Flash-DWC tile-model closed forms.
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` against values
-the pages print, closed forms, special cases and brute force; none is left
-"parity unpinned".
+Every function here is pinned by ``tests/test_oracle_pins.py`` (the int64
+loops, the page arithmetic, the fused and FP8 helpers) and
+``tests/test_oracle_float_pins.py`` (the float64 loops and the magnitude
+``mag``) against values the pages print, closed forms, special cases, brute
+force and PyTorch's float64 convolution gradients; none is left "parity
+unpinned".
 """
 from __future__ import annotations
 
