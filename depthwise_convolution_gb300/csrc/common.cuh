@@ -30,6 +30,17 @@ void note_kernel(const char *family);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// SM count and shared memory per SM that a split-reduction plan is sized for.
+// Workspace sizes are pure functions of the shape, so they are planned for an
+// upper bound (kPlanMaxSms SMs: sm_103a parts have at most 160; 228 KB of
+// shared memory per SM); a launch plans for the current device, capped at
+// those bounds, so the slices it writes never outnumber the ones its
+// workspace was sized for.
+constexpr int kPlanMaxSms = 160;
+constexpr int kPlanMaxSmemPerSm = 228 * 1024;
+int plan_sms(bool launch);
+int plan_smem_per_sm(bool launch);
+
 // ---- element access --------------------------------------------------------
 
 // Two adjacent channels of one storage type, widened to / narrowed from float2.
@@ -321,8 +332,9 @@ cudaError_t launch_wgrad_reduce(const float *part, int Z, long long count, float
                                 cudaStream_t st);
 // Bias gradient, first pass: part[z][c] = sum of dy over the positions of
 // slice z of the P = N*OH*OW positions (the second pass is launch_wgrad_reduce
-// with count = C).  bias_slices() is a pure function of the shape.
-int bias_slices(long long P, int C);
+// with count = C).  bias_slices(P, C, false) is a pure function of the shape
+// (the workspace size); a launch uses bias_slices(P, C, true) <= that.
+int bias_slices(long long P, int C, bool launch);
 cudaError_t launch_bias_slices(long long P, int C, dwconv_dtype dt, const void *dy, float *part, int Z,
                                cudaStream_t st);
 

@@ -209,9 +209,9 @@ __global__ void __launch_bounds__(256) bias_slice_kernel(const T *__restrict__ d
 
 }  // namespace
 
-int bias_slices(long long P, int C) {
+int bias_slices(long long P, int C, bool launch) {
     const long long cblocks = (C + 31) / 32;
-    long long z = (4LL * 152 + cblocks - 1) / cblocks;  // about 4 blocks per SM of a GB300
+    long long z = (4LL * plan_sms(launch) + cblocks - 1) / cblocks;  // about 4 blocks per SM
     if (z > P) z = P;
     if (z > 4096) z = 4096;
     return (int)(z < 1 ? 1 : z);

@@ -17,6 +17,7 @@ namespace {
 std::atomic<unsigned long long> g_launches{0};
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_smem_per_sm[kMaxDevices];
 }  // namespace
 
 void note_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
@@ -36,6 +37,21 @@ int sm_count() {
         g_sm_count[dev].store(v, std::memory_order_relaxed);
     }
     return v;
+}
+
+int plan_sms(bool launch) { return launch ? std::min(sm_count(), kPlanMaxSms) : kPlanMaxSms; }
+
+int plan_smem_per_sm(bool launch) {
+    if (!launch) return kPlanMaxSmemPerSm;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kPlanMaxSmemPerSm;
+    int v = g_smem_per_sm[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || v <= 0)
+            v = kPlanMaxSmemPerSm;
+        g_smem_per_sm[dev].store(v, std::memory_order_relaxed);
+    }
+    return std::min(v, kPlanMaxSmemPerSm);
 }
 
 namespace {
@@ -141,12 +157,15 @@ cudaError_t launch_tall_strip(const TiledConv &p, dwconv_dtype dt, cudaStream_t 
     return e;
 }
 
-// wgrad split: slices of the N*OH*OW axis.  A pure function of the shape so
-// that the workspace size can be computed without a device.
-int wgrad_slices(const Shape &s) {
+// wgrad split of the direct path: slices of the N*OH*OW axis.  With
+// launch = false a pure function of the shape, so that the workspace size can
+// be computed without a device; a launch plans for the current device's SMs
+// (never more slices than the workspace holds).
+int wgrad_slices(const Shape &s, bool launch) {
     const long long positions = (long long)s.N * s.OH * s.OW;
     const long long per_slice_blocks = (long long)((s.C + 31) / 32) * s.FH * s.FW;
-    long long z = (1216 + per_slice_blocks - 1) / per_slice_blocks;  // ~8 blocks per SM
+    const long long blocks = 8LL * plan_sms(launch);                  // ~8 blocks per SM
+    long long z = (blocks + per_slice_blocks - 1) / per_slice_blocks;
     long long zmax = positions / 256;                                 // >= 256 positions a slice
     if (zmax < 1) zmax = 1;
     if (z > zmax) z = zmax;
@@ -395,7 +414,7 @@ size_t dwconv_bwd_filter_workspace_size_2d(int N, int H, int W, int C, int FH, i
     if (make_shape(N, H, W, C, FH, FW, stride_h, stride_w, dilation_h, dilation_w, pad_h, pad_w, s) != DWCONV_OK)
         return 0;
     const size_t per_slice = (size_t)FH * FW * C * sizeof(float);
-    size_t need = (size_t)wgrad_slices(s) * per_slice;
+    size_t need = (size_t)wgrad_slices(s, false) * per_slice;
     TiledConv p;
     if (wgrad_tiled_params(s, dtype, nullptr, nullptr, nullptr, p)) {
         const size_t tiled = (size_t)wgrad_tiled_plan(p, dtype) * per_slice;
@@ -446,7 +465,7 @@ dwconv_status bwd_filter_impl(int N, int H, int W, int C, int FH, int FW, int st
     }
     // Shapes without a tiled instance take the exact fp32 path, also for the
     // hybrid-accumulation entry point (its bound holds a fortiori).
-    const int Z = wgrad_slices(s);
+    const int Z = wgrad_slices(s, true);
     cudaError_t e = launch_wgrad_direct(s, dtype, x, dy, part, Z, cs);
     if (e != cudaSuccess) return DWCONV_ERR_CUDA;
     return cuda_status(launch_wgrad_reduce(part, Z, (long long)FH * FW * C, dw, cs));
@@ -491,7 +510,7 @@ size_t dwconv_bwd_bias_workspace_size(int N, int OH, int OW, int C) {
     if (N < 1 || OH < 1 || OW < 1 || C < 1) return 0;
     const long long P = (long long)N * OH * OW;
     if (P > (1LL << 40) || (long long)C * P > (1LL << 50)) return 0;
-    return (size_t)bias_slices(P, C) * (size_t)C * sizeof(float);
+    return (size_t)bias_slices(P, C, false) * (size_t)C * sizeof(float);
 }
 
 dwconv_status dwconv_bwd_bias(int N, int OH, int OW, int C, dwconv_dtype dtype, const void *dy, float *db,
@@ -504,7 +523,7 @@ dwconv_status dwconv_bwd_bias(int N, int OH, int OW, int C, dwconv_dtype dtype, 
     if (!aligned(dy, elem_size(dtype)) || !aligned(db, 4) || !aligned(workspace, 16)) return DWCONV_ERR_MISALIGNED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const long long P = (long long)N * OH * OW;
-    const int Z = bias_slices(P, C);
+    const int Z = bias_slices(P, C, true);
     float *part = static_cast<float *>(workspace);
     cudaError_t e = launch_bias_slices(P, C, dtype, dy, part, Z, cs);
     if (e != cudaSuccess) return cuda_status(e);

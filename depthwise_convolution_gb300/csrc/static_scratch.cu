@@ -15,10 +15,14 @@
 // name as a device address (on the host the name denotes a host-side shadow
 // object), so the first call on each device asks the runtime for the array's
 // device address with cudaGetSymbolAddress, with that device current, and
-// caches it; later calls on that device reuse the cached address.
+// caches it; later calls on that device reuse the cached address.  The cache
+// remembers which context the address belongs to: after a device reset the
+// module is loaded again into a new context, possibly elsewhere, and the next
+// call looks the address up again.
 #include <mutex>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace {
 
@@ -27,20 +31,25 @@ static __device__ __align__(256) unsigned char g_scratch[DWCONV_STATIC_SCRATCH_B
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices];  // device address of g_scratch, per device
+void *g_scratch_addr[kMaxDevices];            // device address of g_scratch, per device
+unsigned long long g_scratch_ctx[kMaxDevices];  // the context that address belongs to
 
-// Device address of g_scratch on the current device, looked up once per device.
+// Device address of g_scratch on the current device, looked up once per
+// device and context.
 cudaError_t scratch_address(void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const unsigned long long ctx = dwc::current_context_id();
+    if (!ctx) return cudaErrorInvalidValue;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_addr[dev];
     return cudaSuccess;

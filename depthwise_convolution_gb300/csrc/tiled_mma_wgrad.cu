@@ -240,9 +240,9 @@ cudaError_t with_shape(int FH, int FW, F &&f) {
     return cudaErrorNotSupported;
 }
 
-// Shape-only plan: geometry and slices (about one wave of resident CTAs on a
-// 152-SM GB300 over all channel tiles).
-bool plan_wm(const TiledConv &p, dwconv_dtype dt, GeoWM &g, int &Zc) {
+// Plan: geometry and slices (about one wave of resident CTAs over all channel
+// tiles), for the workspace bound or the current device (plan_sms).
+bool plan_wm(const TiledConv &p, dwconv_dtype dt, GeoWM &g, int &Zc, bool launch) {
     if ((dt != DWCONV_FP16 && dt != DWCONV_BF16) || p.FW < 8) return false;
     g = GeoWM{};
     g.tiles_h = (p.OHs + kWOTH - 1) / kWOTH;
@@ -258,11 +258,11 @@ bool plan_wm(const TiledConv &p, dwconv_dtype dt, GeoWM &g, int &Zc) {
         using C = CfgW<decltype(nfb)::value, decltype(nhb)::value>;
         g.x_bytes = (unsigned)g.HR * C::SWX * 16;
         ok = C::smem + 1024 <= 227 * 1024 && g.HR <= 256 && C::SWX <= 256;
-        resident = std::max(1, std::min(2, (int)(228 * 1024 / (C::smem + 2048))));
+        resident = std::max(1, std::min(2, (int)(plan_smem_per_sm(launch) / (C::smem + 2048))));
         return cudaSuccess;
     });
     if (!ok) return false;
-    long long z = 152LL * resident / g.ctiles;
+    long long z = (long long)plan_sms(launch) * resident / g.ctiles;
     if (z > g.per_ctile) z = g.per_ctile;
     if (z < 1) z = 1;
     Zc = (int)z;
@@ -307,13 +307,13 @@ cudaError_t run_wm(const TiledConv &p, dwconv_dtype dt, const GeoWM &g, int Zc, 
 int tiled_mma_wgrad_slices(const TiledConv &p, dwconv_dtype dt) {
     GeoWM g;
     int Zc = 0;
-    return DWCONV_MMA_WGRAD && plan_wm(p, dt, g, Zc) ? Zc : 0;
+    return DWCONV_MMA_WGRAD && plan_wm(p, dt, g, Zc, false) ? Zc : 0;
 }
 
 cudaError_t launch_tiled_mma_wgrad(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st) {
     GeoWM g;
     int Zc = 0;
-    if (!DWCONV_MMA_WGRAD || !plan_wm(p, dt, g, Zc)) return cudaErrorNotSupported;
+    if (!DWCONV_MMA_WGRAD || !plan_wm(p, dt, g, Zc, true)) return cudaErrorNotSupported;
     return with_shape(p.FH, p.FW, [&](auto nfb, auto nhb) {
         constexpr int NFB = decltype(nfb)::value, NHB = decltype(nhb)::value;
         return dt == DWCONV_FP16 ? run_wm<__half, NFB, NHB>(p, dt, g, Zc, part, st)

@@ -220,19 +220,21 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
 }
 
-// Shape-only plan: which instance, its geometry, and the slice count Zc --
-// about one full wave: 152 SMs x the CTAs of this instance that fit on an SM
-// (its register bound MINB, or fewer if shared memory holds fewer).
+// Plan: which instance, its geometry, and the slice count Zc -- about one
+// full wave: the SMs x the CTAs of this instance that fit on an SM (its
+// register bound MINB, or fewer if shared memory holds fewer).  Planned for
+// the bounds of plan_sms / plan_smem_per_sm (workspace size) or the current
+// device (launch), so the launch's Zc never exceeds the workspace's.
 template <typename T, int FH, int FW, int TH, int TW, int MINB>
-bool plan_geo(const TiledConv &p, Geo &g, int &Zc, size_t &smem) {
+bool plan_geo(const TiledConv &p, Geo &g, int &Zc, size_t &smem, bool launch) {
     g = make_geo(p, TH, TW, sizeof(T), true, sizeof(T) == 2 ? DWCONV_W16_SMEM_KB * 1024 : 110 * 1024);
     if (g.units == 0) return false;
     smem = stage_bytes(g, TH, TW, sizeof(T), true);
     const size_t red_bytes = (size_t)(kThreads / 32) * FH * FW * 16 * sizeof(float2);
     if (smem < red_bytes) smem = red_bytes;
     if (smem > 220 * 1024) return false;
-    const int resident = std::max(1, std::min(MINB, (int)(228 * 1024 / (smem + 1024))));
-    int z = 152 * resident / g.ctiles;
+    const int resident = std::max(1, std::min(MINB, (int)(plan_smem_per_sm(launch) / (smem + 1024))));
+    int z = plan_sms(launch) * resident / g.ctiles;
     if (z > g.per_ctile) z = g.per_ctile;
     if (z < 1) z = 1;
     Zc = z;
@@ -244,7 +246,7 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t s
     Geo g;
     int Zc;
     size_t smem;
-    if (!plan_geo<T, FH, FW, TH, TW, MINB>(p, g, Zc, smem)) return cudaErrorNotSupported;
+    if (!plan_geo<T, FH, FW, TH, TW, MINB>(p, g, Zc, smem, true)) return cudaErrorNotSupported;
     auto kern = tiled_wgrad_kernel<T, FH, FW, TH, TW, MINB, HA>;
     CUtensorMap halo_map, dy_map;
     if (!make_halo_map(&halo_map, p, g, dt, sizeof(T)) ||
@@ -269,9 +271,10 @@ cudaError_t dispatch(const TiledConv &p, dwconv_dtype dt, float *part, cudaStrea
     size_t smem;
     int Zc = 0;
     bool ok = false;
-    if (p.FH == 7 && p.FW == 7) ok = plan_geo<T, 7, 7, TH7, TW7, MB7>(p, g, Zc, smem);
-    else if (p.FH == 5 && p.FW == 5) ok = plan_geo<T, 5, 5, 4, 7, 2>(p, g, Zc, smem);
-    else if (p.FH == 3 && p.FW == 3) ok = plan_geo<T, 3, 3, 4, 7, 3>(p, g, Zc, smem);
+    const bool launch = Zc_out == nullptr;
+    if (p.FH == 7 && p.FW == 7) ok = plan_geo<T, 7, 7, TH7, TW7, MB7>(p, g, Zc, smem, launch);
+    else if (p.FH == 5 && p.FW == 5) ok = plan_geo<T, 5, 5, 4, 7, 2>(p, g, Zc, smem, launch);
+    else if (p.FH == 3 && p.FW == 3) ok = plan_geo<T, 3, 3, 4, 7, 3>(p, g, Zc, smem, launch);
     if (!ok) return cudaErrorNotSupported;
     if (Zc_out) {  // planning only
         *Zc_out = Zc;

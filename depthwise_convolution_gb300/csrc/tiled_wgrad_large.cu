@@ -175,15 +175,16 @@ __global__ void __launch_bounds__(kWLThreads, 1)
         }
 }
 
-// Shape-only plan: geometry and the slice count Zc (about two CTAs per SM of
-// a 152-SM GB300 for 16-bit data, one for fp32, over all channel tiles and
-// tap groups).  Returns false if no instance covers the shape.
-bool plan_w(const TiledConv &p, dwconv_dtype dt, GeoW &g, int &Zc) {
+// Plan: geometry and the slice count Zc (about two CTAs per SM for 16-bit
+// data, one for fp32, over all channel tiles and tap groups), for the
+// workspace bound or the current device (plan_sms).  Returns false if no
+// instance covers the shape.
+bool plan_w(const TiledConv &p, dwconv_dtype dt, GeoW &g, int &Zc, bool launch) {
     if (dt != DWCONV_FP32 && dt != DWCONV_FP16 && dt != DWCONV_BF16) return false;
     const size_t es = dt == DWCONV_FP32 ? 4 : 2;
     g = make_geo_w(p, es);
     if (g.per_ctile == 0 || g.HH > 256 || g.HW > 256 || 2 * (size_t)g.stage > 220 * 1024) return false;
-    const long long target = 152LL * (es == 2 ? 2 : 1);
+    const long long target = (long long)plan_sms(launch) * (es == 2 ? 2 : 1);
     long long z = target / ((long long)g.ctiles * g.groups);
     if (z > g.per_ctile) z = g.per_ctile;
     if (z < 1) z = 1;
@@ -227,13 +228,13 @@ cudaError_t run_w(const TiledConv &p, dwconv_dtype dt, const GeoW &g, int Zc, fl
 int tiled_wgrad_large_slices(const TiledConv &p, dwconv_dtype dt) {
     GeoW g;
     int Zc = 0;
-    return plan_w(p, dt, g, Zc) ? Zc : 0;
+    return plan_w(p, dt, g, Zc, false) ? Zc : 0;
 }
 
 cudaError_t launch_tiled_wgrad_large(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st) {
     GeoW g;
     int Zc = 0;
-    if (!plan_w(p, dt, g, Zc)) return cudaErrorNotSupported;
+    if (!plan_w(p, dt, g, Zc, true)) return cudaErrorNotSupported;
     switch (dt) {
         case DWCONV_FP32: return run_w<float>(p, dt, g, Zc, part, st);
         case DWCONV_FP16: return run_w<__half>(p, dt, g, Zc, part, st);

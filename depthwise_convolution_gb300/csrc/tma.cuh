@@ -18,7 +18,15 @@ namespace dwc {
 
 constexpr unsigned kSpinLimit = 1u << 26;  // try_wait polls before giving up (seconds)
 
-// Device error word: bit 0 = a bounded wait gave up.
+// Unique id of the context current in the calling thread (the device's
+// primary context, made current if none is), 0 if it cannot be read.  A
+// device reset destroys the context and the next one gets a new id, so caches
+// of device addresses keyed by it never hand out an address of a context that
+// no longer exists.
+unsigned long long current_context_id();
+
+// Device error word: bit 0 = a bounded wait gave up.  Its address is looked up
+// once per context.
 unsigned *device_error_word();
 // Reads and clears the error word of the current device (after syncing `st`).
 cudaError_t take_device_error(cudaStream_t st, unsigned *value);

@@ -30,16 +30,51 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+unsigned long long g_err_ctx[kMaxDevices];  // context id the cached address belongs to
+
 }  // namespace
+
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return 0;
+    if (!ctx) {  // no context in this thread yet: bind the device's primary context
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return 0;
+        if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    }
+    unsigned long long id = 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 unsigned *device_error_word() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    const unsigned long long ctx = current_context_id();
+    if (!ctx) return nullptr;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_err_addr[dev]) {
+    if (!g_err_addr[dev] || g_err_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
         g_err_addr[dev] = static_cast<unsigned *>(p);
+        g_err_ctx[dev] = ctx;
     }
     return g_err_addr[dev];
 }

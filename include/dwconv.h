@@ -136,8 +136,8 @@ size_t dwconv_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int 
  * then summed in a fixed order (§5.1 "accumulation-axis parallelisation"), so
  * repeated calls give bit-identical dw.  x [N][H][W][C], dy [N][OH][OW][C],
  * dw [FH][FW][C] float (fully overwritten).  `workspace` is caller-owned
- * device memory of at least dwconv_bwd_filter_workspace_size() bytes, 256-byte
- * aligned; it may be NULL only if that size is 0.  fp32, fp16 and bf16 only
+ * device memory of at least dwconv_bwd_filter_workspace_size() bytes, 16-byte
+ * aligned (else DWCONV_ERR_MISALIGNED); it may be NULL only if that size is 0.  fp32, fp16 and bf16 only
  * (DWCONV_INT8 and DWCONV_FP8_E4M3: DWCONV_ERR_UNSUPPORTED, workspace size 0).
  */
 dwconv_status dwconv_bwd_filter(int N, int H, int W, int C, int FH, int FW, int stride,
@@ -187,7 +187,10 @@ dwconv_status dwconv_bwd_bias(int N, int OH, int OW, int C, dwconv_dtype dtype, 
  *   before anything is enqueued; use dwconv_bwd_filter for those.
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current) and caches it; make that
- *   first call before any stream capture on the device.
+ *   first call before any stream capture on the device.  The cached address
+ *   belongs to the device's current context: after a device reset the first
+ *   call in the new context looks it up again (so make that call, too, outside
+ *   a stream capture).
  * - All calls on a device share the one array, and it keeps whatever the last
  *   call left in it.  Calls whose work overlaps on the GPU (different streams,
  *   no ordering between them) race on it and give wrong results: order them.

@@ -7,7 +7,10 @@ of a caller workspace.
 Called here straight through the C ABI (ctypes, raw device pointers) and
 checked against the workspace entry point dwconv_bwd_filter on consecutive
 calls, so that whatever one call leaves in the shared scratch cannot leak into
-the next.  This file is named to be collected last.
+the next.  Both run the same kernels with the same split of the accumulation
+axis and reduce it in a fixed order, so the two results must agree bit for
+bit; each is also checked against the oracle within the usual tolerance.  This
+file is named to be collected last.
 """
 import pytest
 import torch
@@ -39,17 +42,25 @@ CALLS = [
 ]
 
 
+def check_one(lib, dtype, shape, seed):
+    """One static call against the workspace entry point (bit for bit) and the
+    oracle (within the tolerance of the other wgrad parity tests)."""
+    N, H, W, C, FH, FW, S, D, P = shape
+    host = random_inputs(dtype, N, H, W, C, FH, FW, S, D, P, seed=seed)
+    d = {k: (None if v is None else v.cuda()) for k, v in host.items()}
+    expect = ops.dwconv_bwd_filter(d["x"], d["dy"], FH, FW, S, D, P)
+    got = torch.full((FH, FW, C), float("nan"), dtype=torch.float32, device="cuda")
+    assert static_call(lib, d, dtype, S, D, P, got) == _lib.OK
+    torch.cuda.synchronize()
+    assert torch.equal(got, expect), f"static scratch {dtype} seed {seed}: differs from dwconv_bwd_filter"
+    ref, mag = oracle.wgrad(to64(host["x"]), to64(host["dy"]), FH, FW, S, D, P)
+    compare(to64(got), ref, mag, dtype, False, f"static scratch {dtype} seed {seed} vs oracle")
+
+
 def test_static_scratch_matches_the_workspace_entry_point():
     lib = _lib.load()
-    for dtype, (N, H, W, C, FH, FW, S, D, P), seed in CALLS:
-        host = random_inputs(dtype, N, H, W, C, FH, FW, S, D, P, seed=seed)
-        d = {k: (None if v is None else v.cuda()) for k, v in host.items()}
-        expect = ops.dwconv_bwd_filter(d["x"], d["dy"], FH, FW, S, D, P)
-        got = torch.full((FH, FW, C), float("nan"), dtype=torch.float32, device="cuda")
-        assert static_call(lib, d, dtype, S, D, P, got) == _lib.OK
-        torch.cuda.synchronize()
-        _, mag = oracle.wgrad(to64(host["x"]), to64(host["dy"]), FH, FW, S, D, P)
-        compare(to64(got), to64(expect), mag, dtype, False, f"static scratch {dtype} seed {seed}")
+    for dtype, shape, seed in CALLS:
+        check_one(lib, dtype, shape, seed)
 
 
 def test_static_scratch_rejects_shapes_beyond_its_size():
@@ -65,3 +76,6 @@ def test_static_scratch_rejects_shapes_beyond_its_size():
     assert lib.dwconv_launch_count() == before
     assert lib.dwconv_bwd_filter_static(*args[:9], _lib.INT8, x.data_ptr(), x.data_ptr(),
                                         dw.data_ptr(), None) == _lib.ERR_UNSUPPORTED
+    # A rejected call enqueues nothing and leaves the shared array usable: the
+    # next valid call still matches the workspace entry point.
+    check_one(lib, *CALLS[0][:2], seed=21)
