@@ -1,0 +1,30 @@
+// Tensor-core large-filter forward pass / stride-1 input gradient: plain
+// instances for filter heights 27 and 29 (kernel in tiled_mma_large_kernel.cuh).
+// A height runs with the number of 16-input blocks its square filter needs,
+// ceil((FH + 7) / 16); a narrower or wider filter of that height runs here
+// when it needs the same number.
+#include "tiled_mma_large_kernel.cuh"
+
+namespace dwc {
+namespace {
+
+template <typename T>
+cudaError_t by_height(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    const int nkb = (p.FW + 7 + 15) / 16;
+    if (p.FH == 27 && nkb == 3) return large_by_width<T, 27, 3, false>(p, dt, st);
+    if (p.FH == 29 && nkb == 3) return large_by_width<T, 29, 3, false>(p, dt, st);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_mma_large_h3(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
+    if (p.fz.pre() || p.fz.post()) return cudaErrorNotSupported;
+    switch (dt) {
+        case DWCONV_FP16: return by_height<__half>(p, dt, st);
+        case DWCONV_BF16: return by_height<__nv_bfloat16>(p, dt, st);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace dwc
