@@ -394,6 +394,19 @@ cudaError_t launch_tiled_mma_fused(const TiledConv &p, dwconv_dtype dt, cudaStre
 // Tensor-core Toeplitz kernel for large 16-bit filters (tiled_mma_large.cu).
 cudaError_t launch_tiled_mma_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 
+// Stride-2, dilation-1 passes of square 3x3 / 5x5 / 7x7 filters, fp32 / fp16 /
+// bf16 (tiled_strided.cu); cudaErrorNotSupported for any other shape.  The
+// caller checks the layout (whole 16-byte channel rows, 16-byte aligned
+// tensors).  strided_wgrad_slices: the workspace plan (slices of the
+// accumulation axis for the workspace bound, 0 if not covered).
+cudaError_t launch_strided_fwd(const Shape &s, dwconv_dtype dt, const void *x, const void *w, const float *bias,
+                               void *y, cudaStream_t st);
+cudaError_t launch_strided_dgrad(const Shape &s, dwconv_dtype dt, const void *dy, const void *w, void *dx,
+                                 cudaStream_t st);
+int strided_wgrad_slices(const Shape &s, dwconv_dtype dt);
+cudaError_t launch_strided_wgrad(const Shape &s, dwconv_dtype dt, const void *x, const void *dy, float *part,
+                                 float *dw, cudaStream_t st);
+
 // Large filters (FW >= 8, any FH), forward and stride-1 input gradient.
 cudaError_t launch_tiled_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 

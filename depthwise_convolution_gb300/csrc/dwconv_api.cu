@@ -300,6 +300,11 @@ dwconv_status fwd_impl(int N, int H, int W, int C, int FH, int FW, int stride_h,
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
+    // Stride 2, dilation 1 (not a unit-stride sub-grid): the strided kernel.
+    if (!fz.pre() && !fz.post() && tiled_layout_ok(s, dtype, x, y, w)) {
+        cudaError_t e = launch_strided_fwd(s, dtype, x, w, static_cast<const float *>(bias), y, cs);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
     return cuda_status(launch_fwd_direct(s, dtype, x, w, bias, y, fz, cs));
 }
 
@@ -397,6 +402,11 @@ dwconv_status dwconv_bwd_data_2d(int N, int H, int W, int C, int FH, int FW, int
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
+    // Stride 2, dilation 1: all four output phases of dx in one strided kernel.
+    if (tiled_layout_ok(s, dtype, dy, dx, w)) {
+        cudaError_t e = launch_strided_dgrad(s, dtype, dy, w, dx, cs);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
     return cuda_status(launch_dgrad_direct(s, dtype, dy, w, dx, cs));
 }
 
@@ -420,6 +430,7 @@ size_t dwconv_bwd_filter_workspace_size_2d(int N, int H, int W, int C, int FH, i
         const size_t tiled = (size_t)wgrad_tiled_plan(p, dtype) * per_slice;
         if (tiled > need) need = tiled;
     }
+    need = std::max(need, (size_t)strided_wgrad_slices(s, dtype) * per_slice);
     return need;
 }
 
@@ -461,6 +472,10 @@ dwconv_status bwd_filter_impl(int N, int H, int W, int C, int FH, int FW, int st
         cudaError_t e = launch_tiled_wgrad(p, dtype, part, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma_wgrad(wgrad_large_view(p), dtype, part, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_wgrad_large(wgrad_large_view(p), dtype, part, cs);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
+    if ((s.C * es) % 16 == 0 && aligned(x, 16) && aligned(dy, 16)) {
+        cudaError_t e = launch_strided_wgrad(s, dtype, x, dy, part, dw, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
     // Shapes without a tiled instance take the exact fp32 path, also for the
