@@ -85,6 +85,18 @@ def peaks():
     return out
 
 
+def measured_fma_rates():
+    """FMA-pipe rates measured now by the pipe-rate probes (libdwprobe.so):
+    fp32 FFMA, packed FFMA2, mixed-precision f16 / bf16 FMA, in TFLOP/s -- the
+    measured counterparts of the derived FP32 peak.  None if the probe library
+    is not built (it is not part of the convolution library)."""
+    try:
+        from depthwise_convolution_gb300 import probes
+        return probes.fma_rates()
+    except Exception as e:  # report, do not hide
+        return {"error": str(e)[:200]}
+
+
 def pass_roofline(kernel, valid_flops, unique_bytes, t_ms, pk, fma_peak_tflops):
     """Roofline of one pass: the binding unit, its peak, what was achieved, the fraction."""
     tensor = kernel in TENSOR_KERNELS
@@ -480,6 +492,7 @@ def main():
     pk = peaks()
     sms = torch.cuda.get_device_properties(local).multi_processor_count
     fma_peak_tflops = sms * FMA_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+    fma_probe = measured_fma_rates()
 
     wl = synthetic.WORKLOADS[args.workload]
     layer = Layer(wl, rank=rank)
@@ -521,7 +534,8 @@ def main():
                     peak_source=(f"measured dense bf16 (cuBLAS) {pk['bf16_tflops']} TFLOP/s" if tensor else
                                  f"derived: {sms} SMs x {FMA_LANES_PER_SM} fp32 FMA lanes x 2 flop x "
                                  f"{pk['sm_max_mhz']:.0f} MHz (max SM clock)") + f"; HBM {pk['hbm_gbs']} GB/s",
-                    peak_kind=pk["source"], flops_per_launch=layer.valid,
+                    peak_kind=pk["source"] if tensor or rf["bound"] == "hbm" else "derived",
+                    fma_probe_tflops=fma_probe, flops_per_launch=layer.valid,
                     unique_bytes_per_launch=layer.unique(dom))
 
     e2e_ms, h2d, d2h = time_e2e(layer, max(10, args.steps // 10))
@@ -531,13 +545,15 @@ def main():
 
     sweep = {}
     if rank == 0 and ws == 1 and not args.no_sweep:
-        for name, other in synthetic.WORKLOADS.items():
+        for name, other in list(synthetic.WORKLOADS.items()) + list(synthetic.EXTRA_LAYERS.items()):
             if name == wl.name:
                 continue
             try:
                 lay = Layer(other)
                 s_ms, pp, _ = time_layer(lay, max(20, args.steps // 10), 3, flush)
                 entry = {"ms_per_step": round(statistics.mean(s_ms), 4)}
+                if name in synthetic.EXTRA_LAYERS:
+                    entry["extra_layer"] = True
                 for p in other.passes:
                     t_ms = statistics.mean(pp[p])
                     ub = lay.unique(p)

@@ -164,3 +164,15 @@ STAGE_SWEEP = [
 ]
 for _wl in STAGE_SWEEP:
     WORKLOADS[_wl.name] = _wl
+
+# Further layers bench.py times next to the workloads (not configurations of
+# the benchmark): the stride-2 down-sampling layer, and odd square filters of
+# the Flash-DWC §6.1 sweep (3 to 51) on the 31x31 layer's shape.
+EXTRA_LAYERS = {
+    "bf16-train-3x3s2-128x56x56x96": Workload(
+        "bf16-train-3x3s2-128x56x56x96", "bf16", 128, 56, 56, 96, 3, 3, 2, 1, 1, False,
+        ("fwd", "dgrad", "wgrad"), 61),
+}
+for _i, _F in enumerate((9, 15, 21, 27)):
+    _name = f"bf16-fwd-{_F}x{_F}-32x56x56x128"
+    EXTRA_LAYERS[_name] = Workload(_name, "bf16", 32, 56, 56, 128, _F, _F, 1, 1, _F // 2, True, ("fwd",), 62 + _i)
