@@ -171,9 +171,22 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce(const float *_
     __shared__ float acc[kReduceWarps][32];
     const int lane = threadIdx.x % 32, r = threadIdx.x / 32;
     const long long i = blockIdx.x * 32LL + lane;
+    // Launched as a programmatic dependent of the kernel that writes `part`:
+    // wait here until that grid has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     float sum = 0.f;
-    if (i < count)
-        for (int z = r; z < Z; z += kReduceWarps) sum += part[(long long)z * count + i];
+    if (i < count) {
+        // Loads in batches of 8 (all in flight at once), added in slice order.
+        int z = r;
+        for (; z + 7 * kReduceWarps < Z; z += 8 * kReduceWarps) {
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = part[(long long)(z + q * kReduceWarps) * count + i];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sum += v[q];
+        }
+        for (; z < Z; z += kReduceWarps) sum += part[(long long)z * count + i];
+    }
     acc[r][lane] = sum;
     __syncthreads();
     if (r == 0 && i < count) {
@@ -319,9 +332,22 @@ cudaError_t launch_wgrad_reduce(const float *part, int Z, long long count, float
                                 cudaStream_t st) {
     const long long blocks = (count + 31) / 32;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    wgrad_reduce<<<(unsigned)blocks, 32 * kReduceWarps, 0, st>>>(part, Z, count, dw);
+    // Programmatic dependent launch: the reduction's blocks are scheduled as
+    // the producing kernel drains instead of after a full launch gap; they
+    // wait (griddepcontrol.wait) for its completion before reading.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(32 * kReduceWarps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, wgrad_reduce, part, Z, count, dw);
     note_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace dwc

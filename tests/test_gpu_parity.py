@@ -167,7 +167,9 @@ def test_zero_input_gives_bias_only():
     ("bf16", (2, 40, 40, 32, 7, 7, 1, 1, 3), "dgrad", "tiled_mma"),
     ("bf16", (1, 40, 40, 32, 31, 31, 1, 1, 15), "fwd", "tiled_mma_large"),
     ("fp32", (2, 40, 40, 32, 7, 7, 1, 1, 3), "fwd", "tiled_small"),
-    ("bf16", (1, 30, 30, 32, 15, 15, 1, 1, 7), "fwd", "tiled_large"),
+    ("fp32", (1, 30, 30, 32, 15, 15, 1, 1, 7), "fwd", "tiled_large"),
+    ("bf16", (1, 30, 30, 32, 15, 15, 1, 1, 7), "fwd", "tiled_mma_large"),
+    ("bf16", (2, 16, 15, 24, 3, 3, 2, 1, 1), "dgrad", "strided_dgrad"),
     ("fp16", (2, 40, 40, 32, 7, 7, 1, 1, 3), "wgrad", "tiled_wgrad"),
     ("bf16", (2, 10, 10, 5, 3, 3, 1, 1, 1), "fwd", "direct_fwd"),
 ])

@@ -46,7 +46,7 @@ def test_half_accumulate_within_derived_bound(case):
     ref, mag = oracle.wgrad(to64(x), to64(dy), FH, FW, S, D, P)
     err = np.abs(to64(dw) - ref)
     assert np.all(err <= BOUND * mag), (kernel, float((err / np.maximum(mag, 1e-30)).max()))
-    expect = "direct_wgrad" if S == 2 and D == 1 else "tiled_wgrad_ha"
+    expect = "strided_wgrad" if S == 2 and D == 1 else "tiled_wgrad_ha"
     assert kernel == expect
 
 
