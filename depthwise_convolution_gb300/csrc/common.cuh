@@ -407,6 +407,15 @@ int strided_wgrad_slices(const Shape &s, dwconv_dtype dt);
 cudaError_t launch_strided_wgrad(const Shape &s, dwconv_dtype dt, const void *x, const void *dy, float *part,
                                  float *dw, cudaStream_t st);
 
+// Whole-map kernels for 7x7 maps, 3x3 / 5x5 / 7x7 filters with "same"
+// padding, unit stride, fp32 / fp16 / bf16 (tiled_smallmap.cu): forward and
+// stride-1 input gradient (p.flip), and the weight gradient (partials into
+// part[Z][FH*FW][C], then the fixed-order reduction into p.out);
+// smallmap_wgrad_slices: Z for the workspace bound (0 if not covered).
+cudaError_t launch_smallmap(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
+int smallmap_wgrad_slices(const TiledConv &p, dwconv_dtype dt);
+cudaError_t launch_smallmap_wgrad(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t st);
+
 // Large filters (FW >= 8, any FH), forward and stride-1 input gradient.
 cudaError_t launch_tiled_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st);
 

@@ -296,6 +296,7 @@ dwconv_status fwd_impl(int N, int H, int W, int C, int FH, int FW, int stride_h,
         cudaError_t e = launch_tall_strip(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma_large(p, dtype, cs);
+        if (e == cudaErrorNotSupported) e = launch_smallmap(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_small(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
@@ -398,6 +399,7 @@ dwconv_status dwconv_bwd_data_2d(int N, int H, int W, int C, int FH, int FW, int
         cudaError_t e = launch_tall_strip(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma_large(p, dtype, cs);
+        if (e == cudaErrorNotSupported) e = launch_smallmap(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_small(p, dtype, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
@@ -429,6 +431,7 @@ size_t dwconv_bwd_filter_workspace_size_2d(int N, int H, int W, int C, int FH, i
     if (wgrad_tiled_params(s, dtype, nullptr, nullptr, nullptr, p)) {
         const size_t tiled = (size_t)wgrad_tiled_plan(p, dtype) * per_slice;
         if (tiled > need) need = tiled;
+        need = std::max(need, (size_t)smallmap_wgrad_slices(p, dtype) * per_slice);
     }
     need = std::max(need, (size_t)strided_wgrad_slices(s, dtype) * per_slice);
     return need;
@@ -469,7 +472,8 @@ dwconv_status bwd_filter_impl(int N, int H, int W, int C, int FH, int FW, int st
     TiledConv p;
     if (wgrad_tiled_params(s, dtype, x, dy, dw, p) && aligned(x, 16) && aligned(dy, 16)) {
         p.half_accumulate = half_accumulate;
-        cudaError_t e = launch_tiled_wgrad(p, dtype, part, cs);
+        cudaError_t e = launch_smallmap_wgrad(p, dtype, part, cs);
+        if (e == cudaErrorNotSupported) e = launch_tiled_wgrad(p, dtype, part, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_mma_wgrad(wgrad_large_view(p), dtype, part, cs);
         if (e == cudaErrorNotSupported) e = launch_tiled_wgrad_large(wgrad_large_view(p), dtype, part, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
