@@ -235,6 +235,7 @@ cudaError_t with_shape(int FH, int FW, F &&f) {
     if (nfb <= 1 && nhb <= 2) return f(std::integral_constant<int, 1>{}, std::integral_constant<int, 2>{});
     if (nfb <= 2 && nhb <= 1) return f(std::integral_constant<int, 2>{}, std::integral_constant<int, 1>{});
     if (nfb <= 2 && nhb <= 2) return f(std::integral_constant<int, 2>{}, std::integral_constant<int, 2>{});
+    if (nfb <= 2 && nhb <= 3) return f(std::integral_constant<int, 2>{}, std::integral_constant<int, 3>{});
     if (nfb <= 2 && nhb <= 4) return f(std::integral_constant<int, 2>{}, std::integral_constant<int, 4>{});
     if (nfb <= 4 && nhb <= 1) return f(std::integral_constant<int, 4>{}, std::integral_constant<int, 1>{});
     return cudaErrorNotSupported;
