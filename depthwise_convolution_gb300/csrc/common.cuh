@@ -30,6 +30,14 @@ void note_kernel(const char *family);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Prepares `kern` for a launch of `threads` threads with `smem` bytes of
+// dynamic shared memory: raises its shared-memory limit if this context has
+// not set one that large yet (the limit is per kernel and is never lowered)
+// and, if per_sm is not null, stores how many such CTAs fit on an SM (looked
+// up once per kernel, context, block size and shared-memory size), so a
+// repeated launch pays table lookups instead of two runtime queries.
+cudaError_t kernel_setup(const void *kern, int threads, size_t smem, int *per_sm);
+
 // SM count and shared memory per SM that a split-reduction plan is sized for.
 // Workspace sizes are pure functions of the shape, so they are planned for an
 // upper bound (kPlanMaxSms SMs: sm_103a parts have at most 160; 228 KB of

@@ -5,6 +5,8 @@
 #include <algorithm>
 #include <atomic>
 #include <climits>
+#include <mutex>
+#include <unordered_map>
 
 #include <utility>
 
@@ -37,6 +39,55 @@ int sm_count() {
         g_sm_count[dev].store(v, std::memory_order_relaxed);
     }
     return v;
+}
+
+namespace {
+struct SetupKey {
+    const void *kern;
+    unsigned long long ctx;
+    int threads;
+    size_t smem;
+    bool operator==(const SetupKey &o) const {
+        return kern == o.kern && ctx == o.ctx && threads == o.threads && smem == o.smem;
+    }
+};
+struct SetupHash {
+    size_t operator()(const SetupKey &k) const {
+        size_t h = std::hash<const void *>()(k.kern);
+        h = h * 1000003u ^ std::hash<unsigned long long>()(k.ctx);
+        h = h * 1000003u ^ (size_t)k.threads;
+        return h * 1000003u ^ k.smem;
+    }
+};
+std::mutex g_setup_mu;
+std::unordered_map<SetupKey, int, SetupHash> g_occupancy;    // (kernel, context, threads, smem) -> CTAs per SM
+std::unordered_map<SetupKey, size_t, SetupHash> g_smem_limit;  // (kernel, context) -> largest limit set
+}  // namespace
+
+cudaError_t kernel_setup(const void *kern, int threads, size_t smem, int *per_sm) {
+    const unsigned long long ctx = current_context_id();
+    const SetupKey key{kern, ctx, threads, smem}, fkey{kern, ctx, 0, 0};
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    // The shared-memory limit is one value per kernel: raise it when a launch
+    // needs more than has been set in this context, never lower it.
+    auto lim = g_smem_limit.find(fkey);
+    if (!ctx || lim == g_smem_limit.end() || lim->second < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (ctx) g_smem_limit[fkey] = smem;
+    }
+    if (!per_sm) return cudaSuccess;
+    auto it = g_occupancy.find(key);
+    if (ctx && it != g_occupancy.end()) {
+        *per_sm = it->second;
+        return cudaSuccess;
+    }
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (ctx) g_occupancy[key] = n;
+    *per_sm = n;
+    return cudaSuccess;
 }
 
 int plan_sms(bool launch) { return launch ? std::min(sm_count(), kPlanMaxSms) : kPlanMaxSms; }

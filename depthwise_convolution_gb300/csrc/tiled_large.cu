@@ -327,10 +327,8 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
         !encode_tmap_4d(&filt_map, dt, p.w, fdims, fstr, fbox))
         return cudaErrorNotSupported;
     auto kern = tiled_large_kernel<T, TH, TW, MAXR, FWC, FLIP, FUSE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLThreads + 32, smem);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kLThreads + 32, smem, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
     const long long slots = (long long)sm_count() * per_sm;

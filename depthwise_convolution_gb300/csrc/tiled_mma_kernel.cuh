@@ -494,10 +494,8 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
         !make_out_map(&omap, p, out_dt, sizeof(typename OutOf<T>::type), obox, kPB))
         return cudaErrorNotSupported;
     auto kern = tiled_mma_kernel<T, FH, FW, G, NI, KNB, FUSE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem + 1024);
-    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMThreads, C::smem + 1024);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kMThreads, C::smem + 1024, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
     const long long slots = (long long)sm_count() * per_sm;

@@ -330,10 +330,8 @@ cudaError_t run_large(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     if (!encode_tmap_4d(&map, dt, base, dims, str, box) || !make_out_map(&omap, p, dt, es, obox, 0))
         return cudaErrorNotSupported;
     auto kern = tiled_mma_large_kernel<T, FH, NKB, G, FUSE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem + 1024);
-    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLThreads, C::smem + 1024);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kLThreads, C::smem + 1024, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
     const int grid = (int)std::min<long long>(g.units, (long long)sm_count() * per_sm);

@@ -289,7 +289,7 @@ cudaError_t run_wm(const TiledConv &p, dwconv_dtype dt, const GeoWM &g, int Zc, 
         return cudaErrorNotSupported;
     auto kern = tiled_mma_wgrad_kernel<T, NFB, NHB>;
     const int smem = (int)C::smem + 1024;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kWThreads, smem, nullptr);
     if (e != cudaSuccess) return e;
     kern<<<g.ctiles * Zc, kWThreads, smem, st>>>(halo_map, dy_map, p, g, part, Zc, device_error_word());
     note_launches(1);

@@ -264,10 +264,8 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     if (smem > 220 * 1024) return cudaErrorNotSupported;
     CUtensorMap map;
     if (!make_halo_map(&map, p, g, dt, sizeof(T))) return cudaErrorNotSupported;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kThreads, smem, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
     const long long slots = (long long)sm_count() * per_sm;

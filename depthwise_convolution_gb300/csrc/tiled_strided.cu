@@ -464,10 +464,8 @@ cudaError_t run_fwd(const SArgs &a, dwconv_dtype dt, cudaStream_t st) {
     CUtensorMap map;
     if (!make_nhwc_map(&map, a.in, a.N, a.H, a.W, a.C, g.HH, g.HW, g.NI, dt, sizeof(T))) return cudaErrorNotSupported;
     auto kern = strided_fwd_kernel<T, F, TH, TW, MINB>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kThreads, smem, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
     const int grid = (int)std::min<long long>(g.units, (long long)sm_count() * per_sm);
@@ -490,10 +488,8 @@ cudaError_t run_dgrad(const SArgs &a, dwconv_dtype dt, cudaStream_t st) {
     if (!make_nhwc_map(&map, a.in, a.N, a.OH, a.OW, a.C, g.HH, g.HW, g.NI, dt, sizeof(T)))
         return cudaErrorNotSupported;
     auto kern = strided_dgrad_kernel<T, F, TH, TW, MINB>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kThreads, smem, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
     const int grid = (int)std::min<long long>(g.units, (long long)sm_count() * per_sm);
@@ -533,7 +529,7 @@ cudaError_t run_wgrad(const SArgs &a, dwconv_dtype dt, float *part, float *dw, c
         !make_nhwc_map(&dy_map, a.dy, a.N, a.OH, a.OW, a.C, g.RT * TH, g.CT * TW, g.NI, dt, sizeof(T)))
         return cudaErrorNotSupported;
     auto kern = strided_wgrad_kernel<T, F, TH, TW, MINB>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kThreads, smem, nullptr);
     if (e != cudaSuccess) return e;
     kern<<<g.ctiles * Zc, kThreads, smem, st>>>(halo_map, dy_map, a, g, part, Zc, device_error_word());
     note_launches(1);

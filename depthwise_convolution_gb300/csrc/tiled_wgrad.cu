@@ -252,7 +252,7 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, float *part, cudaStream_t s
     if (!make_halo_map(&halo_map, p, g, dt, sizeof(T)) ||
         !make_tile_map(&dy_map, p.dy, p, g, TH, TW, dt, sizeof(T)))
         return cudaErrorNotSupported;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kThreads, smem, nullptr);
     if (e != cudaSuccess) return e;
     kern<<<g.ctiles * Zc, kThreads, smem, st>>>(halo_map, dy_map, p, g, part, Zc, device_error_word());
     note_launches(1);

@@ -213,7 +213,7 @@ cudaError_t run_w(const TiledConv &p, dwconv_dtype dt, const GeoW &g, int Zc, fl
         return cudaErrorNotSupported;
     const size_t smem = 2 * (size_t)g.stage;
     auto kern = tiled_wgrad_large_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kWLThreads, smem, nullptr);
     if (e != cudaSuccess) return e;
     kern<<<g.ctiles * g.groups * Zc, kWLThreads, smem, st>>>(halo_map, dy_map, p, g, part, Zc, device_error_word());
     note_launches(1);

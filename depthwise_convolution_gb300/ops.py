@@ -7,11 +7,23 @@ torch.empty when the caller passes none) and the current CUDA stream.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 
 import torch
 
 from . import _lib
+
+_NULL_CTX = contextlib.nullcontext()
+_L = None
+
+
+def _ll():
+    """The loaded library (fast path after the first call)."""
+    global _L
+    if _L is None:
+        _L = _lib.load()
+    return _L
 
 _DTYPE = {torch.int8: _lib.INT8, torch.float32: _lib.FP32, torch.float16: _lib.FP16,
           torch.bfloat16: _lib.BF16}
@@ -51,14 +63,22 @@ def _dev(t: torch.Tensor, name: str, ndim: int, ref: torch.Tensor = None) -> int
 
 def _on(t: torch.Tensor):
     """The library works on the current device: make t's device current for the call
-    (the default stream is then that device's current stream)."""
+    (the default stream is then that device's current stream).  No switch when it
+    already is current."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError("inputs must be CUDA tensors")
+    if t.get_device() == torch.cuda.current_device():
+        return _NULL_CTX
     return torch.cuda.device(t.device)
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream) -> int:
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -77,11 +97,25 @@ def _axes(stride, dilation, pad):
     return sh, sw, dh, dw, ph, pw
 
 
+def _out_hw(H, W, FH, FW, stride, dilation, pad):
+    """(OH, OW) for the wrappers' shape checks (the library validates again):
+    floor((X + 2P - D(F-1) - 1)/S) + 1 per axis; invalid sizes go through
+    dwconv_output_size, which raises the library's error."""
+    (sh, sw), (dh, dw), (ph, pw) = _pair(stride, "stride"), _pair(dilation, "dilation"), _pair(pad, "pad")
+    if min(H, W, FH, FW, sh, sw, dh, dw) <= 0 or min(ph, pw) < 0:
+        return dwconv_output_size(H, W, FH, FW, stride, dilation, pad)
+    oh = (H + 2 * ph - dh * (FH - 1) - 1) // sh + 1
+    ow = (W + 2 * pw - dw * (FW - 1) - 1) // sw + 1
+    if oh < 1 or ow < 1:
+        return dwconv_output_size(H, W, FH, FW, stride, dilation, pad)
+    return oh, ow
+
+
 def dwconv_output_size(H, W, FH, FW, stride=1, dilation=1, pad=0):
     """(OH, OW) of the forward pass; raises DwconvError on invalid sizes.
     stride, dilation and pad: an int (both axes) or an (h, w) pair."""
     oh, ow = ctypes.c_int(0), ctypes.c_int(0)
-    _lib.check(_lib.load().dwconv_output_size_2d(H, W, FH, FW, *_axes(stride, dilation, pad),
+    _lib.check(_ll().dwconv_output_size_2d(H, W, FH, FW, *_axes(stride, dilation, pad),
                                                   ctypes.byref(oh), ctypes.byref(ow)),
                "dwconv_output_size")
     return oh.value, ow.value
@@ -99,14 +133,14 @@ def dwconv_fwd(x, w, bias=None, stride=1, dilation=1, pad=0, out=None, stream=No
     bias_dtype = torch.int32 if dt == _lib.INT8 else torch.float32
     if bias is not None and (bias.dtype != bias_dtype or tuple(bias.shape) != (C,)):
         raise ValueError(f"bias must be [C] {bias_dtype}")
-    OH, OW = dwconv_output_size(H, W, FH, FW, stride, dilation, pad)
+    OH, OW = _out_hw(H, W, FH, FW, stride, dilation, pad)
     y_dtype = _y_dtype(x, dt)
     if out is None:
         out = torch.empty((N, OH, OW, C), dtype=y_dtype, device=x.device)
     elif out.dtype != y_dtype or tuple(out.shape) != (N, OH, OW, C):
         raise ValueError("out has the wrong shape or dtype")
     with _on(x):
-        _lib.check(_lib.load().dwconv_fwd_2d(
+        _lib.check(_ll().dwconv_fwd_2d(
             N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
             _dev(x, "x", 4), _dev(w, "w", 3, x), None if bias is None else _dev(bias, "bias", 1, x),
             _dev(out, "out", 4, x), _stream(stream)), "dwconv_fwd")
@@ -149,14 +183,14 @@ def dwconv_fwd_fused(x, w, bias=None, in_scale=None, in_shift=None, in_act="none
             raise ValueError(f"{name} must be [C] float32")
     if w.dtype != x.dtype or tuple(w.shape) != (FH, FW, C):
         raise ValueError("w must be [FH, FW, C] with x's dtype")
-    OH, OW = dwconv_output_size(H, W, FH, FW, stride, dilation, pad)
+    OH, OW = _out_hw(H, W, FH, FW, stride, dilation, pad)
     y_dtype = _y_dtype(x, dt)
     if out is None:
         out = torch.empty((N, OH, OW, C), dtype=y_dtype, device=x.device)
     elif out.dtype != y_dtype or tuple(out.shape) != (N, OH, OW, C):
         raise ValueError("out has the wrong shape or dtype")
     with _on(x):
-        _lib.check(_lib.load().dwconv_fwd_fused_2d(
+        _lib.check(_ll().dwconv_fwd_fused_2d(
             N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
             _dev(x, "x", 4), _vec(in_scale, C, "in_scale", x), _vec(in_shift, C, "in_shift", x), ia,
             _dev(w, "w", 3, x), None if bias is None else _dev(bias, "bias", 1, x),
@@ -172,14 +206,14 @@ def dwconv_bwd_data(dy, w, H, W, stride=1, dilation=1, pad=0, out=None, stream=N
     dt = _code(dy)
     if w.dtype != dy.dtype or tuple(w.shape) != (FH, FW, C):
         raise ValueError("w must be [FH, FW, C] with dy's dtype")
-    if dwconv_output_size(H, W, FH, FW, stride, dilation, pad) != (OH, OW):
+    if _out_hw(H, W, FH, FW, stride, dilation, pad) != (OH, OW):
         raise ValueError("dy's spatial size is not the forward output of an H x W input")
     if out is None:
         out = torch.empty((N, H, W, C), dtype=dy.dtype, device=dy.device)
     elif out.dtype != dy.dtype or tuple(out.shape) != (N, H, W, C):
         raise ValueError("out has the wrong shape or dtype")
     with _on(dy):
-        _lib.check(_lib.load().dwconv_bwd_data_2d(
+        _lib.check(_ll().dwconv_bwd_data_2d(
             N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
             _dev(dy, "dy", 4), _dev(w, "w", 3, dy), _dev(out, "out", 4, dy), _stream(stream)),
             "dwconv_bwd_data")
@@ -189,7 +223,7 @@ def dwconv_bwd_data(dy, w, H, W, stride=1, dilation=1, pad=0, out=None, stream=N
 def dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation, pad, dtype) -> int:
     """Workspace bytes dwconv_bwd_filter needs (dtype: a torch dtype or ABI code)."""
     code = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
-    return int(_lib.load().dwconv_bwd_filter_workspace_size_2d(N, H, W, C, FH, FW,
+    return int(_ll().dwconv_bwd_filter_workspace_size_2d(N, H, W, C, FH, FW,
                                                                *_axes(stride, dilation, pad), code))
 
 
@@ -203,17 +237,17 @@ def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, work
     if dy.dtype != x.dtype:
         raise ValueError("dy must have x's dtype")
     if (dy.shape[0], dy.shape[3]) != (N, C) or \
-            dwconv_output_size(H, W, FH, FW, stride, dilation, pad) != tuple(dy.shape[1:3]):
+            _out_hw(H, W, FH, FW, stride, dilation, pad) != tuple(dy.shape[1:3]):
         raise ValueError("dy's shape is not the forward output's")
     if out is None:
         out = torch.empty((FH, FW, C), dtype=torch.float32, device=x.device)
     elif out.dtype != torch.float32 or tuple(out.shape) != (FH, FW, C):
         raise ValueError("out must be [FH, FW, C] float32")
-    need = dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation, pad, dt)
     if workspace is None:
+        need = dwconv_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, dilation, pad, dt)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    fn = _lib.load().dwconv_bwd_filter_ha_2d if half_accumulate else _lib.load().dwconv_bwd_filter_2d
+    fn = _ll().dwconv_bwd_filter_ha_2d if half_accumulate else _ll().dwconv_bwd_filter_2d
     with _on(x):
         _lib.check(fn(
             N, H, W, C, FH, FW, *_axes(stride, dilation, pad), dt,
@@ -224,7 +258,7 @@ def dwconv_bwd_filter(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=None, work
 
 
 def dwconv_bwd_bias_workspace_size(N, OH, OW, C) -> int:
-    return int(_lib.load().dwconv_bwd_bias_workspace_size(N, OH, OW, C))
+    return int(_ll().dwconv_bwd_bias_workspace_size(N, OH, OW, C))
 
 
 def dwconv_bwd_bias(dy, out=None, workspace=None, stream=None):
@@ -240,7 +274,7 @@ def dwconv_bwd_bias(dy, out=None, workspace=None, stream=None):
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dy.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     with _on(dy):
-        _lib.check(_lib.load().dwconv_bwd_bias(
+        _lib.check(_ll().dwconv_bwd_bias(
             N, OH, OW, C, dt, _dev(dy, "dy", 4), _dev(out, "out", 1, dy),
             _dev(workspace, "workspace", workspace.dim(), dy), ws_bytes, _stream(stream)), "dwconv_bwd_bias")
     return out
@@ -255,14 +289,14 @@ def dwconv_bwd_filter_static(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=Non
     if dy.dtype != x.dtype:
         raise ValueError("dy must have x's dtype")
     if (dy.shape[0], dy.shape[3]) != (N, C) or \
-            dwconv_output_size(H, W, FH, FW, stride, dilation, pad) != tuple(dy.shape[1:3]):
+            _out_hw(H, W, FH, FW, stride, dilation, pad) != tuple(dy.shape[1:3]):
         raise ValueError("dy's shape is not the forward output's")
     if out is None:
         out = torch.empty((FH, FW, C), dtype=torch.float32, device=x.device)
     elif out.dtype != torch.float32 or tuple(out.shape) != (FH, FW, C):
         raise ValueError("out must be [FH, FW, C] float32")
     with _on(x):
-        _lib.check(_lib.load().dwconv_bwd_filter_static(
+        _lib.check(_ll().dwconv_bwd_filter_static(
             N, H, W, C, FH, FW, stride, dilation, pad, dt,
             _dev(x, "x", 4), _dev(dy, "dy", 4, x), _dev(out, "out", 3, x), _stream(stream)),
             "dwconv_bwd_filter_static")
@@ -271,21 +305,21 @@ def dwconv_bwd_filter_static(x, dy, FH, FW, stride=1, dilation=1, pad=0, out=Non
 
 def dwconv_check_device_errors(stream=None) -> None:
     """Wait for the stream; raise DwconvError if a library kernel gave up a bounded wait."""
-    _lib.check(_lib.load().dwconv_check_device_errors(_stream(stream)), "dwconv_check_device_errors")
+    _lib.check(_ll().dwconv_check_device_errors(_stream(stream)), "dwconv_check_device_errors")
 
 
 def dwconv_selftest_timeout(stream=None) -> None:
     """Enqueue the library's failure-detection self-test: a bounded wait that
     runs out (no fault, no hang); the next dwconv_check_device_errors raises
     DwconvError with DWCONV_ERR_TIMEOUT."""
-    _lib.check(_lib.load().dwconv_selftest_timeout(_stream(stream)), "dwconv_selftest_timeout")
+    _lib.check(_ll().dwconv_selftest_timeout(_stream(stream)), "dwconv_selftest_timeout")
 
 
 def dwconv_launch_count() -> int:
     """Kernels libdwconv has launched in this process."""
-    return int(_lib.load().dwconv_launch_count())
+    return int(_ll().dwconv_launch_count())
 
 
 def dwconv_last_kernel() -> str:
     """Kernel family of the latest pass launched from this thread."""
-    return _lib.load().dwconv_last_kernel().decode()
+    return _ll().dwconv_last_kernel().decode()
