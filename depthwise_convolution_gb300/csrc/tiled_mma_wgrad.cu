@@ -14,15 +14,22 @@
 // x column meets every dy column exactly once, so no band is masked: dy
 // outside the tile is zero in the staged copy.
 //
-// Work unit: 8 channels (one per warp) x OTH dy rows x OTW dy columns of one
-// image, 256 threads.  Per unit one thread stages the x halo the taps read and
-// the dy tile with two TMA copies on one mbarrier (double-buffered, bounded
-// waits); ldmatrix.trans + stmatrix build channel-major copies of both (dy
-// twice, the second shifted by one column, so that every A pair is one
-// aligned 32-bit load); each warp then runs its channel's MMAs with the
-// NFB x NHB accumulator blocks in registers for the whole CTA.  Grid =
-// channel tiles x accumulation slices; each CTA writes its slice of the
-// partial sums and wgrad_reduce (direct.cu) sums the slices in a fixed order.
+// Work: 8 channels (one per warp) x OTH-row, OTW-column bands of dy, 256
+// threads.  A band of OTH dy rows reads OTH + FH - 1 x rows, so consecutive
+// bands of an image column share all but OTH of them: each CTA walks an equal
+// share of its channel tile's bands in order (column by column) and keeps the
+// x rows in a ring in shared memory (channel-major, NP pieces of OTH rows), so
+// each step stages and transposes only the OTH new x rows (and the band's dy
+// tile) instead of the whole halo.  Each image column a CTA enters starts with
+// NP - 1 steps that fill the ring.  Per step one thread stages the new x rows
+// and the dy tile by TMA into a ring of staging buffers (bounded waits);
+// ldmatrix.trans + stmatrix build the channel-major copies -- dy twice, the
+// second shifted by one column, so that every A pair is one aligned 32-bit
+// load; each warp then runs its channel's MMAs with the NFB x NHB accumulator
+// blocks in registers for the whole CTA, reading B from the ring at the band's
+// offset (modulo the ring size).  Grid = channel tiles x accumulation slices;
+// each CTA writes its slice of the partial sums and wgrad_reduce (direct.cu)
+// sums the slices in a fixed order.
 #include "mma_common.cuh"
 
 namespace dwc {
@@ -39,53 +46,100 @@ constexpr int kWThreads = 256;
 #ifndef DWCONV_WG_OTW
 #define DWCONV_WG_OTW 64
 #endif
-// dy rows, columns per unit (measured on GB300: 4 x 64 beats 8 x 32 by 8-15 %,
+// dy rows, columns per band (measured on GB300: 4 x 64 beats 8 x 32 by 8-15 %,
 // the wider tile wasting fewer Toeplitz products at its edges)
 constexpr int kWOTH = DWCONV_WG_OTH, kWOTW = DWCONV_WG_OTW;
+constexpr int kWStages = 3;  // staging buffers (new x rows + dy tile of one step each)
+
+// Channel stride of a channel-major copy: 8 mod 16 halves, so that the 16-byte
+// rows stmatrix writes for 8 channels fall in distinct bank quads.
+constexpr int chan_stride(int v) { return v + ((8 - v % 16) + 16) % 16; }
 
 template <int NFB, int NHB>
 struct CfgW {
     static constexpr int FWMAX = 16 * NFB, FHMAX = 8 * NHB;
-    // x halo: rows OTH + FH - 1 staged, OTH + 8 NHB - 1 allocated (the last
-    // block's surplus rows only reach unused accumulator columns); columns
-    // OTW + FW - 1 rounded up to whole 16-column groups, NG of them at most.
+    // x columns OTW + FW - 1 rounded up to whole 16-column groups, NG of them at most.
     static constexpr int NG = (kWOTW + FWMAX - 1 + 15) / 16;
     static constexpr int SWX = 16 * NG;
+    // Diagonals d = grp - fb whose blocks meet a dy column of the tile: 0 <= d < ND.
+    static constexpr int ND = NG < (kWOTW + 14) / 16 + 1 ? NG : (kWOTW + 14) / 16 + 1;
+    // x rows one band's MMAs read, from the band's first x row (the last
+    // block's surplus rows only reach unused accumulator columns).
     static constexpr int TXR = kWOTH + FHMAX - 1;
+    static constexpr int NP = (TXR + kWOTH - 1) / kWOTH;  // pieces of OTH x rows a window spans
     // T_x row stride: 8 rows of a B load fall in distinct bank quads.
     static constexpr int RSX = SWX % 16 == 8 ? SWX : SWX + ((8 - SWX % 16 + 16) % 16);
-    static constexpr int CSX = TXR * RSX;
-    // T_dy: dy column e sits at LM + e; A reads e from -(16 NFB - 1) to 16 NG.
-    static constexpr int LM = 16 * NFB;
-    static constexpr int DW = LM + SWX + 8;
-    static constexpr int CSD = 2 * kWOTH * DW + 16;  // two copies; +16 halves: copies apart in banks
-    static constexpr unsigned x_bytes_max = (unsigned)(kWOTH + FHMAX - 1) * SWX * 16;
+    // T_dy: dy column e sits at LM + e (copy 1: e + 1); the A loads reach e
+    // from -15 to 16 ND - 1, the transposes write up to OTW + 7; 8 mod 16
+    // halves per row keeps the two copies' A loads in disjoint banks.
+    static constexpr int LM = 16;
+    static constexpr int DW = chan_stride(LM + (16 * ND > kWOTW + 8 ? 16 * ND : kWOTW + 8) + 1);
+    static constexpr int CSD = chan_stride(2 * kWOTH * DW);  // two copies per channel
+    static constexpr unsigned x_bytes = (unsigned)kWOTH * SWX * 16;  // one piece: OTH rows x SWX cols x 8 ch
     static constexpr unsigned dy_bytes = kWOTH * kWOTW * 16;
-    static constexpr unsigned dy_off = align1k(x_bytes_max);  // dy box within a stage
+    static constexpr unsigned dy_off = align1k(x_bytes);  // dy box within a stage
     static constexpr unsigned stage = dy_off + align1k(dy_bytes);
-    static constexpr unsigned tx_off = 2 * stage;
-    static constexpr unsigned td_off = tx_off + align1k(kWCh * CSX * 2);
-    static constexpr unsigned zero_off = td_off + align1k(kWCh * CSD * 2);
+    static constexpr unsigned tx_off = kWStages * stage;
+    static constexpr unsigned td_bytes = kWCh * CSD * 2;
+    static constexpr unsigned smem_with(int pieces) {
+        return tx_off + kWCh * chan_stride(pieces * kWOTH * RSX) * 2 + td_bytes + 16;
+    }
+    // Ring pieces: rounded up to a multiple of 8 rows when two CTAs still fit
+    // an SM, so that the 8 rows of a B load that wraps around the ring's end
+    // stay in distinct bank quads too.
+    static constexpr int NP8 = ((NP * kWOTH + 7) / 8 * 8) / kWOTH;
+    static constexpr int NPR = 2 * (smem_with(NP8) + 2048) <= 228 * 1024 ? NP8 : NP;
+    static constexpr int R = NPR * kWOTH;  // ring rows
+    static constexpr int CSX = chan_stride(R * RSX);
+    static constexpr unsigned td_off = tx_off + kWCh * CSX * 2;  // 16-byte aligned, as stmatrix needs
+    static constexpr unsigned zero_off = td_off + td_bytes;
     static constexpr unsigned smem = zero_off + 16;
+    // Small accumulator shapes leave room for three CTAs per SM.
+    static constexpr int kMinBlocks = NFB * NHB <= 2 ? 3 : 2;
 };
 
+// Bands of a channel tile, numbered column by column: band f is band
+// f mod tiles_h of image column f / tiles_h (column = image n x column tile).
 struct GeoWM {
-    int tiles_h, tiles_w, per_ctile, ctiles;
-    int HR;            // x halo rows staged (OTH + FH - 1)
-    unsigned x_bytes;  // bytes of the staged x box
+    int tiles_h, tiles_w, ctiles;
+    int total;  // N * tiles_w * tiles_h
 };
+
+// A CTA's walk over its band range [f0, f1): one segment per image column
+// it meets, each NP - 1 ring-filling steps (x only) and then one step per
+// band.  Step k of a segment stages x piece k (rows r0 + k OTH .., with
+// r0 = b0 OTH - pad); steps k >= NP - 1 also stage the dy tile of band
+// b0 + k - (NP - 1) and run its MMAs on the ring window of pieces
+// k - (NP - 1) .. k.
+struct Cursor {
+    int f;       // first band of the segment (flat); f >= f1 when done
+    int n, twi;  // image, column tile
+    int b0, b1;  // band range of the segment within the column
+    int k;       // step within the segment
+};
+
+__device__ __forceinline__ void seg_start(Cursor &c, const GeoWM &g, int f, int f1) {
+    c.f = f;
+    c.k = 0;
+    if (f >= f1) return;
+    const int col = f / g.tiles_h;
+    c.n = col / g.tiles_w;
+    c.twi = col % g.tiles_w;
+    c.b0 = f - col * g.tiles_h;
+    c.b1 = min(g.tiles_h, f1 - col * g.tiles_h);
+}
 
 template <typename T, int NFB, int NHB>
-__global__ void __launch_bounds__(kWThreads, 2)
+__global__ void __launch_bounds__(kWThreads, CfgW<NFB, NHB>::kMinBlocks)
     tiled_mma_wgrad_kernel(const __grid_constant__ CUtensorMap halo_map, const __grid_constant__ CUtensorMap dy_map,
                            TiledConv p, GeoWM g, float *__restrict__ part, int Zc, unsigned *err) {
     using C = CfgW<NFB, NHB>;
-    constexpr int NG = C::NG;
-    extern __shared__ __align__(1024) unsigned char smem_dyn[];
-    __shared__ __align__(8) uint64_t bars[2];
+    constexpr int NG = C::NG, NP = C::NP, NS = kWStages;
+    // 128-byte alignment (the staging buffers sit at 1 KB multiples from it)
+    // is what the unswizzled TMA boxes need.
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bars[NS];
 
-    unsigned char *smem_raw = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int gq = lane / 4, t4 = lane % 4;
     const int tr = lane % 8, tj = lane / 8;
@@ -93,23 +147,29 @@ __global__ void __launch_bounds__(kWThreads, 2)
     const unsigned tx_addr = s_addr + C::tx_off, td_addr = s_addr + C::td_off, zero_addr = s_addr + C::zero_off;
     const int ctile = blockIdx.x / Zc, z = blockIdx.x % Zc;
 
-    // Zero T_x and T_dy once: margins and surplus rows are never written again.
+    // Zero T_x and T_dy once: T_dy's margins are never written again.
     for (unsigned i = tid; i < (C::zero_off + 16 - C::tx_off) / 16; i += kWThreads)
         reinterpret_cast<uint4 *>(smem_raw + C::tx_off)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int b = 0; b < NS; ++b) mbar_init(&bars[b], 1);
         mbar_fence_init();
     }
     __syncthreads();
 
-    auto issue = [&](int v, int b) {
-        const int band = v % g.tiles_h, rest = v / g.tiles_h;
-        const int twi = rest % g.tiles_w, n = rest / g.tiles_w;
+    // This CTA's bands: an equal share of the channel tile's, in order.
+    const int f0 = (int)((long long)g.total * z / Zc), f1 = (int)((long long)g.total * (z + 1) / Zc);
+    auto next = [&](Cursor &c) {
+        if (++c.k == NP - 1 + (c.b1 - c.b0)) seg_start(c, g, c.f + (c.b1 - c.b0), f1);
+    };
+    auto issue = [&](const Cursor &c, int b) {
+        const bool band = c.k >= NP - 1;
         unsigned char *dst = smem_raw + b * C::stage;
-        mbar_arrive_expect_tx(&bars[b], g.x_bytes + C::dy_bytes);
-        tma_load_4d(dst, &halo_map, ctile * kWCh, twi * kWOTW - p.pad_w, band * kWOTH - p.pad_h, n, &bars[b]);
-        tma_load_4d(dst + C::dy_off, &dy_map, ctile * kWCh, twi * kWOTW, band * kWOTH, n, &bars[b]);
+        mbar_arrive_expect_tx(&bars[b], C::x_bytes + (band ? C::dy_bytes : 0u));
+        tma_load_4d(dst, &halo_map, ctile * kWCh, c.twi * kWOTW - p.pad_w, (c.b0 + c.k) * kWOTH - p.pad_h, c.n,
+                    &bars[b]);
+        if (band)
+            tma_load_4d(dst + C::dy_off, &dy_map, ctile * kWCh, c.twi * kWOTW, (c.b0 + c.k - (NP - 1)) * kWOTH,
+                        c.n, &bars[b]);
     };
 
     float acc[NFB][NHB][4];
@@ -124,40 +184,50 @@ __global__ void __launch_bounds__(kWThreads, 2)
     // A pair of lane (gq, t4), block fb, group grp: dy columns e, e+1 with
     // e = 8 grp + 2t4 - 16 fb - gq (- 8 for M rows 8-15); copy q = gq & 1
     // holds dy[e'] at column LM + e' + q, where e + q is even.
-    const int q = gq & 1;
-    const unsigned a_lane = td_c + 2u * (unsigned)(q * kWOTH * C::DW + C::LM + 2 * t4 - gq + q);
-    // B pair: x row i + 8 hb + gq, columns 8 grp + 2t4, +1.
-    const unsigned b_lane = tx_c + 2u * (unsigned)(gq * C::RSX + 2 * t4);
+    const int q2 = gq & 1;
+    const unsigned a_lane = td_c + 2u * (unsigned)(q2 * kWOTH * C::DW + C::LM + 2 * t4 - gq + q2);
+    // B pair: x row (band row i + 8 hb + gq of the window), columns 8 grp + 2t4, +1.
+    const unsigned b_col = tx_c + 2u * (unsigned)(2 * t4);
 
-    int v = z;
-    if (tid == 0 && v < g.per_ctile) issue(v, 0);
-    for (int k = 0; v < g.per_ctile; ++k, v += Zc) {
-        const int vn = v + Zc;
-        if (tid == 0 && vn < g.per_ctile) issue(vn, (k + 1) & 1);
-        if (!mbar_wait(&bars[k & 1], (k >> 1) & 1)) {
+    Cursor ld, cur;
+    seg_start(ld, g, f0, f1);
+    seg_start(cur, g, f0, f1);
+    int issued = 0;  // steps thread 0 has issued
+    if (tid == 0)
+        for (; issued < NS - 1 && ld.f < f1; ++issued, next(ld)) issue(ld, issued);
+    for (int s = 0; cur.f < f1; ++s, next(cur)) {
+        if (tid == 0 && ld.f < f1) {
+            issue(ld, (s + NS - 1) % NS);  // the buffer of step s - 1, free since its first barrier
+            next(ld);
+            ++issued;
+        }
+        if (!mbar_wait(&bars[s % NS], (s / NS) & 1)) {
+            // Give up: thread 0 lets the copies it issued land (bounded) before leaving.
             report_timeout(err);
-            if (tid == 0 && vn < g.per_ctile) mbar_wait(&bars[(k + 1) & 1], ((k + 1) >> 1) & 1);
+            if (tid == 0)
+                for (int j = s + 1; j < issued; ++j) mbar_wait(&bars[j % NS], (j / NS) & 1);
             return;
         }
-        const unsigned sx = s_addr + (k & 1) * C::stage;
+        const unsigned sx = s_addr + (s % NS) * C::stage;
         const unsigned sd = sx + C::dy_off;
-        // Transpose the x halo [HR][SWX][8 ch] -> T_x[ch][row][col], four
-        // 8-pixel blocks per step (lane (tr, tj) addresses pixel tr of block
-        // tj); blocks past the last repeat it (same data to the same place).
+        const bool band = cur.k >= NP - 1;
+        // New x rows [OTH][SWX][8 ch] -> ring slot k mod NP of T_x[ch][row][col],
+        // four 8-pixel blocks per step (lane (tr, tj) addresses pixel tr of block tj).
         {
             constexpr int CB = C::SWX / 8;  // 8-pixel blocks per row
-            const int nb = g.HR * CB;
+            constexpr int nb = kWOTH * CB;
+            const int slot = (cur.k % C::NPR) * kWOTH;
             for (int m0 = warp * 4; m0 < nb; m0 += kWThreads / 8) {
                 const int m = min(m0 + tj, nb - 1);
                 const int row = m / CB, col0 = (m % CB) * 8;
                 unsigned v0, v1, v2, v3;
                 ldsm_x4_trans(v0, v1, v2, v3, sx + (unsigned)((row * C::SWX + col0 + tr) * 16));
-                stsm_x4(tx_addr + 2u * (unsigned)(tr * C::CSX + row * C::RSX + col0), v0, v1, v2, v3);
+                stsm_x4(tx_addr + 2u * (unsigned)(tr * C::CSX + (slot + row) * C::RSX + col0), v0, v1, v2, v3);
             }
         }
         // dy: copy 0 at columns LM + j, copy 1 (dy[j - 1]) at LM + j; copy 1's
         // blocks start one pixel early, with the zero pixel outside the tile.
-        {
+        if (band) {
             constexpr int nb0 = kWOTH * (kWOTW / 8), nb1 = kWOTH * (kWOTW / 8 + 1);
             for (int m0 = warp * 4; m0 < nb0 + nb1; m0 += kWThreads / 8) {
                 const int m = min(m0 + tj, nb0 + nb1 - 1);
@@ -175,39 +245,58 @@ __global__ void __launch_bounds__(kWThreads, 2)
                         v0, v1, v2, v3);
             }
         }
-        __syncthreads();  // T_x, T_dy ready; this staging buffer is free
+        __syncthreads();  // the new ring rows and T_dy are ready; this staging buffer is free
+        if (!band) continue;
 
         // MMAs of this warp's channel, 16 x columns each (m16n8k16).  A of
-        // block fb, group grp holds dy columns e0 = 16 grp + 2t4 - 16 fb - gq
-        // (a0), e0 - 8 (a1, M rows 8-15), e0 + 8 (a2, k 8-15) and e0 again
-        // (a3: rows 8-15 and k 8-15 cancel).  Blocks (grp, fb) whose x columns
-        // meet no dy column of the tile are skipped at compile time.
+        // block fb, group grp depends on the diagonal d = grp - fb only: dy
+        // columns e0 = 16 d + 2t4 - gq (a0), e0 - 8 (a1, M rows 8-15), e0 + 8
+        // (a2, k 8-15) and e0 again (a3: rows 8-15 and k 8-15 cancel), and
+        // a1 of diagonal d is a2 of diagonal d - 1; so a row loads 2 ND + 1
+        // pairs.  Blocks with d outside [0, ND) meet no dy column of the tile
+        // and are skipped at compile time.  B of block hb comes from the
+        // window's x row i + 8 hb + gq, ring row (window start + that) mod R.
+        const int base = ((cur.k - (NP - 1)) % C::NPR) * kWOTH;
 #pragma unroll 1
         for (int i = 0; i < kWOTH; ++i) {
+            constexpr int ND = C::ND;
+            const unsigned arow = a_lane + 2u * (unsigned)(i * C::DW);
+            unsigned a0[ND], a2[ND], a1first;
+            asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(a1first) : "r"(arow - 16u));  // 8 columns left
+#pragma unroll
+            for (int d = 0; d < ND; ++d) {
+                asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(a0[d]) : "r"(arow + 32u * d));
+                asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(a2[d]) : "r"(arow + 32u * d + 16u));  // 8 right
+            }
+            unsigned brow[NHB];
+#pragma unroll
+            for (int hb = 0; hb < NHB; ++hb) {
+                int rr = base + i + 8 * hb + gq;
+                if (rr >= C::R) rr -= C::R;
+                brow[hb] = b_col + 2u * (unsigned)(rr * C::RSX);
+            }
 #pragma unroll
             for (int grp = 0; grp < NG; ++grp) {
+                if (grp - (NFB - 1) >= ND) continue;  // every block of this group skipped
                 unsigned b[NHB][2];
 #pragma unroll
                 for (int hb = 0; hb < NHB; ++hb) {
-                    const unsigned ba = b_lane + 2u * (unsigned)((i + 8 * hb) * C::RSX + 16 * grp);
+                    const unsigned ba = brow[hb] + 32u * (unsigned)grp;
                     asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(b[hb][0]) : "r"(ba));
                     asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(b[hb][1]) : "r"(ba + 16u));
                 }
 #pragma unroll
                 for (int fb = 0; fb < NFB; ++fb) {
-                    // dy columns 16 grp - 16 fb - 15 .. 16 grp - 16 fb + 15.
-                    if (16 * grp - 16 * fb + 15 < 0 || 16 * grp - 16 * fb - 15 >= kWOTW) continue;
-                    const unsigned a = a_lane + 2u * (unsigned)(i * C::DW + 16 * grp - 16 * fb);
-                    unsigned a0, a1, a2;
-                    asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(a0) : "r"(a));
-                    asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(a1) : "r"(a - 16u));  // 8 columns left
-                    asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(a2) : "r"(a + 16u));  // 8 columns right
+                    const int d = grp - fb;
+                    if (d < 0 || d >= ND) continue;
+                    const unsigned a1 = d == 0 ? a1first : a2[d > 0 ? d - 1 : 0];
 #pragma unroll
-                    for (int hb = 0; hb < NHB; ++hb) MmaOp<T>::run(acc[fb][hb], a0, a1, a2, a0, b[hb][0], b[hb][1]);
+                    for (int hb = 0; hb < NHB; ++hb)
+                        MmaOp<T>::run(acc[fb][hb], a0[d], a1, a2[d], a0[d], b[hb][0], b[hb][1]);
                 }
             }
         }
-        __syncthreads();  // every warp is done with T_x / T_dy
+        __syncthreads();  // every warp is done with this window and T_dy
     }
 
     // D[m][n] of block (fb, hb): lane (gq, t4) holds m = gq (+8), n = 2t4 (+1).
@@ -241,32 +330,58 @@ cudaError_t with_shape(int FH, int FW, F &&f) {
     return cudaErrorNotSupported;
 }
 
-// Plan: geometry and slices (about one wave of resident CTAs over all channel
-// tiles), for the workspace bound or the current device (plan_sms).
+// Plan for the workspace bound or the current device (plan_sms): at most one
+// wave of resident CTAs over all channel tiles, each with an equal range of
+// bands.  A range pays NP - 1 ring-filling steps (x only, taken as a quarter
+// of a band step) per image column it meets; the slice count with the
+// shortest worst range wins, the most slices on ties.
 bool plan_wm(const TiledConv &p, dwconv_dtype dt, GeoWM &g, int &Zc, bool launch) {
     if ((dt != DWCONV_FP16 && dt != DWCONV_BF16) || p.FW < 8) return false;
     g = GeoWM{};
     g.tiles_h = (p.OHs + kWOTH - 1) / kWOTH;
     g.tiles_w = (p.OWs + kWOTW - 1) / kWOTW;
     g.ctiles = (p.C + kWCh - 1) / kWCh;
-    const long long per = (long long)p.N * g.tiles_h * g.tiles_w;
-    if (per >= (1LL << 30)) return false;
-    g.per_ctile = (int)per;
-    g.HR = kWOTH + p.FH - 1;
+    const long long total = (long long)p.N * g.tiles_w * g.tiles_h;
+    if (total >= (1LL << 30)) return false;
+    g.total = (int)total;
     bool ok = false;
-    int resident = 1;  // CTAs per SM: two by the register bound, fewer if shared memory holds fewer
-    with_shape(p.FH, p.FW, [&](auto nfb, auto nhb) {
-        using C = CfgW<decltype(nfb)::value, decltype(nhb)::value>;
-        g.x_bytes = (unsigned)g.HR * C::SWX * 16;
-        ok = C::smem + 1024 <= 227 * 1024 && g.HR <= 256 && C::SWX <= 256;
-        resident = std::max(1, std::min(2, (int)(plan_smem_per_sm(launch) / (C::smem + 2048))));
-        return cudaSuccess;
+    int resident = 1, fill = 0;  // CTAs per SM; ring-filling steps per segment
+    const cudaError_t e = with_shape(p.FH, p.FW, [&](auto nfb, auto nhb) {
+        constexpr int NFB = decltype(nfb)::value, NHB = decltype(nhb)::value;
+        using C = CfgW<NFB, NHB>;
+        ok = C::smem <= 227 * 1024 && C::SWX <= 256;
+        fill = C::NP - 1;
+        // The bound: what shared memory and the register bound allow; at a
+        // launch: the occupancy the device reports for this kernel.
+        resident = std::max(1, std::min(C::kMinBlocks, (int)(plan_smem_per_sm(launch) / (C::smem + 2048))));
+        if (!ok || !launch) return cudaSuccess;
+        const void *kern = dt == DWCONV_FP16 ? reinterpret_cast<const void *>(tiled_mma_wgrad_kernel<__half, NFB, NHB>)
+                                             : reinterpret_cast<const void *>(tiled_mma_wgrad_kernel<__nv_bfloat16, NFB, NHB>);
+        int per_sm = 0;
+        const cudaError_t k = kernel_setup(kern, kWThreads, C::smem, &per_sm);
+        if (k == cudaSuccess) resident = std::max(1, std::min(resident, per_sm));
+        return k;
     });
-    if (!ok) return false;
-    long long z = (long long)plan_sms(launch) * resident / g.ctiles;
-    if (z > g.per_ctile) z = g.per_ctile;
-    if (z < 1) z = 1;
-    Zc = (int)z;
+    if (e != cudaSuccess || !ok) return false;
+    const long long target = std::min(total, std::max(1LL, (long long)plan_sms(launch) * resident / g.ctiles));
+    long long best = -1;
+    for (long long z = target; z >= 1; --z) {
+        const long long L = (total + z - 1) / z;           // bands of the longest range
+        const long long segs = (L + g.tiles_h - 2) / g.tiles_h + 1;  // columns it can meet
+        const long long cost = 4 * L + fill * segs;
+        if (best < 0 || cost < best) {
+            best = cost;
+            Zc = (int)z;
+        }
+        if (4 * L > best) break;  // fewer slices only lengthen the ranges
+    }
+    if (launch) {
+        // The partial-sum workspace was sized by the bound plan: never more slices.
+        GeoWM gb;
+        int zb = 0;
+        if (!plan_wm(p, dt, gb, zb, false)) return false;
+        Zc = std::min(Zc, zb);
+    }
     return true;
 }
 
@@ -278,7 +393,7 @@ cudaError_t run_wm(const TiledConv &p, dwconv_dtype dt, const GeoWM &g, int Zc, 
     const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
     uint64_t str[3];
     in_strides(p, es, str);
-    const uint32_t box[4] = {(uint32_t)kWCh, (uint32_t)C::SWX, (uint32_t)g.HR, 1};
+    const uint32_t box[4] = {(uint32_t)kWCh, (uint32_t)C::SWX, (uint32_t)kWOTH, 1};  // one ring piece
     const uint64_t ddims[4] = {(uint64_t)p.C, (uint64_t)p.OWs, (uint64_t)p.OHs, (uint64_t)p.N};
     const uint64_t mem_row = (uint64_t)(p.transpose ? p.OHs : p.OWs) * p.C * es, mem_col = (uint64_t)p.C * es;
     const uint64_t dstr[3] = {p.transpose ? mem_row : mem_col, p.transpose ? mem_col : mem_row,
@@ -288,7 +403,7 @@ cudaError_t run_wm(const TiledConv &p, dwconv_dtype dt, const GeoWM &g, int Zc, 
     if (!encode_tmap_4d(&halo_map, dt, base, dims, str, box) || !encode_tmap_4d(&dy_map, dt, p.dy, ddims, dstr, dbox))
         return cudaErrorNotSupported;
     auto kern = tiled_mma_wgrad_kernel<T, NFB, NHB>;
-    const int smem = (int)C::smem + 1024;
+    const int smem = (int)C::smem;
     cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kWThreads, smem, nullptr);
     if (e != cudaSuccess) return e;
     kern<<<g.ctiles * Zc, kWThreads, smem, st>>>(halo_map, dy_map, p, g, part, Zc, device_error_word());
