@@ -135,10 +135,12 @@ __global__ void __launch_bounds__(kLThreads, 1)
             constexpr int kWords = kLCh * FH * 2 * C::FP / 8;  // 16-byte words
             for (int i = tid; i < kWords; i += kLThreads) reinterpret_cast<uint4 *>(F)[i] = make_uint4(0, 0, 0, 0);
             __syncthreads();
-            // Eight loads per thread in flight at a time (one at a time, the
-            // rebuild took 7 % of a 31x31 forward pass).
+            // Loads per thread in flight at a time: one at a time, the rebuild
+            // took 7 % of a 31x31 forward pass.  Measured on GB300: 8 for most
+            // heights; 32 (the whole table in one batch) from 29 rows on (31x31
+            // 2-3 % faster, 29x29 equal; slower for smaller filters).
             const int nw = kLCh * FH * p.FW;
-            constexpr int kBatch = 8;
+            constexpr int kBatch = FH >= 29 ? 32 : 8;
             for (int i0 = tid; i0 < nw; i0 += kBatch * kLThreads) {
                 T v[kBatch];
                 int at[kBatch];  // index of copy 0 in F, or -1
