@@ -18,7 +18,7 @@
 // threads.  A band of OTH dy rows reads OTH + FH - 1 x rows, so consecutive
 // bands of an image column share all but OTH of them: each CTA walks an equal
 // share of its channel tile's bands in order (column by column) and keeps the
-// x rows in a ring in shared memory (channel-major, NP pieces of OTH rows), so
+// x rows in a ring in shared memory (channel-major, NPR >= NP pieces of OTH rows), so
 // each step stages and transposes only the OTH new x rows (and the band's dy
 // tile) instead of the whole halo.  Each image column a CTA enters starts with
 // NP - 1 steps that fill the ring.  Per step one thread stages the new x rows
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kWThreads, CfgW<NFB, NHB>::kMinBlocks)
         const unsigned sx = s_addr + (s % NS) * C::stage;
         const unsigned sd = sx + C::dy_off;
         const bool band = cur.k >= NP - 1;
-        // New x rows [OTH][SWX][8 ch] -> ring slot k mod NP of T_x[ch][row][col],
+        // New x rows [OTH][SWX][8 ch] -> ring slot k mod NPR of T_x[ch][row][col],
         // four 8-pixel blocks per step (lane (tr, tj) addresses pixel tr of block tj).
         {
             constexpr int CB = C::SWX / 8;  // 8-pixel blocks per row
