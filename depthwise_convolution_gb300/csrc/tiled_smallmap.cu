@@ -82,10 +82,15 @@ __device__ __forceinline__ void load_map(const T *img, int C, typename Lane<T>::
 #define DWCONV_SM_FWD16_MINB 3
 #endif
 
-template <typename T, int F>
+// FUSE (forward only): the BN+Act prologue and the affine+activation epilogue
+// of the fused forward pass (Flash-DWC §5.2) -- 1: piecewise-linear
+// activations only, 2: all; 0: plain.  The prologue rewrites the thread's
+// loaded map in registers (x' = round_T(act(s x + t))); positions outside the
+// map are never read, so the padding of x' stays zero as the fusion requires.
+template <typename T, int F, int FUSE>
 __global__ void __launch_bounds__(kSMThreads, sizeof(T) == 2 ? DWCONV_SM_FWD16_MINB : 3)
     smallmap_fwd_kernel(const T *__restrict__ in, const T *__restrict__ w, const float *__restrict__ bias,
-                        T *__restrict__ out, int N, int C, int flip) {
+                        T *__restrict__ out, int N, int C, int flip, Fuse fz) {
     constexpr int P = F / 2;
     using L = Lane<T>;
     const int lane = threadIdx.x % 32, slot = threadIdx.x / 32;
@@ -94,6 +99,30 @@ __global__ void __launch_bounds__(kSMThreads, sizeof(T) == 2 ? DWCONV_SM_FWD16_M
     if (c >= C || n >= N) return;
     typename L::V xr[kMap][kMap], wr[F][F];
     load_map<T>(in + (long long)n * kMap * kMap * C + c, C, xr);
+    if constexpr (FUSE > 0) {
+        if (fz.pre()) {
+            const Affine a0 = affine_in(fz, c);
+            if constexpr (L::CH == 2) {
+                const Affine a1 = affine_in(fz, c + 1);
+                const float2 s2 = make_float2(a0.s, a1.s), t2 = make_float2(a0.t, a1.t);
+                with_act<FUSE == 1>(fz.in_act, [&](auto act) {
+                    constexpr int A = decltype(act)::value;
+#pragma unroll
+                    for (int i = 0; i < kMap; ++i)
+#pragma unroll
+                        for (int j = 0; j < kMap; ++j) xr[i][j] = prologue_packed<T, A>(xr[i][j], s2, t2);
+                });
+            } else {
+                with_act<FUSE == 1>(fz.in_act, [&](auto act) {
+                    constexpr int A = decltype(act)::value;
+#pragma unroll
+                    for (int i = 0; i < kMap; ++i)
+#pragma unroll
+                        for (int j = 0; j < kMap; ++j) xr[i][j] = activate(fmaf(a0.s, xr[i][j], a0.t), A);
+                });
+            }
+        }
+    }
 #pragma unroll
     for (int fh = 0; fh < F; ++fh)
 #pragma unroll
@@ -120,6 +149,24 @@ __global__ void __launch_bounds__(kSMThreads, sizeof(T) == 2 ? DWCONV_SM_FWD16_M
                     if (iw < 0 || iw >= kMap) continue;
                     L::fma(acc[ow], wr[fh][fw], xr[ih][iw]);
                 }
+        }
+        if constexpr (FUSE > 0) {
+            if (fz.post()) {
+                const Affine o0 = affine_out(fz, c);
+                const Affine o1 = L::CH == 2 ? affine_out(fz, c + 1) : o0;
+                with_act<FUSE == 1>(fz.out_act, [&](auto act) {
+                    constexpr int A = decltype(act)::value;
+#pragma unroll
+                    for (int ow = 0; ow < kMap; ++ow) {
+                        if constexpr (L::CH == 2) {
+                            acc[ow].x = activate(fmaf(o0.s, acc[ow].x, o0.t), A);
+                            acc[ow].y = activate(fmaf(o1.s, acc[ow].y, o1.t), A);
+                        } else {
+                            acc[ow] = activate(fmaf(o0.s, acc[ow], o0.t), A);
+                        }
+                    }
+                });
+            }
         }
 #pragma unroll
         for (int ow = 0; ow < kMap; ++ow) L::store(o + (oh * kMap + ow) * C, acc[ow]);
@@ -209,15 +256,17 @@ cudaError_t by_filter(int F, Fn &&fn) {
 // whole tensor, fp32 / fp16 / bf16, even channel count.
 int channels_per_cta(dwconv_dtype dt) { return dt == DWCONV_FP32 ? lanes_channels<float>() : lanes_channels<__half>(); }
 
-bool covered(const TiledConv &p, dwconv_dtype dt) {
+// The shapes the whole-map kernels take (any fusion aside).
+bool covered_shape(const TiledConv &p, dwconv_dtype dt) {
     const int F = p.FH;
     return (dt == DWCONV_FP32 || dt == DWCONV_FP16 || dt == DWCONV_BF16) && p.FW == F &&
            (F == 3 || F == 5 || F == 7) && p.pad_h == F / 2 && p.pad_w == F / 2 && p.Hs == kMap &&
            p.Ws == kMap && p.Hf == kMap && p.Wf == kMap && p.in_step_h == 1 && p.in_step_w == 1 &&
            p.in_off_h == 0 && p.in_off_w == 0 && p.OHs == kMap && p.OWs == kMap && p.OHf == kMap &&
            p.OWf == kMap && p.out_step_h == 1 && p.out_step_w == 1 && !p.zero_phases && !p.transpose &&
-           !p.fz.pre() && !p.fz.post() && p.C % 2 == 0;
+           p.C % 2 == 0;
 }
+bool covered(const TiledConv &p, dwconv_dtype dt) { return covered_shape(p, dt) && !p.fz.pre() && !p.fz.post(); }
 
 // Image ranges of the weight gradient: about two waves of CTAs over the
 // channel groups, at least one image per slot; a pure function of the shape
@@ -234,16 +283,24 @@ int wgrad_ranges(const TiledConv &p, bool launch, int *per_range) {
 }  // namespace
 
 cudaError_t launch_smallmap(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
-    if (!covered(p, dt)) return cudaErrorNotSupported;
+    if (!covered_shape(p, dt)) return cudaErrorNotSupported;
+    const bool fused = p.fz.pre() || p.fz.post();
+    if (fused && p.flip) return cudaErrorNotSupported;  // fusion is a forward-pass feature
+    const int level = !fused ? 0 : act_is_light(p.fz.in_act) && act_is_light(p.fz.out_act) ? 1 : 2;
     const int cpc = channels_per_cta(dt);
     const dim3 grid((unsigned)((p.C + cpc - 1) / cpc), (unsigned)((p.N + kSlots - 1) / kSlots));
     return by_dtype(dt, [&](auto tag) {
         using T = decltype(tag);
         return by_filter(p.FH, [&](auto f) {
             constexpr int F = decltype(f)::value;
-            smallmap_fwd_kernel<T, F><<<grid, kSMThreads, 0, st>>>(
-                static_cast<const T *>(p.in), static_cast<const T *>(p.w), p.bias, static_cast<T *>(p.out), p.N,
-                p.C, p.flip);
+            auto go = [&](auto fuse) {
+                smallmap_fwd_kernel<T, F, decltype(fuse)::value><<<grid, kSMThreads, 0, st>>>(
+                    static_cast<const T *>(p.in), static_cast<const T *>(p.w), p.bias, static_cast<T *>(p.out),
+                    p.N, p.C, p.flip, p.fz);
+            };
+            if (level == 0) go(std::integral_constant<int, 0>{});
+            else if (level == 1) go(std::integral_constant<int, 1>{});
+            else go(std::integral_constant<int, 2>{});
             note_launches(1);
             note_kernel("smallmap");
             return cudaGetLastError();

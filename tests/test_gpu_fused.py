@@ -20,7 +20,10 @@ CASES = [
     ("bf16", (3, 9, 12, 48, 3, 3, 1, 1, 1), "tiled_mma"),      # G = 2, two images per unit, odd N
     ("fp16", (2, 18, 24, 16, 31, 31, 1, 1, 15), "tiled_mma_large"),
     ("bf16", (2, 20, 40, 8, 13, 13, 1, 1, 6), "tiled_mma_large"),
-    ("bf16", (4, 7, 7, 64, 7, 7, 1, 1, 3), "tiled_small"),     # 7x7 maps: CUDA-core kernel
+    ("bf16", (4, 7, 7, 64, 7, 7, 1, 1, 3), "smallmap"),        # 7x7 maps, "same": whole-map kernel
+    ("fp16", (5, 7, 7, 40, 5, 5, 1, 1, 2), "smallmap"),        # 5 images (slots of 4), 20 channel pairs
+    ("fp32", (3, 7, 7, 96, 3, 3, 1, 1, 1), "smallmap"),        # fp32: one channel per lane
+    ("bf16", (2, 7, 7, 32, 7, 7, 1, 1, 2), "tiled_small"),     # 7x7 maps, other padding: CUDA-core kernel
     ("fp32", (2, 17, 23, 36, 7, 7, 1, 1, 3), "tiled_small"),
     ("fp32", (2, 12, 15, 32, 3, 5, 1, 1, (1, 2)), "tiled_small"),
     ("fp16", (2, 24, 24, 32, 3, 3, 2, 2, 2), "tiled_mma"),     # stride 2 dilation 2: even sub-grid
