@@ -352,9 +352,10 @@ dwconv_status fwd_impl(int N, int H, int W, int C, int FH, int FW, int stride_h,
         if (e == cudaErrorNotSupported) e = launch_tiled_large(p, dtype, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
-    // Stride 2, dilation 1 (not a unit-stride sub-grid): the strided kernel.
-    if (!fz.pre() && !fz.post() && tiled_layout_ok(s, dtype, x, y, w)) {
-        cudaError_t e = launch_strided_fwd(s, dtype, x, w, static_cast<const float *>(bias), y, cs);
+    // Stride 2, dilation 1 (not a unit-stride sub-grid): the strided kernel
+    // (plain, or with the epilogue of a fused pass).
+    if (!fz.pre() && tiled_layout_ok(s, dtype, x, y, w)) {
+        cudaError_t e = launch_strided_fwd(s, dtype, x, w, static_cast<const float *>(bias), y, fz, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
     return cuda_status(launch_fwd_direct(s, dtype, x, w, bias, y, fz, cs));

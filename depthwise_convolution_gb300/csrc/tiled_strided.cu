@@ -93,13 +93,17 @@ struct SArgs {
     const void *w;      // filter (forward, input gradient)
     const void *dy;     // weight gradient: dy
     const float *bias;  // forward, nullable
+    Fuse fz;            // forward: epilogue (affine + activation) only
     void *out;          // y, dx
     int N, H, W, C, OH, OW, PH, PW;
 };
 
 // ---------------------------------------------------------------- forward
 
-template <typename T, int F, int TH, int TW, int MINB>
+// EPI: the affine+activation epilogue of the fused forward pass (Flash-DWC
+// §5.2) on the fp32 sums -- 1: piecewise-linear activations only, 2: all;
+// 0: plain (separate instances, so the plain pass keeps its code).
+template <typename T, int F, int TH, int TW, int MINB, int EPI>
 __global__ void __launch_bounds__(kThreads, MINB)
     strided_fwd_kernel(const __grid_constant__ CUtensorMap halo_map, SArgs a, Geo g, unsigned *err) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -181,6 +185,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
         const int n = cur.group * g.NI + img_l;
         if (cvalid && n < a.N) {
+            if constexpr (EPI > 0) {
+                const Affine o0 = affine_out(a.fz, c), o1 = affine_out(a.fz, c + 1);
+                with_act<EPI == 1>(a.fz.out_act, [&](auto act) {
+                    constexpr int A = decltype(act)::value;
+#pragma unroll
+                    for (int th = 0; th < TH; ++th)
+#pragma unroll
+                        for (int tw = 0; tw < TW; ++tw) {
+                            acc[th][tw].x = activate(fmaf(o0.s, acc[th][tw].x, o0.t), A);
+                            acc[th][tw].y = activate(fmaf(o1.s, acc[th][tw].y, o1.t), A);
+                        }
+                });
+            }
             const int i0 = cur.band * tile_rows + rt * TH, jj0 = cur.twi * tile_cols + ct * TW;
             T *img = out + (long long)n * a.OH * a.OW * a.C + c;
 #pragma unroll
@@ -454,7 +471,7 @@ size_t stage_cap() {
 
 int rows_halo(int tile, int F) { return (tile - 1) * kS + F; }
 
-template <typename T, int F, int TH, int TW, int MINB>
+template <typename T, int F, int TH, int TW, int MINB, int EPI>
 cudaError_t run_fwd(const SArgs &a, dwconv_dtype dt, cudaStream_t st) {
     const Geo g = make_geo_s(a.N, a.OH, a.OW, a.C, TH, TW, kTiles, sizeof(T), 0, stage_cap<T>(),
                              [](int r) { return rows_halo(r, F); }, [](int c) { return rows_halo(c, F); });
@@ -463,7 +480,7 @@ cudaError_t run_fwd(const SArgs &a, dwconv_dtype dt, cudaStream_t st) {
     if (smem > 220 * 1024 || g.HH > 256 || g.HW > 256) return cudaErrorNotSupported;
     CUtensorMap map;
     if (!make_nhwc_map(&map, a.in, a.N, a.H, a.W, a.C, g.HH, g.HW, g.NI, dt, sizeof(T))) return cudaErrorNotSupported;
-    auto kern = strided_fwd_kernel<T, F, TH, TW, MINB>;
+    auto kern = strided_fwd_kernel<T, F, TH, TW, MINB, EPI>;
     int per_sm = 0;
     cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kThreads, smem, &per_sm);
     if (e != cudaSuccess) return e;
@@ -579,15 +596,19 @@ SArgs args_of(const Shape &s) {
 }  // namespace
 
 cudaError_t launch_strided_fwd(const Shape &s, dwconv_dtype dt, const void *x, const void *w, const float *bias,
-                               void *y, cudaStream_t st) {
-    if (!covered(s, dt)) return cudaErrorNotSupported;
+                               void *y, const Fuse &fz, cudaStream_t st) {
+    if (!covered(s, dt) || fz.pre()) return cudaErrorNotSupported;  // epilogue only
     SArgs a = args_of(s);
-    a.in = x; a.w = w; a.bias = bias; a.out = y;
+    a.in = x; a.w = w; a.bias = bias; a.out = y; a.fz = fz;
+    const int epi = !fz.post() ? 0 : act_is_light(fz.out_act) ? 1 : 2;
     return by_dtype(dt, [&](auto tag) {
         using T = decltype(tag);
         return by_filter<T>(s.FH, [&](auto f) {
             constexpr int F = decltype(f)::value;
-            return run_fwd<T, F, fwd_th<T>(), kTW, fwd_minb<T, F>()>(a, dt, st);
+            constexpr int TH = fwd_th<T>(), MB = fwd_minb<T, F>();
+            if (epi == 0) return run_fwd<T, F, TH, kTW, MB, 0>(a, dt, st);
+            if (epi == 1) return run_fwd<T, F, TH, kTW, MB, 1>(a, dt, st);
+            return run_fwd<T, F, TH, kTW, MB, 2>(a, dt, st);
         });
     });
 }
