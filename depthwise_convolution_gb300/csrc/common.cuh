@@ -408,7 +408,7 @@ cudaError_t launch_tiled_mma_large(const TiledConv &p, dwconv_dtype dt, cudaStre
 // tensors).  strided_wgrad_slices: the workspace plan (slices of the
 // accumulation axis for the workspace bound, 0 if not covered).
 cudaError_t launch_strided_fwd(const Shape &s, dwconv_dtype dt, const void *x, const void *w, const float *bias,
-                               void *y, const Fuse &fz, cudaStream_t st);  // fz: epilogue only
+                               void *y, const Fuse &fz, cudaStream_t st);
 cudaError_t launch_strided_dgrad(const Shape &s, dwconv_dtype dt, const void *dy, const void *w, void *dx,
                                  cudaStream_t st);
 int strided_wgrad_slices(const Shape &s, dwconv_dtype dt);

@@ -353,8 +353,8 @@ dwconv_status fwd_impl(int N, int H, int W, int C, int FH, int FW, int stride_h,
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }
     // Stride 2, dilation 1 (not a unit-stride sub-grid): the strided kernel
-    // (plain, or with the epilogue of a fused pass).
-    if (!fz.pre() && tiled_layout_ok(s, dtype, x, y, w)) {
+    // (plain or fused).
+    if (tiled_layout_ok(s, dtype, x, y, w)) {
         cudaError_t e = launch_strided_fwd(s, dtype, x, w, static_cast<const float *>(bias), y, fz, cs);
         if (e != cudaErrorNotSupported) return cuda_status(e);
     }

@@ -93,17 +93,18 @@ struct SArgs {
     const void *w;      // filter (forward, input gradient)
     const void *dy;     // weight gradient: dy
     const float *bias;  // forward, nullable
-    Fuse fz;            // forward: epilogue (affine + activation) only
+    Fuse fz;            // forward: BN+Act prologue, affine+activation epilogue
     void *out;          // y, dx
     int N, H, W, C, OH, OW, PH, PW;
 };
 
 // ---------------------------------------------------------------- forward
 
-// EPI: the affine+activation epilogue of the fused forward pass (Flash-DWC
-// §5.2) on the fp32 sums -- 1: piecewise-linear activations only, 2: all;
+// FUSE: the fused forward pass (Flash-DWC §5.2) -- the BN+Act prologue on the
+// staged halo (in place, padding kept zero) and the affine+activation
+// epilogue on the fp32 sums; 1: piecewise-linear activations only, 2: all;
 // 0: plain (separate instances, so the plain pass keeps its code).
-template <typename T, int F, int TH, int TW, int MINB, int EPI>
+template <typename T, int F, int TH, int TW, int MINB, int FUSE>
 __global__ void __launch_bounds__(kThreads, MINB)
     strided_fwd_kernel(const __grid_constant__ CUtensorMap halo_map, SArgs a, Geo g, unsigned *err) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -152,6 +153,50 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const Unit cur = decode(g, u);
         const int c = cur.ctile * 32 + 2 * cp;
         const bool cvalid = c < a.C;
+        if constexpr (FUSE > 0) {
+            if (a.fz.pre()) {
+                // BN+Act prologue once per staged value, in place: thread (cp, t)
+                // takes channel pair cp of every kTiles-th halo row.  Positions
+                // outside the input are padding of x' and stay zero; x' is
+                // rounded to T as the unfused layer would store it.
+                T *hbuf = reinterpret_cast<T *>(smem_raw + (k & 1) * buf_stride);
+                const Affine a0 = cvalid ? affine_in(a.fz, c) : Affine{1.f, 0.f};
+                const Affine a1 = cvalid ? affine_in(a.fz, c + 1) : Affine{1.f, 0.f};
+                const float2 s2 = make_float2(a0.s, a1.s), t2 = make_float2(a0.t, a1.t);
+                // Halo columns [c_lo, c_hi) lie inside the input.
+                const int col_in = cur.twi * tile_cols * kS - a.PW;
+                const int c_lo = min(max(-col_in, 0), g.HW), c_hi = max(min(a.W - col_in, g.HW), c_lo);
+                with_act<FUSE == 1>(a.fz.in_act, [&](auto act) {
+                    [[maybe_unused]] constexpr int A = decltype(act)::value;
+#pragma unroll 1
+                    for (int rr = t; rr < g.NI * g.HH; rr += kTiles) {
+                        const int im = rr / g.HH, r = rr - im * g.HH;
+                        const int ih = cur.band * tile_rows * kS - a.PH + r;
+                        const bool rok = ih >= 0 && ih < a.H && cur.group * g.NI + im < a.N;
+                        T *row = hbuf + rr * g.HW * 32 + 2 * cp;
+                        const int lo = rok ? c_lo : g.HW, hi = rok ? c_hi : g.HW;
+#pragma unroll 1
+                        for (int col = 0; col < lo; ++col) Pair<T>::store(row + col * 32, make_float2(0.f, 0.f));
+#pragma unroll 4
+                        for (int col = lo; col < hi; ++col) {
+                            if constexpr (sizeof(T) == 4) {
+                                float2 *q = reinterpret_cast<float2 *>(row + col * 32);
+                                *q = prologue_f32<A>(*q, s2, t2);
+                            } else {
+                                unsigned *q = reinterpret_cast<unsigned *>(row + col * 32);
+                                *q = prologue_packed<T, A>(*q, s2, t2);
+                            }
+                        }
+#pragma unroll 1
+                        for (int col = hi; col < g.HW; ++col) Pair<T>::store(row + col * 32, make_float2(0.f, 0.f));
+                    }
+                });
+                // The generic-proxy writes come before this buffer's next TMA
+                // fill; every thread sees the whole transformed halo.
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                __syncthreads();
+            }
+        }
         if (cur.ctile != loaded_ctile) {
             loaded_ctile = cur.ctile;
 #pragma unroll
@@ -185,9 +230,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
         const int n = cur.group * g.NI + img_l;
         if (cvalid && n < a.N) {
-            if constexpr (EPI > 0) {
+            if (FUSE > 0 && a.fz.post()) {
                 const Affine o0 = affine_out(a.fz, c), o1 = affine_out(a.fz, c + 1);
-                with_act<EPI == 1>(a.fz.out_act, [&](auto act) {
+                with_act<FUSE == 1>(a.fz.out_act, [&](auto act) {
                     constexpr int A = decltype(act)::value;
 #pragma unroll
                     for (int th = 0; th < TH; ++th)
@@ -471,7 +516,7 @@ size_t stage_cap() {
 
 int rows_halo(int tile, int F) { return (tile - 1) * kS + F; }
 
-template <typename T, int F, int TH, int TW, int MINB, int EPI>
+template <typename T, int F, int TH, int TW, int MINB, int FUSE>
 cudaError_t run_fwd(const SArgs &a, dwconv_dtype dt, cudaStream_t st) {
     const Geo g = make_geo_s(a.N, a.OH, a.OW, a.C, TH, TW, kTiles, sizeof(T), 0, stage_cap<T>(),
                              [](int r) { return rows_halo(r, F); }, [](int c) { return rows_halo(c, F); });
@@ -480,7 +525,7 @@ cudaError_t run_fwd(const SArgs &a, dwconv_dtype dt, cudaStream_t st) {
     if (smem > 220 * 1024 || g.HH > 256 || g.HW > 256) return cudaErrorNotSupported;
     CUtensorMap map;
     if (!make_nhwc_map(&map, a.in, a.N, a.H, a.W, a.C, g.HH, g.HW, g.NI, dt, sizeof(T))) return cudaErrorNotSupported;
-    auto kern = strided_fwd_kernel<T, F, TH, TW, MINB, EPI>;
+    auto kern = strided_fwd_kernel<T, F, TH, TW, MINB, FUSE>;
     int per_sm = 0;
     cudaError_t e = kernel_setup(reinterpret_cast<const void *>(kern), kThreads, smem, &per_sm);
     if (e != cudaSuccess) return e;
@@ -597,10 +642,10 @@ SArgs args_of(const Shape &s) {
 
 cudaError_t launch_strided_fwd(const Shape &s, dwconv_dtype dt, const void *x, const void *w, const float *bias,
                                void *y, const Fuse &fz, cudaStream_t st) {
-    if (!covered(s, dt) || fz.pre()) return cudaErrorNotSupported;  // epilogue only
+    if (!covered(s, dt)) return cudaErrorNotSupported;
     SArgs a = args_of(s);
     a.in = x; a.w = w; a.bias = bias; a.out = y; a.fz = fz;
-    const int epi = !fz.post() ? 0 : act_is_light(fz.out_act) ? 1 : 2;
+    const int epi = !fz.pre() && !fz.post() ? 0 : act_is_light(fz.in_act) && act_is_light(fz.out_act) ? 1 : 2;
     return by_dtype(dt, [&](auto tag) {
         using T = decltype(tag);
         return by_filter<T>(s.FH, [&](auto f) {

@@ -27,15 +27,14 @@ CASES = [
     ("fp32", (2, 17, 23, 36, 7, 7, 1, 1, 3), "tiled_small"),
     ("fp32", (2, 12, 15, 32, 3, 5, 1, 1, (1, 2)), "tiled_small"),
     ("fp16", (2, 24, 24, 32, 3, 3, 2, 2, 2), "tiled_mma"),     # stride 2 dilation 2: even sub-grid
-    ("fp32", (2, 13, 13, 12, 3, 3, 2, 1, 1), "direct_fwd"),    # stride 2 + prologue: direct kernel
-    ("bf16", (3, 29, 30, 64, 7, 7, 2, 1, 3), "direct_fwd"),    # stride 2, 7x7
+    ("fp32", (2, 13, 13, 12, 3, 3, 2, 1, 1), "strided_fwd"),   # stride 2: the strided kernel
+    ("bf16", (3, 29, 30, 64, 7, 7, 2, 1, 3), "strided_fwd"),   # stride 2, 7x7, ragged tiles
+    ("fp16", (2, 16, 21, 32, 5, 5, 2, 1, (2, 1)), "strided_fwd"),  # stride 2, unequal padding
     ("bf16", (1, 9, 11, 5, 3, 3, 1, 1, 1), "direct_fwd"),      # odd C: direct kernel
     ("fp32", (1, 20, 24, 32, 9, 9, 1, 1, 4), "direct_fwd"),    # large filter + prologue: direct
 ]
 # epilogue-only families where they differ from the prologue ones
-POST_ONLY = {("fp32", (1, 20, 24, 32, 9, 9, 1, 1, 4)): "tiled_large",
-             ("fp32", (2, 13, 13, 12, 3, 3, 2, 1, 1)): "strided_fwd",   # the stride-2 kernel's epilogue
-             ("bf16", (3, 29, 30, 64, 7, 7, 2, 1, 3)): "strided_fwd"}
+POST_ONLY = {("fp32", (1, 20, 24, 32, 9, 9, 1, 1, 4)): "tiled_large"}
 
 ACTS = ["relu", "relu6", "silu", "gelu"]
 
