@@ -47,7 +47,7 @@ DEFAULT_WORKLOAD = "fp16-train-7x7-128x56x56x96"
 METRIC = "DWC fwd/dgrad/wgrad GFLOP/s and HBM GB/s as % of roofline on 1xGB300"
 L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2, written (then another buffer read) between timed steps
 FMA_LANES_PER_SM = 128              # fp32 FMA units per SM on Blackwell
-TENSOR_KERNELS = {"tiled_mma", "tiled_mma_large", "tiled_mma_wgrad"}   # kernel families on the tensor pipe
+TENSOR_KERNELS = {"tiled_mma", "tiled_mma_ring", "tiled_mma_large", "tiled_mma_wgrad"}   # kernel families on the tensor pipe
 
 
 # ----------------------------------------------------------------- helpers

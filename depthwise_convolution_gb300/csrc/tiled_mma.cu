@@ -1,9 +1,10 @@
 // Tensor-core forward pass and stride-1 input gradient for 16-bit data and
 // 3x3, 5x5 and 7x7 filters: shape rules and the launcher of the plain passes.
 // The kernel (Flash-DWC §4.2 Toeplitz packing on mma.sync) is in
-// tiled_mma_kernel.cuh; the fused forward pass has its own instances in
-// tiled_mma_fused.cu.
-#include "tiled_mma_kernel.cuh"
+// tiled_mma_kernel.cuh, its warp-specialised form for maps wider than 32
+// columns in tiled_mma_ring_kernel.cuh; the fused forward pass has its own
+// instances in tiled_mma_fused.cu.
+#include "tiled_mma_ring_kernel.cuh"
 
 namespace dwc {
 
@@ -21,8 +22,8 @@ cudaError_t launch_tiled_mma(const TiledConv &p, dwconv_dtype dt, cudaStream_t s
     if (!DWCONV_MMA || p.zero_phases) return cudaErrorNotSupported;
     if (p.fz.pre() || p.fz.post()) return launch_tiled_mma_fused(p, dt, st);
     switch (dt) {
-        case DWCONV_FP16: return by_filter<__half, false>(p, dt, st);
-        case DWCONV_BF16: return by_filter<__nv_bfloat16, false>(p, dt, st);
+        case DWCONV_FP16: return by_filter_plain<__half>(p, dt, st);
+        case DWCONV_BF16: return by_filter_plain<__nv_bfloat16>(p, dt, st);
         case DWCONV_FP8_E4M3: return p.flip ? cudaErrorNotSupported : by_filter<__nv_fp8_e4m3, false>(p, dt, st);
         default: return cudaErrorNotSupported;
     }

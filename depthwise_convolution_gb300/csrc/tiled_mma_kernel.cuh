@@ -512,6 +512,18 @@ __global__ void __launch_bounds__(kMThreads, (Cfg<FH, G, NI, KNB, in_es<T>()>::M
     if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
 }
 
+// Halo map as for the CUDA-core kernels (box: 32 channels x columns x rows x
+// images), with the 64-byte swizzle for 16-bit data (the inner box row is
+// exactly one 32-channel pixel).
+inline bool make_mma_halo_map(CUtensorMap *map, const TiledConv &p, dwconv_dtype dt, size_t es, const uint32_t box[4],
+                              int swizzle) {
+    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off_h * p.Wf + p.in_off_w) * p.C * es;
+    const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
+    const uint64_t str[3] = {(uint64_t)p.in_step_w * p.C * es, (uint64_t)p.in_step_h * p.Wf * p.C * es,
+                             (uint64_t)p.Hf * p.Wf * p.C * es};
+    return encode_tmap_4d(map, dt, base, dims, str, box, swizzle);
+}
+
 template <typename T, int FH, int FW, int G, int NI, int KNB, bool FUSE>
 cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     using C = Cfg<FH, G, NI, KNB, in_es<T>()>;
@@ -525,21 +537,15 @@ cudaError_t run(const TiledConv &p, dwconv_dtype dt, cudaStream_t st) {
     if (units >= (1LL << 30)) return cudaErrorNotSupported;
     g.per_ctile = (int)per;
     g.units = (int)units;
-    // Halo map as for the CUDA-core kernels, NI images per box, 64-byte
-    // swizzle (the inner box row is exactly one 32-channel pixel).  The output
-    // map covers y (or dx) directly; the TMA store clips the tile at the edges.
-    const size_t es = sizeof(T);
-    const char *base = static_cast<const char *>(p.in) + ((size_t)p.in_off_h * p.Wf + p.in_off_w) * p.C * es;
-    const uint64_t dims[4] = {(uint64_t)p.C, (uint64_t)p.Ws, (uint64_t)p.Hs, (uint64_t)p.N};
-    const uint64_t str[3] = {(uint64_t)p.in_step_w * p.C * es, (uint64_t)p.in_step_h * p.Wf * p.C * es,
-                             (uint64_t)p.Hf * p.Wf * p.C * es};
+    // The output map covers y (or dx) directly; the TMA store clips the tile
+    // at the edges.
     const uint32_t box[4] = {(uint32_t)kCh, (uint32_t)C::SW, (uint32_t)C::HRI, (uint32_t)NI};
     const uint32_t obox[4] = {(uint32_t)kCh, (uint32_t)C::OTW, (uint32_t)C::OTH, (uint32_t)NI};
     CUtensorMap map, omap;
     // FP8: the halo is staged unswizzled (32-byte pixels) and gathered bytewise;
     // the output is bf16.
     const dwconv_dtype out_dt = dt == DWCONV_FP8_E4M3 ? DWCONV_BF16 : dt;
-    if (!encode_tmap_4d(&map, dt, base, dims, str, box, sizeof(T) == 1 ? 0 : kPB) ||
+    if (!make_mma_halo_map(&map, p, dt, sizeof(T), box, sizeof(T) == 1 ? 0 : kPB) ||
         !make_out_map(&omap, p, out_dt, sizeof(typename OutOf<T>::type), obox, kPB))
         return cudaErrorNotSupported;
     auto kern = tiled_mma_kernel<T, FH, FW, G, NI, KNB, FUSE>;

@@ -45,7 +45,7 @@ def test_16bit_training_passes_beyond_2_31_elements():
 
     x = _repeat(d["x"].cuda(), N)
     y = ops.dwconv_fwd(x, w, None, S, D, P)
-    assert ops.dwconv_last_kernel() == "tiled_mma"
+    assert ops.dwconv_last_kernel() == "tiled_mma_ring"
     ops.dwconv_check_device_errors()
     for n in imgs:
         ref, mag = oracle.fwd(to64(d["x"][n % B:n % B + 1]), to64(d["w"]), None, S, D, P)
@@ -54,7 +54,7 @@ def test_16bit_training_passes_beyond_2_31_elements():
 
     dy = _repeat(d["dy"].cuda(), N)
     dx = ops.dwconv_bwd_data(dy, w, H, W, S, D, P)
-    assert ops.dwconv_last_kernel() == "tiled_mma"
+    assert ops.dwconv_last_kernel() == "tiled_mma_ring"
     ops.dwconv_check_device_errors()
     for n in imgs:
         ref, mag = oracle.dgrad(to64(d["dy"][n % B:n % B + 1]), to64(d["w"]), H, W, S, D, P)

@@ -163,8 +163,10 @@ def test_zero_input_gives_bias_only():
 
 
 @pytest.mark.parametrize("dtype,case,pass_name,family", [
-    ("fp16", (2, 40, 40, 32, 7, 7, 1, 1, 3), "fwd", "tiled_mma"),
-    ("bf16", (2, 40, 40, 32, 7, 7, 1, 1, 3), "dgrad", "tiled_mma"),
+    ("fp16", (2, 40, 40, 32, 7, 7, 1, 1, 3), "fwd", "tiled_mma_ring"),
+    ("bf16", (2, 40, 40, 32, 7, 7, 1, 1, 3), "dgrad", "tiled_mma_ring"),
+    ("bf16", (2, 40, 40, 32, 3, 3, 1, 1, 1), "fwd", "tiled_mma"),
+    ("fp16", (2, 30, 30, 32, 7, 7, 1, 1, 3), "fwd", "tiled_mma"),
     ("bf16", (1, 40, 40, 32, 31, 31, 1, 1, 15), "fwd", "tiled_mma_large"),
     ("fp32", (2, 40, 40, 32, 7, 7, 1, 1, 3), "fwd", "tiled_small"),
     ("fp32", (1, 30, 30, 32, 15, 15, 1, 1, 7), "fwd", "tiled_large"),
